@@ -1,0 +1,462 @@
+"""Pins that tie the CPU oracle to facts fixed by the pages and by mathematics.
+
+Each ``check_*`` function takes an oracle module (the real one, or a copy with a planted mistake)
+and raises AssertionError when the oracle disagrees with a pinned fact.  The expected values come
+from the pages' worked examples (tests/golden/), closed forms, hand-worked quantiser cases, brute
+force on tiny inputs and mathematical bounds -- never from the oracle's own formulas retyped.
+"""
+from __future__ import annotations
+
+import json
+import os
+from itertools import product
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "sd_tutorial_examples.json")
+
+
+def golden():
+    with open(GOLDEN, encoding="utf-8") as f:
+        return json.load(f)
+
+
+def bf16_bits(values):
+    """Bit patterns of values that are exactly representable in bf16 (checked)."""
+    v = np.asarray(values, dtype=np.float32)
+    bits = (v.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    back = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    assert np.array_equal(back, v), "test value not exactly representable in bf16"
+    return bits
+
+
+# ---------------------------------------------------------------- a1: weight quantiser / packer
+
+def check_pack_layout(o):
+    # byte j holds k = 2j in bits 0..3 and k = 2j+1 in bits 4..7, two's complement
+    codes = np.array([[1, -2, 7, -8, 0, -1, 3, 4]], dtype=np.int8)
+    assert o.pack_codes(codes).tolist() == [[0xE1, 0x87, 0xF0, 0x43]]
+    # every byte value round-trips through unpack / pack
+    allb = np.arange(256, dtype=np.uint8).reshape(1, 256)
+    c = o.unpack_codes(allb)
+    assert c.min() == -8 and c.max() == 7
+    assert c[0, 2 * 0x9F] == -1 and c[0, 2 * 0x9F + 1] == -7  # 0x9F: low nibble F (-1), high 9 (-7)
+    assert np.array_equal(o.pack_codes(c), allb)
+
+
+def check_weight_grid_roundtrip(o):
+    # W exactly on the grid code * s with s a power of two and +-7 present: codes and scales recovered
+    rng = np.random.default_rng(11)
+    N, K = 6, 512
+    G = K // 128
+    s = 2.0 ** rng.integers(-12, -2, size=(N, G))
+    c = rng.integers(-7, 8, size=(N, K))
+    for n in range(N):
+        for g in range(G):
+            c[n, g * 128] = 7 if (n + g) % 2 else -7
+    c[0, 0:15] = np.arange(-7, 8)  # every producible code
+    W = (c * np.repeat(s, 128, axis=1)).astype(np.float32)
+    codes, S = o.quantize_weights(bf16_bits(W))
+    assert S.dtype == np.float16
+    assert np.array_equal(S.astype(np.float64), s)
+    assert np.array_equal(codes.astype(np.int64), c)
+
+
+def check_weight_hand_cases(o):
+    def quant(group_values):
+        row = np.zeros(128, dtype=np.float32)
+        row[: len(group_values)] = group_values
+        codes, S = o.quantize_weights(bf16_bits(row[None, :]))
+        return codes[0, : len(group_values)].tolist(), float(S[0, 0])
+
+    # amax 7 -> s = 1: ties go to even, 5 stays 5 (a divisor of 8 would give 6)
+    codes, s = quant([7.0, 2.5, 3.5, -2.5, 5.0, 0.5, 1.5, -7.0, -0.5])
+    assert s == 1.0
+    assert codes == [7, 2, 4, -2, 5, 0, 2, -7, 0]
+    # amax 1: fp16(1/7) = 0.142822265625; 0.5 / that = 3.5008... -> 4.  (The fp32 scale 1/7 would
+    # give 0.5 / 0.14285715 = 3.4999998 -> 3: the scale must be rounded to fp16 first.)
+    codes, s = quant([1.0, 0.5, -0.5])
+    assert s == 0.142822265625
+    assert codes == [7, 4, -4]
+    # fp16-subnormal scale: amax = 7 * 2^-20 -> s = 2^-20 (subnormal in fp16, exact)
+    t = 2.0 ** -20
+    codes, s = quant([7 * t, 3 * t, -5 * t])
+    assert s == t and codes == [7, 3, -5]
+    # scale underflows to 0 in fp16 (2^-26 < half the smallest subnormal) -> all codes 0
+    t = 2.0 ** -26
+    codes, s = quant([7 * t, 3 * t])
+    assert s == 0.0 and codes == [0, 0]
+    # all-zero group
+    codes, s = quant([0.0, 0.0])
+    assert s == 0.0 and codes == [0, 0]
+
+
+def check_pack_end_to_end(o):
+    # pack_weights = quantise + nibble layout, on a hand case
+    row = np.zeros((1, 128), dtype=np.float32)
+    row[0, :4] = [7.0, -1.0, 2.0, -7.0]
+    Wp, S = o.pack_weights(bf16_bits(row))
+    assert Wp.shape == (1, 64) and S.shape == (1, 1)
+    assert Wp[0, 0] == 0xF7 and Wp[0, 1] == 0x92 and float(S[0, 0]) == 1.0
+
+
+# ---------------------------------------------------------------- a2: W4A16
+
+def check_w4a16_onehot_and_grid(o):
+    rng = np.random.default_rng(5)
+    N, K = 40, 256
+    s = 2.0 ** rng.integers(-8, -3, size=(N, K // 128))
+    c = rng.integers(-7, 8, size=(N, K))
+    c[:, 0] = 7
+    c[:, 128] = -7
+    W = (c * np.repeat(s, 128, axis=1)).astype(np.float32)
+    Wp, S = o.pack_weights(bf16_bits(W))
+    # one-hot activations select one input column of W (exactly)
+    for k in [0, 1, 77, 128, 200, 255]:
+        x = np.zeros((1, K), dtype=np.float32)
+        x[0, k] = 1.0
+        y = o.linear_w4a16(bf16_bits(x), Wp, S)
+        assert y.shape == (1, N)
+        assert np.array_equal(y[0], W[:, k].astype(np.float64))
+    # on-grid weights: the W4A16 product equals the plain product with W
+    x = rng.integers(-64, 64, size=(3, K)).astype(np.float32) / 16
+    y = o.linear_w4a16(bf16_bits(x), Wp, S)
+    ref = x.astype(np.float64) @ W.astype(np.float64).T
+    assert np.allclose(y, ref, rtol=0, atol=1e-12)
+    # a subset of output rows
+    rows = np.array([3, 17, 39])
+    assert np.allclose(o.linear_w4a16(bf16_bits(x), Wp, S, rows=rows), ref[:, rows], rtol=0, atol=1e-12)
+
+
+def check_w4a16_error_bound(o):
+    # |y - x W^T| <= sum_k |x_k| * s_{n,g(k)} / 2  (each weight moves at most half a step)
+    rng = np.random.default_rng(6)
+    N, K, M = 24, 384, 4
+    Wf = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    Wb = bf16_bits((Wf.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32))
+    Wv = (Wb.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    xf = rng.standard_normal((M, K)).astype(np.float32)
+    xb = bf16_bits((xf.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32))
+    xv = (xb.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    Wp, S = o.pack_weights(Wb)
+    y = o.linear_w4a16(xb, Wp, S)
+    exact = xv @ Wv.T
+    s_full = np.repeat(S.astype(np.float64), 128, axis=1)        # [N, K]
+    # the half-step bound uses the fp16-rounded scale; amax/fp16(amax/7) can exceed 7 by a rounding
+    # margin, so allow the clamp's extra fraction of a step for the largest weights
+    bound = np.abs(xv) @ (s_full * 0.5 * (1 + 2.0 ** -9)).T + 1e-12
+    assert np.all(np.abs(y - exact) <= bound)
+    # and the bound is not vacuous: the error is a small fraction of the output scale
+    assert np.linalg.norm(y - exact) < 0.2 * np.linalg.norm(exact)
+
+
+# ---------------------------------------------------------------- a3: activation quantiser
+
+def check_act_quant_hand_cases(o):
+    x = np.zeros((3, 128), dtype=np.float32)
+    x[0, :8] = [7.0, 3.5, -3.5, 2.5, 0.0, -7.0, 0.5, 1.5]
+    x[1, :3] = [1.0, 0.5, -0.5]           # fp32 scale 1/7: 0.5 / 0.14285715 = 3.4999998 -> 3
+    qa, s_a = o.quantize_activations(bf16_bits(x))
+    assert s_a.dtype == np.float32
+    assert s_a[0] == 1.0
+    assert qa[0, :8].tolist() == [7, 4, -4, 2, 0, -7, 0, 2]
+    assert s_a[1] == np.float32(1.0) / np.float32(7.0)
+    assert qa[1, :3].tolist() == [7, 3, -3]
+    assert s_a[2] == 0.0 and not qa[2].any()       # all-zero token
+    # an outlier channel takes the scale: codes +-7 there, everything below s/2 rounds to 0
+    y = np.zeros((1, 256), dtype=np.float32)
+    y[0, 10] = -140.0
+    y[0, 20:30] = 9.0
+    y[0, 30:40] = 11.0
+    qa, s_a = o.quantize_activations(bf16_bits(y))
+    assert s_a[0] == 20.0 and qa[0, 10] == -7
+    assert not qa[0, 20:30].any() and (qa[0, 30:40] == 1).all()
+
+
+# ---------------------------------------------------------------- a4: W4A4
+
+def check_w4a4_bruteforce(o):
+    rng = np.random.default_rng(7)
+    M, N, K = 3, 5, 256
+    x = rng.integers(-40, 41, size=(M, K)).astype(np.float32) / 4
+    W = rng.integers(-7, 8, size=(N, K)).astype(np.float32) / 64
+    W[:, 0] = 7 / 64
+    W[:, 128] = -7 / 64
+    Wp, S = o.pack_weights(bf16_bits(W))
+    r = o.linear_w4a4(bf16_bits(x), Wp, S)
+    qa, s_a = r["qa"], r["s_a"]
+    wc = np.rint(W * 64).astype(np.int64)          # on-grid weights: codes are W * 64
+    for m in range(M):
+        for n in range(N):
+            for g in range(2):
+                total = 0
+                for k in range(128 * g, 128 * g + 128):
+                    total += int(qa[m, k]) * int(wc[n, k])
+                assert r["acc"][m, n, g] == total
+    assert r["acc"].dtype == np.int32
+    # y equals the plain fp64 product of the dequantised activations and dequantised weights
+    xa = qa.astype(np.float64) * s_a.astype(np.float64)[:, None]
+    ref = xa @ o.dequantize_weights(Wp, S).T
+    assert np.allclose(r["y"], ref, rtol=1e-12, atol=0)
+
+
+def check_w4a4_extremes(o):
+    # every pair of the 16 codes, including -8 which the packer never produces but kernels accept
+    ca = np.repeat(np.arange(-8, 8), 16)             # [256]
+    cw = np.tile(np.arange(-8, 8), 16)
+    Wp = o.pack_codes(cw[None, :].astype(np.int8))
+    acc = o.w4a4_group_sums(ca[None, :].astype(np.int8), Wp)
+    # sum over all pairs of (a * w) for a, w in [-8, 7]: (sum a)(sum w) split per group of 128
+    # group 0 holds a in [-8, -1], group 1 holds a in [0, 7]; each with the full w range (sum -8)
+    assert acc.shape == (1, 1, 2)
+    assert acc[0, 0, 0] == 288     # (sum_{a=-8..-1} a) * (sum_{w=-8..7} w) = (-36) * (-8)
+    assert acc[0, 0, 1] == -224    # (sum_{a=0..7} a) * (sum_{w=-8..7} w) = 28 * (-8)
+    # largest magnitude group: 128 products of (-8)(-8)
+    big = o.w4a4_group_sums(np.full((1, 128), -8, np.int8), o.pack_codes(np.full((1, 128), -8, np.int8)))
+    assert big[0, 0, 0] == 8192
+
+
+def check_w4a4_constant_activation(o):
+    # x constant c > 0: s_a = c / 7 and every code is 7, so y = c * sum_k w_k (on-grid weights)
+    rng = np.random.default_rng(8)
+    N, K = 7, 256
+    W = rng.integers(-7, 8, size=(N, K)).astype(np.float32) / 32
+    W[:, 0] = 7 / 32
+    W[:, 128] = -7 / 32
+    Wp, S = o.pack_weights(bf16_bits(W))
+    x = np.full((2, K), 3.5, dtype=np.float32)
+    r = o.linear_w4a4(bf16_bits(x), Wp, S)
+    assert (r["qa"] == 7).all()
+    assert np.allclose(r["y"][0], 3.5 * W.astype(np.float64).sum(axis=1), rtol=1e-6, atol=1e-9)
+
+
+# ---------------------------------------------------------------- a5: softmax
+
+def check_softmax(o):
+    p = o.softmax(np.array([1.0, 0.0]))
+    assert abs(p[0] - 1 / (1 + np.exp(-1.0))) < 1e-15
+    assert np.allclose(o.softmax(np.zeros(7)), np.full(7, 1 / 7), rtol=0, atol=1e-15)
+    p = o.softmax(np.array([-np.inf, 2.0, -np.inf, 2.0]))
+    assert p.tolist() == [0.0, 0.5, 0.0, 0.5]
+    p = o.softmax(np.array([1000.0, 0.0]))
+    assert p[0] == 1.0 and 0 <= p[1] < 1e-300
+    # rows are independent along the last axis
+    q = o.softmax(np.array([[0.0, np.log(3.0)], [np.log(4.0), 0.0]]))
+    assert np.allclose(q, [[0.25, 0.75], [0.8, 0.2]], rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------- a6: greedy verify
+
+def _onehot_logits(argmaxes, V):
+    """bf16 bits [B, G1, V]: 0 everywhere, 1 at each given argmax."""
+    a = np.asarray(argmaxes)
+    L = np.zeros(a.shape + (V,), dtype=np.float32)
+    for idx in np.ndindex(a.shape):
+        L[idx + (a[idx],)] = 1.0
+    return bf16_bits(L)
+
+
+def check_greedy_tutorial_example(o):
+    g = golden()["greedy_example"]
+    d = np.array([g["draft_tokens"]])
+    t = g["target_argmax_first4"] + [0]           # next-position argmax, unused here
+    n, out, targ = o.verify_greedy(_onehot_logits([t], 8), d)
+    assert n[0] == g["accepted"]
+    emitted = [int(v) for v in out[0] if v >= 0]
+    assert emitted == g["emitted"]
+    assert out[0].tolist() == g["emitted"] + [-1, -1]
+    # all four match: gamma + 1 tokens
+    n, out, _ = o.verify_greedy(_onehot_logits([[1, 2, 3, 4, 6]], 8), d)
+    assert n[0] == 4 and len([v for v in out[0] if v >= 0]) == g["max_tokens_if_all_match"]
+    assert out[0].tolist() == [1, 2, 3, 4, 6]
+
+
+def check_greedy_bruteforce(o):
+    V = 3
+    for gamma in (1, 2, 3):
+        for targ in product(range(V), repeat=gamma + 1):
+            L = _onehot_logits([list(targ)], V)
+            for d in product(range(V), repeat=gamma):
+                n, out, t = o.verify_greedy(L, np.array([d]))
+                pre = os.path.commonprefix([list(d), list(targ[:gamma])])
+                assert n[0] == len(pre)
+                assert list(t[0]) == list(targ)
+                assert out[0].tolist() == list(d[: len(pre)]) + [targ[len(pre)]] + [-1] * (gamma - len(pre))
+
+
+def check_greedy_ties(o):
+    L = np.zeros((1, 3, 6), dtype=np.float32)
+    L[0, 0] = [0, 3, 1, 3, 3, 2]        # tie at 1, 3, 4 -> 1
+    L[0, 1] = [-0.0, 0.0, -1, -2, 0.0, -0.0]  # +0 and -0 equal -> 0
+    L[0, 2] = [-np.inf] * 5 + [-5.0]    # single finite value
+    n, out, t = o.verify_greedy(bf16_bits(L), np.array([[1, 0]]))
+    assert t[0].tolist() == [1, 0, 5]
+    assert n[0] == 2 and out[0].tolist() == [1, 0, 5]
+
+
+def _toy_logits(prefix, V, salt):
+    """Deterministic pseudo-model: logits depend only on the prefix (and a salt)."""
+    h = 1469598103934665603
+    for tok in prefix:
+        h = ((h ^ (int(tok) + 1)) * 1099511628211) & ((1 << 63) - 1)
+    rng = np.random.default_rng([h, salt])
+    l = rng.standard_normal(V).astype(np.float32)
+    l[rng.integers(0, V)] += rng.uniform(1.0, 4.0)
+    return l
+
+
+def check_greedy_equivalence(o):
+    # greedy speculative decoding emits exactly target-only greedy decoding
+    V, gamma, L = 40, 3, 60
+    def target(prefix):
+        return _toy_logits(prefix, V, 0)
+    def draft(prefix):
+        return target(prefix) + 0.8 * _toy_logits(prefix, V, 1)
+    def bits(l):
+        return ((l.astype(np.float32).view(np.uint32) + np.uint32(0x8000)) >> np.uint32(16)).astype(np.uint16)
+    def val(b):
+        return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+    ref = [7]
+    while len(ref) < L + 1:
+        v = val(bits(target(ref)))
+        ref.append(int(np.flatnonzero(v == v.max())[0]))
+    seq = [7]
+    accepted = 0
+    calls = 0
+    while len(seq) < L + 1:
+        d = []
+        for _ in range(gamma):
+            v = val(bits(draft(seq + d)))
+            d.append(int(np.flatnonzero(v == v.max())[0]))
+        rows = np.stack([bits(target(seq + d[:i])) for i in range(gamma + 1)])[None]
+        n, out, _ = o.verify_greedy(rows, np.array([d]))
+        seq += [int(v) for v in out[0] if v >= 0]
+        accepted += int(n[0])
+        calls += 1
+    assert seq[: L + 1] == ref
+    assert accepted > 0 and calls < L  # the draft is useful in this toy setup
+
+
+# ---------------------------------------------------------------- a7, a8: sampling verify
+
+def check_sampling_worked_example(o):
+    g = golden()["three_token_example"]
+    p = np.array(g["p_target"])
+    q = np.array(g["q_draft"])
+    x = g["draft_token"]
+    P = np.stack([p, p])             # rows: draft position 0, bonus position
+    Q = q[None, :]
+    r = o.verify_sample_probs(P, Q, [x], [0.0], [0.5, 0.5])
+    assert abs(r["a"][0] - g["accept_prob"]) < 1e-15
+    assert abs(q[x] * r["a"][0] - g["p_proposed_and_accepted"]) < 1e-15
+    # proposing B, which the target rates higher than the draft (0.5 > 0.4), is always accepted
+    rb = o.verify_sample_probs(P, Q, [1], [0.999], [0.0, 0.0])
+    assert rb["a"][0] == 1.0 and rb["n"] == 1
+    # rejection (u >= a) always resamples B from the residual (0, 0.1, 0)
+    for u_res in np.linspace(0.0, 0.999, 37):
+        r = o.verify_sample_probs(P, Q, [x], [0.8], [u_res, 0.0])
+        assert r["n"] == 0 and r["j"] == g["residual_choice"]
+        assert np.allclose(r["residual"], g["residual_unnormalised"], atol=1e-15)
+        assert r["out"].tolist() == [g["residual_choice"], -1]
+    # the test is strict: u == a rejects, u just below accepts and then takes the bonus token
+    # (binary fractions so that a = 0.375 / 0.5 = 0.75 exactly)
+    P2 = np.array([[0.375, 0.375, 0.25], [0.25, 0.5, 0.25]])
+    Q2 = np.array([[0.5, 0.25, 0.25]])
+    r = o.verify_sample_probs(P2, Q2, [0], [0.75], [0.0, 0.0])
+    assert r["a"][0] == 0.75 and r["n"] == 0
+    r = o.verify_sample_probs(P2, Q2, [0], [np.nextafter(0.75, 0)], [0.0, 0.3])
+    assert r["n"] == 1 and r["out"].tolist() == [0, 1]
+
+
+def check_sampling_exact_marginal(o):
+    # Integrating over the draft token x ~ q and both uniforms, out[0] is distributed as p_0.
+    grid = (np.arange(4000) + 0.5) / 4000
+    cases = [(np.array([0.3, 0.5, 0.2]), np.array([0.4, 0.4, 0.2]))]
+    rng = np.random.default_rng(9)
+    for _ in range(3):
+        p = rng.dirichlet(np.ones(4))
+        q = rng.dirichlet(np.ones(4))
+        cases.append((p, q))
+    for p, q in cases:
+        V = p.size
+        prob = np.zeros(V)
+        P = np.stack([p, p])
+        for x in range(V):
+            acc_frac = np.mean([o.verify_sample_probs(P, q[None], [x], [u], [0.0, 0.0])["n"] == 1
+                                for u in grid])
+            bonus = np.zeros(V)
+            for u in grid:
+                bonus[o.verify_sample_probs(P, q[None], [x], [0.0], [0.0, u])["out"][1]] += 1 / grid.size
+            # after acceptance the emitted token at position 0 is x itself
+            prob[x] += q[x] * acc_frac
+            res = np.zeros(V)
+            for u in grid:
+                res[o.verify_sample_probs(P, q[None], [x], [0.999999], [u, 0.0])["j"]] += 1 / grid.size
+            prob += q[x] * (1 - acc_frac) * res
+            assert abs(bonus.sum() - 1) < 1e-9
+        assert np.allclose(prob, p, atol=2e-3), (prob, p)
+
+
+def check_sampling_monte_carlo(o, trials=200_000):
+    g = golden()["three_token_example"]
+    p = np.array(g["p_target"])
+    q = np.array(g["q_draft"])
+    rng = np.random.default_rng(10)
+    xs = rng.choice(3, size=trials, p=q)
+    ua = rng.random(trials)
+    ur = rng.random(trials)
+    P = np.stack([p, p])
+    counts = np.zeros(3)
+    for i in range(trials):
+        r = o.verify_sample_probs(P, q[None], [xs[i]], [ua[i]], [ur[i], 0.0])
+        counts[r["out"][0]] += 1
+    freq = counts / trials
+    sigma = np.sqrt(p * (1 - p) / trials)
+    assert np.all(np.abs(freq - np.array(g["final_distribution"])) < 5 * sigma), freq
+
+
+def check_expected_tokens(o, trials=300_000):
+    g = golden()["expected_tokens_example"]
+    gamma, alpha = g["gamma"], g["alpha"]
+    assert abs(o.expected_tokens(alpha, gamma) - g["E_T"]) < 1e-12
+    assert o.expected_tokens(1.0, gamma) == gamma + 1
+    # constant per-position acceptance alpha: q = (1, 0) proposes token 0, p = (alpha, 1 - alpha)
+    P = np.tile([alpha, 1 - alpha], (gamma + 1, 1))
+    Q = np.tile([1.0, 0.0], (gamma, 1))
+    rng = np.random.default_rng(12)
+    U = rng.random((trials, gamma))
+    T = np.empty(trials)
+    for i in range(trials):
+        T[i] = o.verify_sample_probs(P, Q, [0] * gamma, U[i], [0.5] * (gamma + 1))["n"] + 1
+    se = T.std() / np.sqrt(trials)
+    assert abs(T.mean() - g["E_T"]) < 4 * se, (T.mean(), se)
+    # alpha = 1: every draft accepted, gamma + 1 tokens every time
+    P1 = np.tile([1.0, 0.0], (gamma + 1, 1))
+    for i in range(200):
+        assert o.verify_sample_probs(P1, Q, [0] * gamma, U[i], [0.5] * (gamma + 1))["n"] == gamma
+
+
+def check_sampling_from_logits(o):
+    # verify_sample on logits: the probabilities it reports are the softmax values at the tokens,
+    # and a position where p == q is always accepted
+    l = np.log(np.array([[[0.3, 0.5, 0.2], [0.1, 0.1, 0.8]]], dtype=np.float64))
+    lq = np.log(np.array([[[0.4, 0.4, 0.2]]], dtype=np.float64))
+    tb = ((l.astype(np.float32).view(np.uint32) + np.uint32(0x8000)) >> np.uint32(16)).astype(np.uint16)
+    db = ((lq.astype(np.float32).view(np.uint32) + np.uint32(0x8000)) >> np.uint32(16)).astype(np.uint16)
+    r = o.verify_sample(tb, db, np.array([[0]]), np.array([[0.9]], np.float32), np.array([[0.5, 0.5]], np.float32))
+    assert abs(r["p_tok"][0, 0] - 0.3) < 2e-3 and abs(r["q_tok"][0, 0] - 0.4) < 2e-3
+    assert abs(r["accept_prob"][0, 0] - 0.75) < 5e-3
+    assert r["accept_len"][0] == 0 and r["out_tok"][0].tolist() == [1, -1]
+    same = o.verify_sample(np.concatenate([db, db], axis=1), db, np.array([[2]]), np.array([[0.999]], np.float32),
+                           np.array([[0.5, 0.1]], np.float32))
+    assert same["accept_len"][0] == 1 and same["accept_prob"][0, 0] == 1.0
+
+
+ALL_FAST = [
+    check_pack_layout, check_weight_grid_roundtrip, check_weight_hand_cases, check_pack_end_to_end,
+    check_w4a16_onehot_and_grid, check_w4a16_error_bound, check_act_quant_hand_cases,
+    check_w4a4_bruteforce, check_w4a4_extremes, check_w4a4_constant_activation, check_softmax,
+    check_greedy_tutorial_example, check_greedy_bruteforce, check_greedy_ties,
+    check_greedy_equivalence, check_sampling_worked_example, check_sampling_from_logits,
+]

@@ -1,0 +1,76 @@
+"""Plant one plausible mistake at a time in a private copy of the CPU oracle and check that the
+pins catch it.  Nothing here touches a GPU; the mistakes live only in the in-memory copy."""
+import os
+import types
+
+import pytest
+
+import oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "qspec_oracle.py")
+
+# (name, text in the oracle, replacement)
+MUTATIONS = [
+    ("weight divisor 8", "s32 = amax / np.float32(7.0)", "s32 = amax / np.float32(8.0)"),
+    ("weight scale not fp16-rounded before coding", "s = S.astype(np.float32)[:, :, None]",
+     "s = s32[:, :, None]"),
+    ("weight rounding half up", "q = np.clip(np.rint(q), -8, 7)", "q = np.clip(np.floor(q + 0.5), -8, 7)"),
+    ("nibble order swapped", "return (lo | (hi << 4)).astype(np.uint8)", "return (hi | (lo << 4)).astype(np.uint8)"),
+    ("unpack without sign", "out = np.where(out >= 8, out - 16, out)", "out = out"),
+    ("group scale tiled instead of repeated", "scale = np.repeat(S.astype(np.float64), GROUP, axis=1)",
+     "scale = np.tile(S.astype(np.float64), (1, GROUP))"),
+    ("w4a16 transposed operand", "return x @ Wd.T", "return (Wd @ x.T)"),
+    ("activation divisor 8", "s_a = (amax / np.float32(7.0)).astype(np.float32)",
+     "s_a = (amax / np.float32(8.0)).astype(np.float32)"),
+    ("activation scale rounded to fp16", "s_a = (amax / np.float32(7.0)).astype(np.float32)",
+     "s_a = (amax / np.float32(7.0)).astype(np.float16).astype(np.float32)"),
+    ("w4a4 drops the token scale", "y = s_a.astype(np.float64)[:, None] * np.einsum",
+     "y = 1.0 * np.einsum"),
+    ("w4a4 groups strided", 'acc = np.einsum("mgk,ngk->mng", qa.reshape(M, G, GROUP), codes.reshape(N, G, GROUP))',
+     'acc = np.einsum("mkg,nkg->mng", qa.reshape(M, GROUP, G), codes.reshape(N, GROUP, G))'),
+    ("softmax without max shift", "e = np.exp(l - m)", "e = np.exp(l)"),
+    ("argmax takes the last tie", "for j in range(v.shape[0]):", "for j in reversed(range(v.shape[0])):"),
+    ("greedy drops the target token", "out[b, k] = t[b, k]", "out[b, k] = t[b, k] if k < gamma else -1"),
+    ("greedy compares with the next position", "int(d[b, k]) == int(t[b, k])", "int(d[b, k]) == int(t[b, k + 1])"),
+    ("accept test not strict", "if not (float(u_acc[i]) < a[i]):", "if not (float(u_acc[i]) <= a[i]):"),
+    ("residual keeps negative mass", "r = np.maximum(0.0, p_rows[n] - q_rows[n])", "r = np.abs(p_rows[n] - q_rows[n])"),
+    ("rejection resamples from p", "r = np.maximum(0.0, p_rows[n] - q_rows[n])", "r = p_rows[n]"),
+    ("bonus drawn from the last draft row", "r = p_rows[gamma]", "r = q_rows[gamma - 1]"),
+    ("acceptance ratio inverted", "min(1.0, p_tok[i] / q_tok[i])", "min(1.0, q_tok[i] / p_tok[i])"),
+    ("resample uniform not indexed by n", "j = inverse_cdf(r, float(u_res[n]))", "j = inverse_cdf(r, float(u_res[0]))"),
+    ("inverse cdf non-strict", "hit = np.nonzero(c > u * R)[0]", "hit = np.nonzero(c >= u * R)[0]"),
+    ("E[T] exponent off by one", "return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)",
+     "return (1.0 - alpha ** gamma) / (1.0 - alpha)"),
+]
+
+
+def mutated_oracle(old, new):
+    src = open(SRC, encoding="utf-8").read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src.replace(old, new), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+def caught(mod):
+    checks = list(pins.ALL_FAST) + [pins.check_sampling_exact_marginal,
+                                    lambda o: pins.check_expected_tokens(o, trials=40_000)]
+    for check in checks:
+        try:
+            check(mod)
+        except Exception:
+            return True
+    return False
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new):
+    assert caught(mutated_oracle(old, new)), f"no pin catches: {name}"
+
+
+def test_unmutated_copy_passes():
+    src = open(SRC, encoding="utf-8").read()
+    mod = types.ModuleType("oracle_copy")
+    exec(compile(src, "oracle_copy", "exec"), mod.__dict__)
+    for check in pins.ALL_FAST:
+        check(mod)

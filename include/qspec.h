@@ -1,0 +1,197 @@
+/*
+ * qspec.h -- C ABI of libqspec.so, the GB300 (sm_103a) hot path of QSpec-style quantized
+ * speculative decoding.
+ *
+ * The method (QSpec, as described in "QSpec実行時の2つの量子化による推論の一致率を調べる",
+ * qiita.com/joule, sections "W4A4 と W4A16 量子化" and "QSpec の W4A4 モードと W4A16 モード"):
+ * one set of 4-bit weights serves two modes.  The draft mode (W4A4) also quantises activations
+ * to 4 bits; the verify mode (W4A16) keeps 16-bit activations and converts the 4-bit weights while
+ * multiplying.  Drafted tokens are then checked against the verify-mode distribution with the
+ * standard speculative-decoding rules ("Speculative Decodingとは？LLM生成を速くする方法",
+ * kasblo.com, sections "greedy decodingでは一致するprefixを採用する" and
+ * "samplingでもtargetの確率分布を保つ", eqs. a(x) and p'(x)).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major and contiguous.
+ *    bfloat16 and float16 tensors are passed as uint16_t bit patterns.
+ *  - Every base pointer must be 16-byte aligned (QSPEC_ERR_MISALIGNED otherwise).
+ *  - Work is enqueued asynchronously on `stream` (NULL = legacy default stream).  No entry point
+ *    synchronises except qspec_check_status, and none allocates or frees device memory.
+ *  - Argument checks happen on the host before anything is enqueued; on failure nothing is
+ *    enqueued and the status says why.  Launch failures return QSPEC_ERR_CUDA.
+ *  - Outputs must not alias inputs.
+ *  - Calls are thread-safe.  Calls that share a verify workspace must not overlap on the GPU.
+ */
+#ifndef QSPEC_H_
+#define QSPEC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* same type as cudaStream_t */
+typedef struct CUstream_st* qspec_stream_t;
+
+typedef enum {
+  QSPEC_OK = 0,
+  QSPEC_ERR_INVALID_ARG = 1,        /* null pointer, negative or zero size, bad token id        */
+  QSPEC_ERR_UNSUPPORTED_SHAPE = 2,  /* size outside the documented limits                        */
+  QSPEC_ERR_MISALIGNED = 3,         /* a base pointer is not 16-byte aligned                     */
+  QSPEC_ERR_WORKSPACE = 4,          /* workspace missing or smaller than required                */
+  QSPEC_ERR_CUDA = 5,               /* a CUDA runtime/driver call or a launch failed             */
+  QSPEC_ERR_TIMEOUT = 6             /* a kernel gave up a bounded wait and returned early        */
+} qspec_status;
+
+/* Limits checked by every call. */
+#define QSPEC_GROUP 128             /* input channels per weight scale                           */
+#define QSPEC_MAX_M 4096            /* tokens per linear call                                    */
+#define QSPEC_MAX_GAMMA 16          /* draft length                                              */
+#define QSPEC_MAX_V (1 << 24)       /* vocabulary                                                */
+
+/*
+ * qspec_pack_weights -- symmetric per-group INT4 weight quantiser and packer (step a1).
+ *
+ * The pages fix only "4-bit weights shared by both modes" (QSpec article, section
+ * "QSpec の W4A4 モードと W4A16 モード"); the quantiser is the plain symmetric one:
+ * for each row n and group g of 128 consecutive input channels,
+ *     s[n,g]    = fp16( amax_g |W| / 7 )                   (fp32 IEEE division, round to fp16)
+ *     code[n,k] = clamp( rint( W[n,k] / float(s[n,g]) ), -8, 7 )   (fp32 IEEE division, ties even)
+ * with all codes 0 when s == 0.  Codes are two's complement nibbles: byte Wp[n, j] holds k = 2j in
+ * bits 0..3 and k = 2j+1 in bits 4..7.  This packed format is the format both linear calls read.
+ *
+ *   W   [N, K] bf16 (input), K % 128 == 0, 1 <= N, N*K < 2^40
+ *   Wp  [N, K/2] uint8 (output)
+ *   S   [N, K/128] fp16 (output)
+ * The result is bit-exact (independent of launch configuration).
+ */
+qspec_status qspec_pack_weights(const uint16_t* W, int64_t N, int64_t K, uint8_t* Wp, uint16_t* S,
+                                qspec_stream_t stream);
+
+/*
+ * qspec_linear_w4a16 -- verify-mode linear (step a2): y = x . dequant(Wp, S)^T.
+ *
+ * QSpec article, section "W4A16: 重みのみを 4-bit に量子化": 4-bit weights are converted to
+ * 16-bit values during the product with 16-bit activations.
+ *     y[m,n] = sum_k x[m,k] * code[n,k] * s[n, k/128]
+ * The codes are converted to bf16 exactly, products of each 128-channel group are summed in fp32
+ * and scaled by s[n,g]; y is rounded to bf16 once.
+ *
+ *   x  [M, K] bf16, Wp [N, K/2] uint8, S [N, K/128] fp16 (from qspec_pack_weights)
+ *   y  [M, N] bf16 (output)
+ *   ws, ws_bytes  device workspace, >= qspec_linear_workspace_size(M, N, K), zero-filled before its
+ *                 first use (calls leave it ready for the next call); it holds the partial sums of
+ *                 output tiles whose K range is split between SMs, and the W4A4 activation codes
+ *   1 <= M <= 4096, N % 8 == 0, K % 128 == 0.
+ * The fp32 summation order depends on the device's SM count, so results are reproducible on one
+ * device but may differ in the last bits between devices.
+ */
+qspec_status qspec_linear_w4a16(const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int64_t M,
+                                int64_t N, int64_t K, uint16_t* y, void* ws, size_t ws_bytes,
+                                qspec_stream_t stream);
+
+/*
+ * qspec_linear_w4a4 -- draft-mode linear (steps a3 + a4) with the activation quantiser fused.
+ *
+ * QSpec article, section "W4A4 : 重みと活性値の両方を 4-bit に量子化": activations are also
+ * quantised to 4 bits, so the product runs on 4-bit operands.  Per token m (all of K):
+ *     s_a[m]    = amax_k |x[m,k]| / 7                     (fp32 IEEE division, kept in fp32)
+ *     qa[m,k]   = clamp( rint( x[m,k] / s_a[m] ), -8, 7 ) (fp32 IEEE division, ties even; 0 if s_a==0)
+ *     acc[m,n,g]= sum_{k in group g} qa[m,k] * code[n,k]  (exact integer)
+ *     y[m,n]    = s_a[m] * sum_g float(s[n,g]) * acc[m,n,g]   (fp32, rounded to bf16 once)
+ *
+ *   x, Wp, S, y, M, N, K, ws, ws_bytes as for qspec_linear_w4a16 (the SAME Wp and S serve both modes).
+ *   xq_out  [M, K] int8 codes qa, or NULL              (bit-exact)
+ *   xs_out  [M] fp32 scales s_a, or NULL               (bit-exact)
+ *   acc_out [M, N, K/128] int32 group sums, or NULL    (bit-exact; debugging aid)
+ */
+qspec_status qspec_linear_w4a4(const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int64_t M,
+                               int64_t N, int64_t K, uint16_t* y, int8_t* xq_out, float* xs_out,
+                               int32_t* acc_out, void* ws, size_t ws_bytes, qspec_stream_t stream);
+
+/*
+ * qspec_linear_workspace_size -- bytes of device workspace both linear calls need for an [M, K] x
+ * [N, K] product on the CURRENT device (the size depends on its SM count).  0 for invalid sizes.
+ */
+size_t qspec_linear_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * qspec_verify_workspace_size -- bytes of device workspace that both verify calls need for the
+ * given shape.  The workspace must be zero-filled before its first use (e.g. one cudaMemset
+ * after allocation); every call leaves it ready for the next call.  Returns 0 for invalid sizes.
+ */
+size_t qspec_verify_workspace_size(int32_t B, int32_t gamma, int32_t V);
+
+/*
+ * qspec_verify_greedy -- greedy verification (steps a5 + a6).
+ *
+ * Tutorial, section "greedy decodingでは一致するprefixを採用する": draft tokens are compared left
+ * to right with the target's most likely token; the matching prefix is accepted, the first
+ * mismatching position takes the target's token instead, and when every draft token matches the
+ * target's token for the following position is added (at most gamma+1 tokens per call).
+ *     t[b,i] = argmax_j tgt_logits[b,i,j]    (lowest index among equal maxima; +0 == -0)
+ *     n[b]   = largest k <= gamma with d[b,i] == t[b,i] for all i < k
+ *     out[b] = (d[b,0..n-1], t[b,n], -1, ...)
+ *
+ *   tgt_logits [B, gamma+1, V] bf16   target logits at the gamma draft positions and the next one
+ *   draft_tok  [B, gamma] int32       draft tokens; ids outside [0, V) never match and raise
+ *                                     QSPEC_ERR_INVALID_ARG at the next qspec_check_status
+ *   accept_len [B] int32 (output)     n
+ *   out_tok    [B, gamma+1] int32 (output)
+ *   tgt_argmax [B, gamma+1] int32 (output) or NULL
+ *   ws, ws_bytes                      device workspace, >= qspec_verify_workspace_size(B,gamma,V)
+ *   1 <= B, 1 <= gamma <= 16, 2 <= V <= 2^24, B*(gamma+1)*V < 2^40.  Bit-exact.
+ */
+qspec_status qspec_verify_greedy(const uint16_t* tgt_logits, const int32_t* draft_tok, int32_t B,
+                                 int32_t gamma, int32_t V, int32_t* accept_len, int32_t* out_tok,
+                                 int32_t* tgt_argmax, void* ws, size_t ws_bytes,
+                                 qspec_stream_t stream);
+
+/*
+ * qspec_verify_sample -- sampling verification (steps a5, a7, a8).
+ *
+ * Tutorial, section "samplingでもtargetの確率分布を保つ": with p the target distribution and q the
+ * draft distribution (softmax of the logits, temperature 1, computed in fp32), draft token x at
+ * position i is accepted with probability a(x) = min(1, p(x)/q(x)) (eq. a(x)); at the first
+ * rejection n the emitted token is drawn from the residual max(0, p - q) / sum(...) (eq. p'(x));
+ * when all gamma are accepted a bonus token is drawn from the target distribution at position
+ * gamma.  The library draws no random numbers; the uniforms are inputs:
+ *     accept position i      iff  u_accept[b,i] < a_i          (a_i = 1 when q(x) == 0)
+ *     n[b]                   = first rejected position, or gamma
+ *     j*                     = smallest j with sum_{i<=j} r_i > u_resample[b,n] * sum(r)
+ *                              (r = residual of row n, or p of row gamma; r = p if sum is 0)
+ *     out[b]                 = (d[b,0..n-1], j*, -1, ...)
+ *
+ *   tgt_logits   [B, gamma+1, V] bf16;  draft_logits [B, gamma, V] bf16;  draft_tok [B, gamma]
+ *   u_accept     [B, gamma] fp32 in [0,1);  u_resample [B, gamma+1] fp32 in [0,1)
+ *   accept_len [B], out_tok [B, gamma+1] int32 (outputs)
+ *   accept_prob, p_tok, q_tok  [B, gamma] fp32 (outputs) or NULL: a_i, p_i(d_i), q_i(d_i) at every
+ *                              draft position (also those after the first rejection)
+ *   ws, ws_bytes as for qspec_verify_greedy.  Same size limits.
+ */
+qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const uint16_t* draft_logits,
+                                 const int32_t* draft_tok, const float* u_accept,
+                                 const float* u_resample, int32_t B, int32_t gamma, int32_t V,
+                                 int32_t* accept_len, int32_t* out_tok, float* accept_prob,
+                                 float* p_tok, float* q_tok, void* ws, size_t ws_bytes,
+                                 qspec_stream_t stream);
+
+/*
+ * qspec_check_status -- synchronises `stream`, then reports (and clears) the error words that the
+ * kernels set on the device: the verify workspace's word when `ws` is not NULL, and the library's
+ * own word for the linear kernels of the current device.  QSPEC_ERR_TIMEOUT if a kernel gave up a
+ * bounded wait, QSPEC_ERR_INVALID_ARG if a draft token id was out of range, QSPEC_ERR_CUDA if the
+ * stream reported an error, QSPEC_OK otherwise.
+ */
+qspec_status qspec_check_status(void* ws, qspec_stream_t stream);
+
+/* qspec_status_string -- a static, human-readable name for a status code. */
+const char* qspec_status_string(qspec_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSPEC_H_ */

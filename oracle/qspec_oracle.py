@@ -239,11 +239,10 @@ def softmax(logits) -> np.ndarray:
 def first_argmax(values) -> int:
     """The lowest index j with values[j] == max(values)  (+0 and -0 compare equal)."""
     v = np.asarray(values)
-    mx = np.max(v)
-    for j in range(v.shape[0]):
-        if v[j] == mx:
-            return j
-    raise ValueError("no maximum (NaN input)")
+    hits = np.flatnonzero(v == np.max(v))
+    if hits.size == 0:
+        raise ValueError("no maximum (NaN input)")
+    return int(hits[0])
 
 
 def verify_greedy(tgt_bits, draft_tok):

@@ -1,0 +1,48 @@
+// Shared helpers of the qspec CUDA library (sm_103a).  Nothing here is method arithmetic beyond
+// bit-level bf16 handling.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "qspec.h"
+
+namespace qspec {
+
+constexpr int kGroup = QSPEC_GROUP;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Status of the launches just enqueued on this thread.
+inline qspec_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
+}
+
+inline int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+// bf16 bit pattern (low 16 bits of b) -> fp32, exact.
+__device__ __forceinline__ float bf16_lo(uint32_t b) { return __uint_as_float(b << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t b) { return __uint_as_float(b & 0xFFFF0000u); }
+
+// fp32 -> bf16 bits, round to nearest even (the hardware conversion).
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// 16-byte streaming load that does not allocate in L1 (data read exactly once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+}  // namespace qspec

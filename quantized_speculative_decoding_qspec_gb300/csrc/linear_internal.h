@@ -1,0 +1,26 @@
+// Internal interface between the linear entry points and their kernel families.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qspec.h"
+
+namespace qspec {
+
+// CUDA-core kernels: every shape the entry points accept.
+qspec_status linear_simt(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M,
+                         int N, int K, uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out,
+                         cudaStream_t stream);
+
+// Tensor-core (tcgen05) kernels: the shapes for which linear_tc_supported() is true.
+bool linear_tc_supported(bool a4, int M, int N, int K);
+size_t linear_tc_workspace_size(bool a4, int M, int N, int K);
+qspec_status linear_tc(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M,
+                       int N, int K, uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out,
+                       void* ws, size_t ws_bytes, cudaStream_t stream);
+
+// Reads (synchronously) and clears the error bits the linear kernels set on the current device.
+qspec_status read_and_clear_linear_error(cudaStream_t stream, unsigned int* bits);
+
+}  // namespace qspec

@@ -1,0 +1,733 @@
+// Tensor-core (tcgen05) path of the W4A16 / W4A4 linears over the shared packed INT4 weights.
+//
+// QSpec article ("QSpec実行時の2つの量子化による推論の一致率を調べる"), section
+// "W4A4 と W4A16 量子化": W4A16 converts the 4-bit weights while multiplying 16-bit activations;
+// W4A4 also quantises the activations to 4 bits (one fp32 scale per token here).  Section
+// "QSpec の W4A4 モードと W4A16 モード": both modes read the same 4-bit weights.
+//
+// Design (one GB300 SM per CTA, persistent):
+//  * The product is computed transposed, D[n, m] = sum_k W[n, k] x[m, k]: 128 weight rows form the
+//    MMA's M = 128 side, the tokens (padded to NM = 16..64) its N side, so decode-sized M still
+//    fills the tensor core.
+//  * Work is split "stream-K": the (tile, 128-channel group) units of the whole problem are cut
+//    into gridDim.x equal contiguous ranges, so every SM streams the same number of weight bytes.
+//    A tile whose groups span several CTAs is finished by the last contributor (atomic ticket, no
+//    spinning), which adds the partial sums in CTA order -- the result does not depend on timing.
+//  * Warp roles: warp 0 issues TMA loads (packed weights, 128 rows x 256 channels per stage, and
+//    the activation tile); warp 1 owns TMEM and issues tcgen05.mma; warp 2 stages the fp16 group
+//    scales; warps 3..10 convert INT4 codes to bf16 (exact) straight into TMEM, where they are the
+//    MMA's A operand, and drain the fp32 accumulator of every 128-channel group, scaling it by
+//    s[n, g].  Stages are handed over with mbarriers; every wait is bounded.
+//  * W4A4: the INT4 activation codes are carried as bf16 (exact), so both modes share one MMA
+//    type; products and 128-term group sums are small integers, exact in the fp32 accumulator.
+//    For M <= 4 the per-token quantiser is fused (each CTA computes the token amax itself and
+//    converts the activation tile in shared memory); for larger M a small kernel quantises once
+//    and the GEMM reads the codes.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "linear_internal.h"
+#include "tc_ptx.cuh"
+
+namespace qspec {
+
+// Error bits set by linear kernels that give up a bounded wait (read by qspec_check_status).
+__device__ unsigned int g_linear_error = 0;
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kWorkerWarps = 8;
+constexpr int kFirstWorker = 3;
+constexpr int kThreadsTC = (kFirstWorker + kWorkerWarps) * 32;
+constexpr int kWBytes = 128 * 128;           // one stage of packed weights: 128 rows x 256 channels
+constexpr uint32_t kTmemCols = 512;
+constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (about 2 s) before a wait gives up
+constexpr int kFusedMaxM = 4;
+
+enum Mode : int { kA16 = 0, kA4Fused = 1, kA4Codes = 2 };
+
+__host__ __device__ constexpr int b_bytes(int NM) { return NM * 128 * 4; }  // 4 boxes of NM x 64 bf16
+__host__ __device__ constexpr int stage_bytes(int NM) { return kWBytes + b_bytes(NM); }
+__host__ __device__ constexpr int num_stages(int NM) {
+  return NM <= 16 ? 8 : (NM <= 32 ? 6 : (NM <= 48 ? 5 : 4));
+}
+
+struct Misc {
+  uint32_t tmem_base;
+  int abort_flag;
+  int last;
+  unsigned int amax_bits[kFusedMaxM];
+  float s_a[kFusedMaxM];
+};
+
+__host__ __device__ constexpr size_t smem_bytes(int NM) {
+  return 1024 /* alignment slack */ + size_t(num_stages(NM)) * stage_bytes(NM) +
+         size_t(num_stages(NM)) * 256 * sizeof(__half) + (2 * num_stages(NM) + 9) * sizeof(uint64_t) +
+         sizeof(Misc) + 64;
+}
+
+struct TcArgs {
+  int M, N, K, G, T_m, NMrows;
+  long long U;
+  uint16_t* y;
+  const __half* S;
+  float* partial;         // [gridDim.x][2][128][NM]
+  unsigned int* ticket;   // [tiles]
+  const float* s_a;       // kA4Codes: per-token scales
+  const uint16_t* x;      // kA4Fused: activations for the amax prologue
+  int32_t* acc_out;
+  int8_t* xq_out;
+  float* xs_out;
+};
+
+// Bounded wait: false if it gave up (then the whole CTA runs in abort mode).
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if (*abort_flag) return false;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimit) {
+      *abort_flag = 1;
+      atomicOr(&g_linear_error, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Wait that ignores the abort flag (used to let in-flight copies land before exit); bounded.
+__device__ __forceinline__ void wait_bar_final(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimit) {
+      atomicOr(&g_linear_error, 1u);
+      return;
+    }
+  }
+}
+
+// Stages of one CTA's unit range [u_beg, u_end): a stage is up to two consecutive groups of one tile.
+struct StageIter {
+  long long u, u_beg, u_end;
+  int G;
+  long long tile;
+  int g, ng;
+  bool last;  // last stage of this tile within the CTA
+  __device__ StageIter(long long ub, long long ue, int G_) : u(ub), u_beg(ub), u_end(ue), G(G_) {}
+  __device__ bool next() {
+    if (u >= u_end) return false;
+    tile = u / G;
+    g = static_cast<int>(u - tile * G);
+    const long long tile_end = min((tile + 1) * static_cast<long long>(G), u_end);
+    ng = static_cast<int>(min(2LL, tile_end - u));
+    u += ng;
+    last = u == tile_end;
+    return true;
+  }
+};
+
+__device__ __forceinline__ long long owner_of(long long u, long long U, long long P) {
+  return ((u + 1) * P - 1) / U;
+}
+
+// 8 INT4 codes (one little-endian word, k = 8w + i in bits 4i..4i+3) -> 4 bf16x2 words holding
+// (k0,k1), (k2,k3), (k4,k5), (k6,k7).  Each pair is placed as (c + 8) in the low mantissa bits of
+// bf16 128.0 (exact), then 136 is subtracted: the codes come out exact.
+__device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t* out) {
+  const uint32_t hi = w >> 4;
+  const __nv_bfloat162 off = __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t = __byte_perm(w, hi, static_cast<uint32_t>(i | ((4 + i) << 8)));
+    uint32_t v;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(v) : "r"(t), "r"(0x000F000Fu), "r"(0x43084308u));
+    const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), off);
+    out[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+template <int NM, int MODE>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    linear_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                     const TcArgs a) {
+  constexpr int NS = num_stages(NM);
+  constexpr int SB = stage_bytes(NM);
+  constexpr int HALF = NM / 2;
+  extern __shared__ uint8_t smem_raw[];
+  // the 128-byte swizzle wants 1024-byte aligned tiles (alignment of the shared-window offset)
+  uint8_t* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __half* sc = reinterpret_cast<__half*>(ring + NS * SB);  // [NS][2][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sc + NS * 256);
+  uint64_t* empty = full + NS;
+  uint64_t* afull = empty + NS;
+  uint64_t* afree = afull + 2;
+  uint64_t* dfull = afree + 2;
+  uint64_t* dfree = dfull + 2;
+  uint64_t* done = dfree + 2;
+  Misc* misc = reinterpret_cast<Misc*>(done + 1);
+  volatile int* abort_flag = &misc->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full + i, 2);                  // producer (expect_tx) + scale warp
+      mbar_init(empty + i, kWorkerWarps + 1);  // worker warps + MMA commit
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(afull + i, kWorkerWarps);
+      mbar_init(afree + i, 1);
+      mbar_init(dfull + i, 1);
+      mbar_init(dfree + i, kWorkerWarps);
+    }
+    mbar_init(done, 1);
+    misc->abort_flag = 0;
+    misc->last = 0;
+    for (int i = 0; i < kFusedMaxM; ++i) misc->amax_bits[i] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(&misc->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+
+  // Programmatic dependent launch: let the next kernel start launching; wait for the previous one
+  // before touching global memory.
+  grid_launch_dependents();
+  grid_dependency_wait();
+
+  const long long P = gridDim.x, c = blockIdx.x;
+  const long long u_beg = c * a.U / P, u_end = (c + 1) * a.U / P;
+  const int G = a.G;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      fence_proxy_async_global();
+      StageIter it(u_beg, u_end, G);
+      int s = 0, issued = 0;
+      while (it.next()) {
+        const int slot = s % NS;
+        if (s >= NS) wait_bar(empty + slot, ((s / NS) - 1) & 1, abort_flag);
+        if (!*abort_flag) {
+          ++issued;
+          const int n_tile = static_cast<int>(it.tile / a.T_m), m_tile = static_cast<int>(it.tile % a.T_m);
+          uint8_t* st = ring + slot * SB;
+          mbar_arrive_expect_tx(full + slot, SB);
+          tma_load_2d(st, &tmW, full + slot, it.g * 64, n_tile * 128);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(st + kWBytes + j * (NM * 128), &tmX, full + slot, it.g * 128 + 64 * j, m_tile * a.NMrows);
+        }
+        ++s;
+      }
+      // nothing may still be copying into shared memory when the CTA exits
+      for (int t = (issued > NS ? issued - NS : 0); t < issued; ++t) wait_bar_final(full + t % NS, (t / NS) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, NM);
+      StageIter it(u_beg, u_end, G);
+      int s = 0;
+      while (it.next()) {
+        const int slot = s % NS, pa = s & 1;
+        bool ok = wait_bar(afull + pa, (s >> 1) & 1, abort_flag);
+        if (s >= 2) ok = wait_bar(dfree + pa, ((s >> 1) - 1) & 1, abort_flag) && ok;
+        ok = wait_bar(full + slot, (s / NS) & 1, abort_flag) && ok;
+        if (ok && !*abort_flag) {
+          tc_fence_after();
+          const uint32_t a_base = tmem + pa * 128;
+          const uint32_t b_base = smem_u32(ring + slot * SB + kWBytes);
+          for (int j = 0; j < it.ng; ++j) {
+            const uint32_t d = tmem + 256 + (pa * 2 + j) * NM;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const int kb = j * 8 + kk;  // 16-channel step within the stage
+              const uint64_t bd = smem_desc_sw128(b_base + (kb >> 2) * (NM * 128) + (kb & 3) * 32);
+              mma_bf16_ts(d, a_base + kb * 8, bd, idesc, kk > 0 ? 1u : 0u);
+            }
+          }
+        }
+        mma_commit(empty + slot);
+        mma_commit(afree + pa);
+        mma_commit(dfull + pa);
+        ++s;
+      }
+      mma_commit(done);
+      wait_bar_final(done, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ group-scale stager
+    StageIter it(u_beg, u_end, G);
+    int s = 0;
+    while (it.next()) {
+      const int slot = s % NS;
+      if (s >= NS) wait_bar(empty + slot, ((s / NS) - 1) & 1, abort_flag);
+      const int n0 = static_cast<int>(it.tile / a.T_m) * 128;
+      __half* dst = sc + slot * 256;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane * 4 + i;
+        const int n = n0 + r;
+        __half s0 = __ushort_as_half(0), s1 = __ushort_as_half(0);
+        if (n < a.N) {
+          const __half* srow = a.S + static_cast<long long>(n) * G + it.g;
+          s0 = __ldg(srow);
+          if (it.ng == 2) s1 = __ldg(srow + 1);
+        }
+        dst[r] = s0;
+        dst[128 + r] = s1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full + slot);
+      ++s;
+    }
+  } else {
+    // ------------------------------------------------------------------ workers: dequant + drain
+    const int wi = warp - kFirstWorker;   // 0..7
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int h = wi >> 2;                // which group of a stage (dequant) / token half (drain)
+    const int row = q * 32 + lane;        // output row within the tile = TMEM lane
+    const int wt = wi * 32 + lane;        // 0..255 among the workers
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int M = a.M, N = a.N;
+
+    if constexpr (MODE == kA4Fused) {
+      // per-token amax over all of K (tokens < M <= 4), then s_a = amax / 7 in fp32
+      for (int m = 0; m < M; ++m) {
+        uint32_t mx = 0;
+        const uint16_t* xr = a.x + static_cast<long long>(m) * a.K;
+        for (int k8 = wt; k8 < a.K / 8; k8 += 256) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + k8);
+          mx = max(mx, max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu)));
+          mx = max(mx, max(max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu)));
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+        if (lane == 0) atomicMax(&misc->amax_bits[m], mx);
+      }
+      named_bar_sync(1, kWorkerWarps * 32);
+      if (wt < M) misc->s_a[wt] = __fdiv_rn(__uint_as_float(misc->amax_bits[wt] << 16), 7.0f);
+      named_bar_sync(1, kWorkerWarps * 32);
+      if (blockIdx.x == 0 && a.xs_out && wt < M) a.xs_out[wt] = misc->s_a[wt];
+      if (a.xq_out) {  // this CTA's slice of the int8 codes
+        const int k0 = static_cast<int>(c * a.K / P), k1 = static_cast<int>((c + 1) * a.K / P);
+        for (int m = 0; m < M; ++m) {
+          const float sa = misc->s_a[m];
+          for (int k = k0 + wt; k < k1; k += 256) {
+            const float xv = bf16_lo(a.x[static_cast<long long>(m) * a.K + k]);
+            const float cq = sa == 0.0f ? 0.0f : fminf(fmaxf(rintf(__fdiv_rn(xv, sa)), -8.0f), 7.0f);
+            a.xq_out[static_cast<long long>(m) * a.K + k] = static_cast<int8_t>(cq);
+          }
+        }
+      }
+    }
+
+    float acc[HALF];
+#pragma unroll
+    for (int t = 0; t < HALF; ++t) acc[t] = 0.0f;
+
+    struct Pending {
+      int s, ng, g;
+      long long tile;
+      bool last;
+      float s0, s1;
+    } prev{};
+    bool has_prev = false;
+
+    auto drain = [&](const Pending& p) {
+      const int pa = p.s & 1;
+      const bool ok = wait_bar(dfull + pa, (p.s >> 1) & 1, abort_flag);
+      tc_fence_after();
+      uint32_t d0[HALF], d1[HALF];
+      if (ok) {
+#pragma unroll
+        for (int c8 = 0; c8 < HALF / 8; ++c8)
+          tmem_ld8(tmem + lane_base + 256 + (pa * 2 + 0) * NM + h * HALF + 8 * c8, d0 + 8 * c8);
+        if (p.ng == 2) {
+#pragma unroll
+          for (int c8 = 0; c8 < HALF / 8; ++c8)
+            tmem_ld8(tmem + lane_base + 256 + (pa * 2 + 1) * NM + h * HALF + 8 * c8, d1 + 8 * c8);
+        }
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dfree + pa);
+      if (!ok || *abort_flag) return;
+#pragma unroll
+      for (int t = 0; t < HALF; ++t) acc[t] = fmaf(p.s0, __uint_as_float(d0[t]), acc[t]);
+      if (p.ng == 2) {
+#pragma unroll
+        for (int t = 0; t < HALF; ++t) acc[t] = fmaf(p.s1, __uint_as_float(d1[t]), acc[t]);
+      }
+      if constexpr (MODE != kA16) {
+        if (a.acc_out) {
+          const int n = static_cast<int>(p.tile / a.T_m) * 128 + row;
+          const int m0 = static_cast<int>(p.tile % a.T_m) * a.NMrows + h * HALF;
+#pragma unroll
+          for (int t = 0; t < HALF; ++t) {
+            const int m = m0 + t;
+            if (m < M && n < N) {
+              int32_t* dst = a.acc_out + (static_cast<long long>(m) * N + n) * G + p.g;
+              dst[0] = static_cast<int32_t>(__uint_as_float(d0[t]));
+              if (p.ng == 2) dst[1] = static_cast<int32_t>(__uint_as_float(d1[t]));
+            }
+          }
+        }
+      }
+    };
+
+    auto token_scale = [&](int m) -> float {
+      if constexpr (MODE == kA4Fused) return misc->s_a[m];
+      else if constexpr (MODE == kA4Codes) return __ldg(a.s_a + m);
+      else return 1.0f;
+    };
+
+    auto store_y = [&](long long tile, const float* v) {
+      const int n = static_cast<int>(tile / a.T_m) * 128 + row;
+      const int m0 = static_cast<int>(tile % a.T_m) * a.NMrows + h * HALF;
+#pragma unroll
+      for (int t = 0; t < HALF; ++t) {
+        const int m = m0 + t;
+        if (m < M && n < N) {
+          float o = v[t];
+          if constexpr (MODE != kA16) o *= token_scale(m);
+          a.y[static_cast<long long>(m) * N + n] = f32_to_bf16_bits(o);
+        }
+      }
+    };
+
+    auto epilogue = [&](long long tile) {
+      const long long c_first = owner_of(tile * G, a.U, P);
+      const long long c_last = owner_of((tile + 1) * G - 1, a.U, P);
+      if (c_first == c_last) {
+        if (!*abort_flag) store_y(tile, acc);
+      } else {
+        const int my_slot = (tile == u_beg / G) ? 0 : 1;
+        float* part = a.partial + ((c * 2 + my_slot) * 128 + row) * NM + h * HALF;
+#pragma unroll
+        for (int t = 0; t < HALF; t += 4) *reinterpret_cast<float4*>(part + t) = make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
+        __threadfence();
+        named_bar_sync(1, kWorkerWarps * 32);
+        if (wt == 0) {
+          const unsigned int prevc = atomicAdd(a.ticket + tile, 1u);
+          misc->last = prevc == static_cast<unsigned int>(c_last - c_first);
+        }
+        named_bar_sync(1, kWorkerWarps * 32);
+        if (misc->last) {
+          __threadfence();
+          float sum[HALF];
+#pragma unroll
+          for (int t = 0; t < HALF; ++t) sum[t] = 0.0f;
+          for (long long cc = c_first; cc <= c_last; ++cc) {
+            const int sl = (tile == (cc * a.U / P) / G) ? 0 : 1;
+            const float* src = a.partial + ((cc * 2 + sl) * 128 + row) * NM + h * HALF;
+#pragma unroll
+            for (int t = 0; t < HALF; t += 4) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(src + t));
+              sum[t] += v.x;
+              sum[t + 1] += v.y;
+              sum[t + 2] += v.z;
+              sum[t + 3] += v.w;
+            }
+          }
+          if (!*abort_flag) store_y(tile, sum);
+          if (wt == 0) a.ticket[tile] = 0;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < HALF; ++t) acc[t] = 0.0f;
+    };
+
+    StageIter it(u_beg, u_end, G);
+    int s = 0;
+    while (it.next()) {
+      const int slot = s % NS, pa = s & 1;
+      bool ok = wait_bar(full + slot, (s / NS) & 1, abort_flag);
+      if (s >= 2) ok = wait_bar(afree + pa, ((s >> 1) - 1) & 1, abort_flag) && ok;
+      Pending cur{s, it.ng, it.g, it.tile, it.last, 0.0f, 0.0f};
+      if (ok && !*abort_flag) {
+        cur.s0 = __half2float(sc[slot * 256 + row]);
+        cur.s1 = __half2float(sc[slot * 256 + 128 + row]);
+        uint8_t* st = ring + slot * SB;
+        if constexpr (MODE == kA4Fused) {
+          // activation tile -> INT4 codes (as exact bf16) in place, rows m < M
+          uint8_t* bst = st + kWBytes;
+          for (int m = 0; m < M; ++m) {
+            const int k = wt;  // 0..255 within the stage
+            const int j = k >> 6, kin = k & 63;
+            uint16_t* p = reinterpret_cast<uint16_t*>(bst + j * (NM * 128) + (m >> 3) * 1024 + (m & 7) * 128 +
+                                                      ((((kin >> 3) ^ (m & 7))) << 4) + (kin & 7) * 2);
+            const float sa = misc->s_a[m];
+            const float cq = sa == 0.0f ? 0.0f : fminf(fmaxf(rintf(__fdiv_rn(bf16_lo(*p), sa)), -8.0f), 7.0f);
+            *p = f32_to_bf16_bits(cq);
+          }
+          fence_proxy_async_smem();
+        }
+        if (h < it.ng) {
+          const uint8_t* wrow = st + row * 128;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((((4 * h + cc) ^ (row & 7))) << 4));
+            uint32_t out[16];
+            codes_to_bf16x2(v.x, out);
+            codes_to_bf16x2(v.y, out + 4);
+            codes_to_bf16x2(v.z, out + 8);
+            codes_to_bf16x2(v.w, out + 12);
+            tmem_st16(tmem + lane_base + pa * 128 + h * 64 + cc * 16, out);
+          }
+          tmem_wait_st();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(afull + pa);
+        mbar_arrive(empty + slot);
+      }
+      if (has_prev) {
+        drain(prev);
+        if (prev.last) epilogue(prev.tile);
+      }
+      prev = cur;
+      has_prev = true;
+      ++s;
+    }
+    if (has_prev) {
+      drain(prev);
+      if (prev.last) epilogue(prev.tile);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Per-token quantiser for M > 4 (step a3): codes as exact bf16 for the GEMM, plus the optional
+// int8 codes and fp32 scales.  One CTA per token.
+__global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, int K,
+                                                        uint16_t* __restrict__ codes, float* __restrict__ s_a,
+                                                        int8_t* __restrict__ xq_out, float* __restrict__ xs_out) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int m = blockIdx.x;
+  const uint16_t* xr = x + static_cast<long long>(m) * K;
+  uint32_t mx = 0;
+  for (int k8 = threadIdx.x; k8 < K / 8; k8 += 256) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + k8);
+    mx = max(mx, max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu)));
+    mx = max(mx, max(max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu)));
+  }
+  __shared__ unsigned int s_mx;
+  if (threadIdx.x == 0) s_mx = 0;
+  __syncthreads();
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  if ((threadIdx.x & 31) == 0) atomicMax(&s_mx, mx);
+  __syncthreads();
+  const float sa = __fdiv_rn(__uint_as_float(s_mx << 16), 7.0f);
+  if (threadIdx.x == 0) {
+    s_a[m] = sa;
+    if (xs_out) xs_out[m] = sa;
+  }
+  for (int k = threadIdx.x; k < K; k += 256) {
+    const float cq = sa == 0.0f ? 0.0f : fminf(fmaxf(rintf(__fdiv_rn(bf16_lo(xr[k]), sa)), -8.0f), 7.0f);
+    codes[static_cast<long long>(m) * K + k] = f32_to_bf16_bits(cq);
+    if (xq_out) xq_out[static_cast<long long>(m) * K + k] = static_cast<int8_t>(cq);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int pick_nm(bool a4, int M) {
+  if (a4 && M <= kFusedMaxM) return 16;
+  return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 48 ? 48 : 64));
+}
+
+inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t ticket, partial, codes, s_a, total;
+};
+
+WsLayout ws_layout(bool a4, int M, int N, int K, int P) {
+  const int NM = pick_nm(a4, M);
+  const long long T = (static_cast<long long>(N) + 127) / 128 * ((M + NM - 1) / NM);
+  WsLayout L;
+  size_t off = 0;
+  L.ticket = off;  off = al256(off + sizeof(unsigned int) * T);
+  L.partial = off; off = al256(off + sizeof(float) * size_t(P) * 2 * 128 * NM);
+  L.codes = off;   off = al256(off + ((a4 && M > kFusedMaxM) ? sizeof(uint16_t) * size_t(M) * K : 0));
+  L.s_a = off;     off = al256(off + ((a4 && M > kFusedMaxM) ? sizeof(float) * size_t(M) : 0));
+  L.total = off;
+  return L;
+}
+
+template <int NM, int MODE>
+qspec_status launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcArgs& args, int P,
+                       cudaStream_t stream) {
+  auto kern = linear_tc_kernel<NM, MODE>;
+  const size_t smem = smem_bytes(NM);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return QSPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P);
+  cfg.blockDim = dim3(kThreadsTC);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, args) == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
+}
+
+}  // namespace
+
+bool linear_tc_supported(bool, int M, int N, int K) {
+  return M >= 1 && M <= QSPEC_MAX_M && N >= 8 && K >= kGroup && encode_fn() != nullptr;
+}
+
+size_t linear_tc_workspace_size(bool a4, int M, int N, int K) {
+  return ws_layout(a4, M, N, K, num_sms()).total;
+}
+
+qspec_status linear_tc(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
+                       uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  const int NM = pick_nm(a4, M);
+  const int T_m = (M + NM - 1) / NM;
+  const long long T = (static_cast<long long>(N) + 127) / 128 * T_m;
+  const int G = K / kGroup;
+  const long long U = T * G;
+  const int P = static_cast<int>(std::min<long long>(U, num_sms()));
+  const WsLayout L = ws_layout(a4, M, N, K, num_sms());
+  if (!ws || ws_bytes < L.total) return QSPEC_ERR_WORKSPACE;
+  char* wsb = static_cast<char*>(ws);
+
+  const bool codes_mode = a4 && M > kFusedMaxM;
+  uint16_t* codes = reinterpret_cast<uint16_t*>(wsb + L.codes);
+  float* s_a = reinterpret_cast<float*>(wsb + L.s_a);
+
+  CUtensorMap tmW, tmX;
+  if (!make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wp, static_cast<uint64_t>(K) / 2, static_cast<uint64_t>(N),
+                   static_cast<uint64_t>(K) / 2, 128, 128))
+    return QSPEC_ERR_CUDA;
+  const void* bsrc = codes_mode ? static_cast<const void*>(codes) : static_cast<const void*>(x);
+  if (!make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, bsrc, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(K) * 2, 64, static_cast<uint32_t>(NM)))
+    return QSPEC_ERR_CUDA;
+
+  if (codes_mode) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(M);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, act_quant_kernel, x, K, codes, s_a, xq_out, xs_out) != cudaSuccess)
+      return QSPEC_ERR_CUDA;
+  }
+
+  TcArgs args;
+  args.M = M;
+  args.N = N;
+  args.K = K;
+  args.G = G;
+  args.T_m = T_m;
+  args.NMrows = NM;
+  args.U = U;
+  args.y = y;
+  args.S = reinterpret_cast<const __half*>(S);
+  args.partial = reinterpret_cast<float*>(wsb + L.partial);
+  args.ticket = reinterpret_cast<unsigned int*>(wsb + L.ticket);
+  args.s_a = s_a;
+  args.x = x;
+  args.acc_out = acc_out;
+  args.xq_out = xq_out;
+  args.xs_out = xs_out;
+
+  if (!a4) {
+    switch (NM) {
+      case 16: return launch_tc<16, kA16>(tmW, tmX, args, P, stream);
+      case 32: return launch_tc<32, kA16>(tmW, tmX, args, P, stream);
+      case 48: return launch_tc<48, kA16>(tmW, tmX, args, P, stream);
+      default: return launch_tc<64, kA16>(tmW, tmX, args, P, stream);
+    }
+  }
+  if (!codes_mode) return launch_tc<16, kA4Fused>(tmW, tmX, args, P, stream);
+  switch (NM) {
+    case 16: return launch_tc<16, kA4Codes>(tmW, tmX, args, P, stream);
+    case 32: return launch_tc<32, kA4Codes>(tmW, tmX, args, P, stream);
+    case 48: return launch_tc<48, kA4Codes>(tmW, tmX, args, P, stream);
+    default: return launch_tc<64, kA4Codes>(tmW, tmX, args, P, stream);
+  }
+}
+
+qspec_status read_and_clear_linear_error(cudaStream_t stream, unsigned int* bits) {
+  *bits = 0;
+  if (cudaMemcpyFromSymbolAsync(bits, g_linear_error, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return QSPEC_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return QSPEC_ERR_CUDA;
+  if (*bits) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_linear_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+      return QSPEC_ERR_CUDA;
+  }
+  return QSPEC_OK;
+}
+
+}  // namespace qspec

@@ -1,0 +1,680 @@
+// Steps a5-a8: the fused verify step over vocabulary logits.
+//
+// Tutorial "Speculative Decodingとは？LLM生成を速くする方法" (kasblo.com):
+//  - section "greedy decodingでは一致するprefixを採用する": accept draft tokens while they equal the
+//    target argmax; the first mismatch takes the target token; all-match adds the next target token;
+//  - section "samplingでもtargetの確率分布を保つ": accept x with probability a(x) = min(1, p(x)/q(x))
+//    (eq. a(x)); on rejection draw from the residual max(0, p - q) / sum (eq. p'(x)).
+//
+// All passes are HBM-bound streams over bf16 logits.  One CTA per (row, chunk of the vocabulary)
+// keeps every SM streaming; the per-sequence combine runs in whichever CTA of the sequence finishes
+// last (an atomic ticket per sequence, no spinning).  Counters are reset by that CTA, so the
+// workspace is ready for the next call.
+#include <float.h>
+#include <limits.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace qspec {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kPlanCTAs = 608;    // about 4 CTAs per SM on a 152-SM part
+constexpr int kMinChunk = 2048;   // elements per CTA at least (4 KB of bf16)
+constexpr int kSeg2 = 8;          // pass 2: contiguous elements per thread
+constexpr int kChunk2 = kThreads * kSeg2;
+
+enum : unsigned int { kErrBadToken = 2u };
+
+struct Plan {
+  int chunks;      // chunks per row
+  int chunk_len;   // elements per chunk (multiple of 8)
+};
+
+Plan plan_rows(int64_t rows, int V) {
+  int64_t c = (kPlanCTAs + rows - 1) / rows;
+  const int64_t max_c = (V + kMinChunk - 1) / kMinChunk;
+  if (c > max_c) c = max_c;
+  if (c < 1) c = 1;
+  int64_t len = ((V + c - 1) / c + 7) / 8 * 8;
+  c = (V + len - 1) / len;
+  return {static_cast<int>(c), static_cast<int>(len)};
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace layout (bytes).  Both verify calls use the same layout for a given (B, gamma, V).
+struct Layout {
+  Plan p1;            // pass-1 plan over B * (2 gamma + 1) rows (greedy uses B * (gamma + 1) rows)
+  Plan pg;
+  int chunks2;
+  size_t err, cnt1, cnt2, seq_n, rowstat, part1, part2, total;
+};
+
+Layout layout(int B, int gamma, int V) {
+  Layout L;
+  L.pg = plan_rows(int64_t(B) * (gamma + 1), V);
+  L.p1 = plan_rows(int64_t(B) * (2 * gamma + 1), V);
+  L.chunks2 = (V + kChunk2 - 1) / kChunk2;
+  size_t off = 0;
+  L.err = off;      off += 256;
+  L.cnt1 = off;     off = align256(off + sizeof(unsigned int) * B);
+  L.cnt2 = off;     off = align256(off + sizeof(unsigned int) * B);
+  L.seq_n = off;    off = align256(off + sizeof(int) * B);
+  L.rowstat = off;  off = align256(off + sizeof(float2) * size_t(B) * (2 * gamma + 1));
+  const size_t part_g = sizeof(float2) * size_t(B) * (gamma + 1) * L.pg.chunks;
+  const size_t part_s = sizeof(float2) * size_t(B) * (2 * gamma + 1) * L.p1.chunks;
+  L.part1 = off;    off = align256(off + (part_g > part_s ? part_g : part_s));
+  L.part2 = off;    off = align256(off + sizeof(float) * size_t(B) * L.chunks2);
+  L.total = off;
+  return L;
+}
+
+struct WS {
+  unsigned int* err;
+  unsigned int* cnt1;
+  unsigned int* cnt2;
+  int* seq_n;
+  float2* rowstat;
+  float2* part1;
+  float* part2;
+};
+
+WS bind(void* base, const Layout& L) {
+  char* p = static_cast<char*>(base);
+  return {reinterpret_cast<unsigned int*>(p + L.err), reinterpret_cast<unsigned int*>(p + L.cnt1),
+          reinterpret_cast<unsigned int*>(p + L.cnt2), reinterpret_cast<int*>(p + L.seq_n),
+          reinterpret_cast<float2*>(p + L.rowstat), reinterpret_cast<float2*>(p + L.part1),
+          reinterpret_cast<float*>(p + L.part2)};
+}
+
+// ------------------------------------------------------------------ argmax (greedy)
+
+// (value, index) order for argmax: larger value wins, equal values go to the lower index.
+__device__ __forceinline__ void argmax_take(float& bv, int& bi, float v, int i) {
+  if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+}
+
+__device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+    const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+    argmax_take(bv, bi, ov, oi);
+  }
+}
+
+// Block-wide argmax; every thread gets the result.
+__device__ __forceinline__ void block_argmax(float& bv, int& bi) {
+  __shared__ float sv[kThreads / 32];
+  __shared__ int si[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  warp_argmax(bv, bi);
+  if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+  __syncthreads();
+  bv = lane < kThreads / 32 ? sv[lane] : -INFINITY;
+  bi = lane < kThreads / 32 ? si[lane] : INT_MAX;
+  warp_argmax(bv, bi);
+  __syncthreads();
+}
+
+// Scan logits [beg, end) of one row with each thread taking 16-byte vectors t, t+256, ...
+template <bool kVec>
+__device__ __forceinline__ void scan_argmax(const uint16_t* __restrict__ rp, int beg, int end, float& bv,
+                                            int& bi) {
+  if (kVec) {
+    const int nv = (end - beg) >> 3;
+    const uint4* vp = reinterpret_cast<const uint4*>(rp + beg);
+    for (int v0 = threadIdx.x; v0 < nv; v0 += 4 * kThreads) {
+      uint4 u[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int v = v0 + t * kThreads;
+        u[t] = v < nv ? ld_stream_v4(vp + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int v = v0 + t * kThreads;
+        if (v < nv) {
+          const int i0 = beg + 8 * v;
+          const uint32_t w[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            argmax_take(bv, bi, bf16_lo(w[e]), i0 + 2 * e);
+            argmax_take(bv, bi, bf16_hi(w[e]), i0 + 2 * e + 1);
+          }
+        }
+      }
+    }
+  } else {
+    for (int i = beg + threadIdx.x; i < end; i += kThreads) argmax_take(bv, bi, bf16_lo(rp[i]), i);
+  }
+}
+
+// One CTA per (row, chunk); the last CTA of a sequence applies the greedy rule.
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) greedy_kernel(const uint16_t* __restrict__ L,
+                                                          const int32_t* __restrict__ d, int gamma,
+                                                          int V, Plan plan, WS ws,
+                                                          int32_t* __restrict__ accept_len,
+                                                          int32_t* __restrict__ out_tok,
+                                                          int32_t* __restrict__ tgt_argmax) {
+  const int64_t row = blockIdx.x / plan.chunks;
+  const int c = blockIdx.x % plan.chunks;
+  const int beg = c * plan.chunk_len;
+  const int end = min(V, beg + plan.chunk_len);
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  scan_argmax<kVec>(L + row * V, beg, end, bv, bi);
+  block_argmax(bv, bi);
+
+  __shared__ bool s_last;
+  const int G1 = gamma + 1;
+  const int b = static_cast<int>(row / G1);
+  if (threadIdx.x == 0) {
+    ws.part1[row * plan.chunks + c] = make_float2(bv, __int_as_float(bi));
+    __threadfence();
+    const unsigned int prev = atomicAdd(ws.cnt1 + b, 1u);
+    s_last = prev == static_cast<unsigned int>(G1 * plan.chunks - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  __shared__ int s_t[QSPEC_MAX_GAMMA + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < G1; i += kThreads / 32) {
+    const int64_t r = int64_t(b) * G1 + i;
+    float v = -INFINITY;
+    int k = INT_MAX;
+    for (int cc = lane; cc < plan.chunks; cc += 32) {
+      const float2 pp = __ldcg(ws.part1 + r * plan.chunks + cc);
+      argmax_take(v, k, pp.x, __float_as_int(pp.y));
+    }
+    warp_argmax(v, k);
+    if (lane == 0) s_t[i] = k;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int n = 0;
+    bool bad = false;
+    for (int i = 0; i < gamma; ++i) {
+      const int x = d[int64_t(b) * gamma + i];
+      if (x < 0 || x >= V) bad = true;
+    }
+    while (n < gamma && d[int64_t(b) * gamma + n] == s_t[n]) ++n;
+    if (bad) atomicOr(ws.err, kErrBadToken);
+    accept_len[b] = n;
+    for (int i = 0; i < G1; ++i) {
+      out_tok[int64_t(b) * G1 + i] = i < n ? d[int64_t(b) * gamma + i] : (i == n ? s_t[n] : -1);
+      if (tgt_argmax) tgt_argmax[int64_t(b) * G1 + i] = s_t[i];
+    }
+    ws.cnt1[b] = 0;
+  }
+}
+
+// ------------------------------------------------------------------ softmax statistics (sampling)
+
+// Running (max, sum of exp(l - max)) of a set of logits; -inf logits contribute nothing.
+struct MS {
+  float m, s;
+};
+
+__device__ __forceinline__ MS ms_merge(MS a, MS b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return {m, 0.0f};
+  return {m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
+}
+
+__device__ __forceinline__ void ms_add8(MS& a, const float (&v)[8]) {
+  float m8 = v[0];
+#pragma unroll
+  for (int e = 1; e < 8; ++e) m8 = fmaxf(m8, v[e]);
+  if (m8 > a.m) {
+    a.s = a.m == -INFINITY ? 0.0f : a.s * expf(a.m - m8);
+    a.m = m8;
+  }
+  if (a.m != -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a.s += expf(v[e] - a.m);
+  }
+}
+
+__device__ __forceinline__ MS warp_ms(MS a) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    MS o{__shfl_xor_sync(0xFFFFFFFFu, a.m, off), __shfl_xor_sync(0xFFFFFFFFu, a.s, off)};
+    a = ms_merge(a, o);
+  }
+  return a;
+}
+
+__device__ __forceinline__ MS block_ms(MS a) {
+  __shared__ float sm[kThreads / 32], ss[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  a = warp_ms(a);
+  if (lane == 0) { sm[warp] = a.m; ss[warp] = a.s; }
+  __syncthreads();
+  MS r{lane < kThreads / 32 ? sm[lane] : -INFINITY, lane < kThreads / 32 ? ss[lane] : 0.0f};
+  r = warp_ms(r);
+  __syncthreads();
+  return r;
+}
+
+template <bool kVec>
+__device__ __forceinline__ MS scan_ms(const uint16_t* __restrict__ rp, int beg, int end) {
+  MS a{-INFINITY, 0.0f};
+  if (kVec) {
+    const int nv = (end - beg) >> 3;
+    const uint4* vp = reinterpret_cast<const uint4*>(rp + beg);
+    for (int v0 = threadIdx.x; v0 < nv; v0 += 4 * kThreads) {
+      uint4 u[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int v = v0 + t * kThreads;
+        u[t] = v < nv ? ld_stream_v4(vp + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (v0 + t * kThreads < nv) {
+          const uint32_t w[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) { f[2 * e] = bf16_lo(w[e]); f[2 * e + 1] = bf16_hi(w[e]); }
+          ms_add8(a, f);
+        }
+      }
+    }
+  } else {
+    for (int i = beg + threadIdx.x; i < end; i += kThreads) {
+      float f[8];
+      f[0] = bf16_lo(rp[i]);
+#pragma unroll
+      for (int e = 1; e < 8; ++e) f[e] = -INFINITY;
+      ms_add8(a, f);
+    }
+  }
+  return a;
+}
+
+// Pass 1 of sampling verify: softmax statistics of every target and draft row; the last CTA of a
+// sequence evaluates a_i = min(1, p_i(d_i) / q_i(d_i)) at every draft position and the first
+// rejection n.  Rows [0, B(gamma+1)) are target rows, the next B*gamma rows draft rows.
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) sample_pass1_kernel(
+    const uint16_t* __restrict__ Lt, const uint16_t* __restrict__ Ld, const int32_t* __restrict__ d,
+    const float* __restrict__ u_acc, int B, int gamma, int V, Plan plan, WS ws,
+    int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tok, float* __restrict__ accept_prob,
+    float* __restrict__ p_tok, float* __restrict__ q_tok) {
+  const int64_t row = blockIdx.x / plan.chunks;
+  const int c = blockIdx.x % plan.chunks;
+  const int G1 = gamma + 1;
+  const int64_t n_tgt = int64_t(B) * G1;
+  const bool is_tgt = row < n_tgt;
+  const uint16_t* rp = is_tgt ? Lt + row * V : Ld + (row - n_tgt) * V;
+  const int b = static_cast<int>(is_tgt ? row / G1 : (row - n_tgt) / gamma);
+  const int beg = c * plan.chunk_len;
+  const int end = min(V, beg + plan.chunk_len);
+  MS a = scan_ms<kVec>(rp, beg, end);
+  a = block_ms(a);
+
+  __shared__ bool s_last;
+  if (threadIdx.x == 0) {
+    ws.part1[row * plan.chunks + c] = make_float2(a.m, a.s);
+    __threadfence();
+    const unsigned int prev = atomicAdd(ws.cnt1 + b, 1u);
+    s_last = prev == static_cast<unsigned int>((2 * gamma + 1) * plan.chunks - 1);
+  }
+  __syncthreads();
+  // Pass 2 may start launching now; it waits for this grid's completion before reading.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!s_last) return;
+  __threadfence();
+
+  __shared__ float2 s_stat[2 * QSPEC_MAX_GAMMA + 1];  // [0, G1): target rows; then draft rows
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < 2 * gamma + 1; i += kThreads / 32) {
+    const int64_t r = i < G1 ? int64_t(b) * G1 + i : n_tgt + int64_t(b) * gamma + (i - G1);
+    MS t{-INFINITY, 0.0f};
+    for (int cc = lane; cc < plan.chunks; cc += 32) {
+      const float2 pp = __ldcg(ws.part1 + r * plan.chunks + cc);
+      t = ms_merge(t, MS{pp.x, pp.y});
+    }
+    t = warp_ms(t);
+    if (lane == 0) {
+      s_stat[i] = make_float2(t.m, t.s);
+      ws.rowstat[r] = make_float2(t.m, t.s);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int n = gamma;
+    bool bad = false;
+    for (int i = 0; i < gamma; ++i) {
+      const int x = d[int64_t(b) * gamma + i];
+      float p = 0.0f, q = 0.0f, acc = 0.0f;
+      if (x >= 0 && x < V) {
+        const float lt = bf16_lo(Lt[(int64_t(b) * G1 + i) * V + x]);
+        const float ld = bf16_lo(Ld[(int64_t(b) * gamma + i) * V + x]);
+        p = __fdiv_rn(expf(lt - s_stat[i].x), s_stat[i].y);
+        q = __fdiv_rn(expf(ld - s_stat[G1 + i].x), s_stat[G1 + i].y);
+        acc = q == 0.0f ? 1.0f : fminf(1.0f, __fdiv_rn(p, q));
+      } else {
+        bad = true;  // an invalid draft token is rejected
+      }
+      if (accept_prob) accept_prob[int64_t(b) * gamma + i] = acc;
+      if (p_tok) p_tok[int64_t(b) * gamma + i] = p;
+      if (q_tok) q_tok[int64_t(b) * gamma + i] = q;
+      if (n == gamma && !(u_acc[int64_t(b) * gamma + i] < acc)) n = i;
+    }
+    if (bad) atomicOr(ws.err, kErrBadToken);
+    accept_len[b] = n;
+    for (int i = 0; i < G1; ++i)
+      if (i != n) out_tok[int64_t(b) * G1 + i] = i < n ? d[int64_t(b) * gamma + i] : -1;
+    ws.seq_n[b] = n;
+    ws.cnt1[b] = 0;
+  }
+}
+
+// ------------------------------------------------------------------ residual / bonus resampling
+
+struct RowPair {
+  const uint16_t* t;  // target row n
+  const uint16_t* q;  // draft row n (unused for the bonus row)
+  float mt, inv_st, md, inv_sd;
+  bool bonus;         // r = p (bonus token, or the p fallback when the residual sums to 0)
+};
+
+__device__ __forceinline__ float resid(const RowPair& rp, float lt, float ld) {
+  const float p = expf(lt - rp.mt) * rp.inv_st;
+  if (rp.bonus) return p;
+  return fmaxf(0.0f, p - expf(ld - rp.md) * rp.inv_sd);
+}
+
+// r values of this thread's kSeg2 contiguous elements of chunk c (zeros beyond V).
+template <bool kVec>
+__device__ __forceinline__ void seg_values(const RowPair& rp, int V, int c, float (&r)[kSeg2]) {
+  const int i0 = c * kChunk2 + threadIdx.x * kSeg2;
+  if (kVec && i0 + kSeg2 <= V) {
+    const uint4 ut = ld_stream_v4(rp.t + i0);
+    const uint4 uq = rp.bonus ? make_uint4(0, 0, 0, 0) : ld_stream_v4(rp.q + i0);
+    const uint32_t wt[4] = {ut.x, ut.y, ut.z, ut.w};
+    const uint32_t wq[4] = {uq.x, uq.y, uq.z, uq.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      r[2 * e] = resid(rp, bf16_lo(wt[e]), bf16_lo(wq[e]));
+      r[2 * e + 1] = resid(rp, bf16_hi(wt[e]), bf16_hi(wq[e]));
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < kSeg2; ++e) {
+      const int i = i0 + e;
+      r[e] = i < V ? resid(rp, bf16_lo(rp.t[i]), rp.bonus ? 0.0f : bf16_lo(rp.q[i])) : 0.0f;
+    }
+  }
+}
+
+__device__ __forceinline__ float block_sum(float v) {
+  __shared__ float sw[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+  if (lane == 0) sw[warp] = v;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) t += sw[w];
+  __syncthreads();
+  return t;
+}
+
+template <bool kVec>
+__device__ __forceinline__ float chunk_sum(const RowPair& rp, int V, int c) {
+  float r[kSeg2];
+  seg_values<kVec>(rp, V, c, r);
+  float s = 0.0f;
+#pragma unroll
+  for (int e = 0; e < kSeg2; ++e) s += r[e];
+  return block_sum(s);
+}
+
+// Index of the first element of chunk c whose running sum exceeds `target` (sums start at 0 at the
+// chunk's first element); if rounding leaves no such element, the last element with r > 0.
+// Returns -1 when the chunk has no positive element.
+template <bool kVec>
+__device__ int chunk_select(const RowPair& rp, int V, int c, float target) {
+  __shared__ float s_pref[kThreads];
+  __shared__ int s_hit, s_last_pos;
+  float r[kSeg2];
+  seg_values<kVec>(rp, V, c, r);
+  float seg = 0.0f;
+  int last_pos = -1;
+#pragma unroll
+  for (int e = 0; e < kSeg2; ++e) {
+    seg += r[e];
+    if (r[e] > 0.0f) last_pos = e;
+  }
+  if (threadIdx.x == 0) { s_hit = INT_MAX; s_last_pos = -1; }
+  // inclusive scan of the segment sums in thread order
+  s_pref[threadIdx.x] = seg;
+  __syncthreads();
+  for (int off = 1; off < kThreads; off <<= 1) {
+    const float add = threadIdx.x >= off ? s_pref[threadIdx.x - off] : 0.0f;
+    __syncthreads();
+    s_pref[threadIdx.x] += add;
+    __syncthreads();
+  }
+  const float incl = s_pref[threadIdx.x];
+  const float excl = threadIdx.x ? s_pref[threadIdx.x - 1] : 0.0f;
+  const int base = c * kChunk2 + threadIdx.x * kSeg2;
+  if (incl > target) {
+    float run = excl;
+    int j = -1;
+#pragma unroll
+    for (int e = 0; e < kSeg2; ++e) {
+      run += r[e];
+      if (j < 0 && run > target) j = e;
+    }
+    if (j < 0) j = last_pos;  // rounding: the segment sum crossed but no element did
+    if (j >= 0) atomicMin(&s_hit, (threadIdx.x << 8) | j);
+  }
+  if (last_pos >= 0) atomicMax(&s_last_pos, base + last_pos);
+  __syncthreads();
+  int res;
+  if (s_hit != INT_MAX) {
+    res = c * kChunk2 + (s_hit >> 8) * kSeg2 + (s_hit & 0xFF);
+  } else {
+    res = s_last_pos;
+  }
+  __syncthreads();
+  return res;
+}
+
+// Pass 2: per (sequence, chunk of 2048) residual mass of row n; the last CTA of a sequence walks
+// the chunk sums in index order and selects the token with the inverse CDF.
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) sample_pass2_kernel(
+    const uint16_t* __restrict__ Lt, const uint16_t* __restrict__ Ld,
+    const float* __restrict__ u_res, int B, int gamma, int V, int chunks2, WS ws,
+    int32_t* __restrict__ out_tok) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x / chunks2;
+  const int c = blockIdx.x % chunks2;
+  const int G1 = gamma + 1;
+  const int n = __ldcg(ws.seq_n + b);
+  RowPair rp;
+  rp.bonus = n == gamma;
+  const int64_t rt = int64_t(b) * G1 + n;
+  const int64_t rq = int64_t(B) * G1 + int64_t(b) * gamma + n;
+  const float2 st = __ldcg(ws.rowstat + rt);
+  rp.t = Lt + rt * V;
+  rp.mt = st.x;
+  rp.inv_st = 1.0f / st.y;
+  rp.q = rp.bonus ? nullptr : Ld + (int64_t(b) * gamma + n) * V;
+  if (!rp.bonus) {
+    const float2 sq = __ldcg(ws.rowstat + rq);
+    rp.md = sq.x;
+    rp.inv_sd = 1.0f / sq.y;
+  } else {
+    rp.md = 0.0f;
+    rp.inv_sd = 0.0f;
+  }
+  const float rc = chunk_sum<kVec>(rp, V, c);
+
+  __shared__ bool s_last;
+  if (threadIdx.x == 0) {
+    ws.part2[int64_t(b) * chunks2 + c] = rc;
+    __threadfence();
+    const unsigned int prev = atomicAdd(ws.cnt2 + b, 1u);
+    s_last = prev == static_cast<unsigned int>(chunks2 - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  __shared__ float s_R;
+  __shared__ int s_c, s_fallback;
+  __shared__ float s_before;
+  const float u = u_res[int64_t(b) * G1 + n];
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    if (attempt == 1) {
+      // The residual has no mass (p == q in fp32): draw from p instead.
+      rp.bonus = true;
+      for (int cc = 0; cc < chunks2; ++cc) {
+        const float s = chunk_sum<kVec>(rp, V, cc);
+        if (threadIdx.x == 0) ws.part2[int64_t(b) * chunks2 + cc] = s;
+      }
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      float R = 0.0f;
+      for (int cc = 0; cc < chunks2; ++cc) R += __ldcg(ws.part2 + int64_t(b) * chunks2 + cc);
+      s_R = R;
+      const float target = u * R;
+      float cum = 0.0f;
+      int found = -1, last_pos = -1;
+      float before = 0.0f;
+      for (int cc = 0; cc < chunks2; ++cc) {
+        const float rc2 = __ldcg(ws.part2 + int64_t(b) * chunks2 + cc);
+        if (rc2 > 0.0f) last_pos = cc;
+        if (found < 0 && cum + rc2 > target) { found = cc; before = cum; }
+        cum += rc2;
+      }
+      s_fallback = found < 0;
+      s_c = found < 0 ? last_pos : found;
+      s_before = before;
+    }
+    __syncthreads();
+    if (s_R > 0.0f || attempt == 1) break;
+    __syncthreads();
+  }
+  const int cs = s_c;
+  int j = -1;
+  if (cs >= 0) {
+    const float tgt = s_fallback ? INFINITY : u * s_R - s_before;
+    j = chunk_select<kVec>(rp, V, cs, tgt);
+  }
+  if (threadIdx.x == 0) {
+    out_tok[int64_t(b) * G1 + n] = j;
+    ws.cnt2[b] = 0;
+  }
+}
+
+qspec_status check_verify_args(const void* tgt, const int32_t* d, int B, int gamma, int V,
+                               const int32_t* accept_len, const int32_t* out_tok, void* ws,
+                               size_t ws_bytes) {
+  if (!tgt || !d || !accept_len || !out_tok) return QSPEC_ERR_INVALID_ARG;
+  if (B <= 0 || gamma <= 0 || V <= 0) return QSPEC_ERR_INVALID_ARG;
+  if (gamma > QSPEC_MAX_GAMMA || V < 2 || V > QSPEC_MAX_V ||
+      int64_t(B) * (2 * gamma + 1) * int64_t(V) >= (int64_t(1) << 40))
+    return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(tgt) || !aligned16(d) || !aligned16(accept_len) || !aligned16(out_tok))
+    return QSPEC_ERR_MISALIGNED;
+  if (!ws || !aligned16(ws)) return ws ? QSPEC_ERR_MISALIGNED : QSPEC_ERR_WORKSPACE;
+  if (ws_bytes < layout(B, gamma, V).total) return QSPEC_ERR_WORKSPACE;
+  return QSPEC_OK;
+}
+
+}  // namespace
+
+unsigned int* verify_error_word(void* ws) { return static_cast<unsigned int*>(ws); }
+
+}  // namespace qspec
+
+using namespace qspec;
+
+extern "C" size_t qspec_verify_workspace_size(int32_t B, int32_t gamma, int32_t V) {
+  if (B <= 0 || gamma <= 0 || gamma > QSPEC_MAX_GAMMA || V < 2 || V > QSPEC_MAX_V) return 0;
+  return layout(B, gamma, V).total;
+}
+
+extern "C" qspec_status qspec_verify_greedy(const uint16_t* tgt_logits, const int32_t* draft_tok,
+                                            int32_t B, int32_t gamma, int32_t V,
+                                            int32_t* accept_len, int32_t* out_tok,
+                                            int32_t* tgt_argmax, void* ws, size_t ws_bytes,
+                                            qspec_stream_t stream) {
+  qspec_status st = check_verify_args(tgt_logits, draft_tok, B, gamma, V, accept_len, out_tok, ws, ws_bytes);
+  if (st != QSPEC_OK) return st;
+  if (tgt_argmax && !aligned16(tgt_argmax)) return QSPEC_ERR_MISALIGNED;
+  const Layout L = layout(B, gamma, V);
+  const WS w = bind(ws, L);
+  const int64_t blocks = int64_t(B) * (gamma + 1) * L.pg.chunks;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (V % 8 == 0)
+    greedy_kernel<true><<<unsigned(blocks), kThreads, 0, s>>>(tgt_logits, draft_tok, gamma, V, L.pg, w,
+                                                              accept_len, out_tok, tgt_argmax);
+  else
+    greedy_kernel<false><<<unsigned(blocks), kThreads, 0, s>>>(tgt_logits, draft_tok, gamma, V, L.pg, w,
+                                                               accept_len, out_tok, tgt_argmax);
+  return launch_status();
+}
+
+extern "C" qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const uint16_t* draft_logits,
+                                            const int32_t* draft_tok, const float* u_accept,
+                                            const float* u_resample, int32_t B, int32_t gamma,
+                                            int32_t V, int32_t* accept_len, int32_t* out_tok,
+                                            float* accept_prob, float* p_tok, float* q_tok, void* ws,
+                                            size_t ws_bytes, qspec_stream_t stream) {
+  qspec_status st = check_verify_args(tgt_logits, draft_tok, B, gamma, V, accept_len, out_tok, ws, ws_bytes);
+  if (st != QSPEC_OK) return st;
+  if (!draft_logits || !u_accept || !u_resample) return QSPEC_ERR_INVALID_ARG;
+  if (!aligned16(draft_logits) || !aligned16(u_accept) || !aligned16(u_resample) ||
+      (accept_prob && !aligned16(accept_prob)) || (p_tok && !aligned16(p_tok)) || (q_tok && !aligned16(q_tok)))
+    return QSPEC_ERR_MISALIGNED;
+  const Layout L = layout(B, gamma, V);
+  const WS w = bind(ws, L);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t blocks1 = int64_t(B) * (2 * gamma + 1) * L.p1.chunks;
+  const bool vec = V % 8 == 0;
+  if (vec)
+    sample_pass1_kernel<true><<<unsigned(blocks1), kThreads, 0, s>>>(
+        tgt_logits, draft_logits, draft_tok, u_accept, B, gamma, V, L.p1, w, accept_len, out_tok,
+        accept_prob, p_tok, q_tok);
+  else
+    sample_pass1_kernel<false><<<unsigned(blocks1), kThreads, 0, s>>>(
+        tgt_logits, draft_logits, draft_tok, u_accept, B, gamma, V, L.p1, w, accept_len, out_tok,
+        accept_prob, p_tok, q_tok);
+  if (cudaGetLastError() != cudaSuccess) return QSPEC_ERR_CUDA;
+
+  // Pass 2 with programmatic dependent launch: its CTAs are scheduled while pass 1 drains and
+  // wait (griddepcontrol.wait) for pass 1 to complete before reading the workspace.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(int64_t(B) * L.chunks2));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (vec)
+    e = cudaLaunchKernelEx(&cfg, sample_pass2_kernel<true>, tgt_logits, draft_logits, u_resample, int(B),
+                           int(gamma), int(V), L.chunks2, w, out_tok);
+  else
+    e = cudaLaunchKernelEx(&cfg, sample_pass2_kernel<false>, tgt_logits, draft_logits, u_resample, int(B),
+                           int(gamma), int(V), L.chunks2, w, out_tok);
+  return e == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
+}

@@ -1,0 +1,192 @@
+"""Thin ctypes binding of libqspec.so: same names as the C ABI in include/qspec.h.
+
+Every function only marshals arguments (torch tensors -> device pointers and sizes, the current
+CUDA stream) and raises ``QSpecError`` on a non-OK status.  All computation happens in the CUDA
+library; there is no fallback of any kind -- if the library is missing, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqspec.so")
+
+STATUS = {
+    0: "QSPEC_OK",
+    1: "QSPEC_ERR_INVALID_ARG",
+    2: "QSPEC_ERR_UNSUPPORTED_SHAPE",
+    3: "QSPEC_ERR_MISALIGNED",
+    4: "QSPEC_ERR_WORKSPACE",
+    5: "QSPEC_ERR_CUDA",
+    6: "QSPEC_ERR_TIMEOUT",
+}
+
+# exported symbol -> (restype, argtypes)
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+SIGNATURES = {
+    "qspec_pack_weights": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+    "qspec_linear_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
+    "qspec_linear_w4a16": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _P, ctypes.c_size_t, _P]),
+    "qspec_linear_w4a4": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "qspec_verify_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32]),
+    "qspec_verify_greedy": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "qspec_verify_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                           ctypes.c_size_t, _P]),
+    "qspec_check_status": (ctypes.c_int, [_P, _P]),
+    "qspec_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+class QSpecError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libqspec.so (built by build.py / __graft_entry__.build()) and declare its signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libqspec.so not found at {p}: build it first (python -m "
+                           "quantized_speculative_decoding_qspec_gb300.build)")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise QSpecError(fn, code)
+
+
+def _dt(t, dtype, name):
+    if t is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def qspec_pack_weights(W, Wp, S, stream=None):
+    """W bf16 [N, K] -> Wp uint8 [N, K/2], S fp16 [N, K/128] (outputs written in place)."""
+    _dt(W, torch.bfloat16, "W"); _dt(Wp, torch.uint8, "Wp"); _dt(S, torch.float16, "S")
+    N, K = W.shape
+    _check("qspec_pack_weights", load().qspec_pack_weights(_ptr(W), N, K, _ptr(Wp), _ptr(S), _stream(stream)))
+
+
+def qspec_linear_workspace_size(M, N, K):
+    """Workspace bytes for an [M, K] x [N, K] product on the current device."""
+    return int(load().qspec_linear_workspace_size(M, N, K))
+
+
+def new_linear_workspace(M, N, K, device="cuda"):
+    """A zero-filled linear workspace (zero once; calls keep it ready)."""
+    n = qspec_linear_workspace_size(M, N, K)
+    if n == 0:
+        raise ValueError("invalid linear shape")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def qspec_linear_w4a16(x, Wp, S, y, ws, stream=None):
+    """y bf16 [M, N] = x bf16 [M, K] . dequant(Wp, S)^T."""
+    _dt(x, torch.bfloat16, "x"); _dt(Wp, torch.uint8, "Wp"); _dt(S, torch.float16, "S"); _dt(y, torch.bfloat16, "y")
+    _dt(ws, torch.uint8, "ws")
+    M, K = x.shape
+    N = Wp.shape[0]
+    _check("qspec_linear_w4a16",
+           load().qspec_linear_w4a16(_ptr(x), _ptr(Wp), _ptr(S), M, N, K, _ptr(y), _ptr(ws), ws.numel(),
+                                     _stream(stream)))
+
+
+def qspec_linear_w4a4(x, Wp, S, y, ws, xq_out=None, xs_out=None, acc_out=None, stream=None):
+    """Draft-mode linear with the per-token INT4 activation quantiser fused."""
+    _dt(x, torch.bfloat16, "x"); _dt(Wp, torch.uint8, "Wp"); _dt(S, torch.float16, "S"); _dt(y, torch.bfloat16, "y")
+    _dt(xq_out, torch.int8, "xq_out"); _dt(xs_out, torch.float32, "xs_out"); _dt(acc_out, torch.int32, "acc_out")
+    _dt(ws, torch.uint8, "ws")
+    M, K = x.shape
+    N = Wp.shape[0]
+    _check("qspec_linear_w4a4",
+           load().qspec_linear_w4a4(_ptr(x), _ptr(Wp), _ptr(S), M, N, K, _ptr(y), _ptr(xq_out), _ptr(xs_out),
+                                    _ptr(acc_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def qspec_verify_workspace_size(B, gamma, V):
+    return int(load().qspec_verify_workspace_size(B, gamma, V))
+
+
+def qspec_verify_greedy(tgt_logits, draft_tok, accept_len, out_tok, ws, tgt_argmax=None, stream=None):
+    """Greedy verify: tgt_logits bf16 [B, gamma+1, V], draft_tok int32 [B, gamma]."""
+    _dt(tgt_logits, torch.bfloat16, "tgt_logits"); _dt(draft_tok, torch.int32, "draft_tok")
+    _dt(accept_len, torch.int32, "accept_len"); _dt(out_tok, torch.int32, "out_tok")
+    _dt(tgt_argmax, torch.int32, "tgt_argmax"); _dt(ws, torch.uint8, "ws")
+    B, G1, V = tgt_logits.shape
+    _check("qspec_verify_greedy",
+           load().qspec_verify_greedy(_ptr(tgt_logits), _ptr(draft_tok), B, G1 - 1, V, _ptr(accept_len),
+                                      _ptr(out_tok), _ptr(tgt_argmax), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def qspec_verify_sample(tgt_logits, draft_logits, draft_tok, u_accept, u_resample, accept_len, out_tok, ws,
+                        accept_prob=None, p_tok=None, q_tok=None, stream=None):
+    """Sampling verify (min(1, p/q) test, residual / bonus resampling from the given uniforms)."""
+    _dt(tgt_logits, torch.bfloat16, "tgt_logits"); _dt(draft_logits, torch.bfloat16, "draft_logits")
+    _dt(draft_tok, torch.int32, "draft_tok"); _dt(u_accept, torch.float32, "u_accept")
+    _dt(u_resample, torch.float32, "u_resample"); _dt(accept_len, torch.int32, "accept_len")
+    _dt(out_tok, torch.int32, "out_tok"); _dt(ws, torch.uint8, "ws")
+    for name, t in (("accept_prob", accept_prob), ("p_tok", p_tok), ("q_tok", q_tok)):
+        _dt(t, torch.float32, name)
+    B, G1, V = tgt_logits.shape
+    _check("qspec_verify_sample",
+           load().qspec_verify_sample(_ptr(tgt_logits), _ptr(draft_logits), _ptr(draft_tok), _ptr(u_accept),
+                                      _ptr(u_resample), B, G1 - 1, V, _ptr(accept_len), _ptr(out_tok),
+                                      _ptr(accept_prob), _ptr(p_tok), _ptr(q_tok), _ptr(ws), ws.numel(),
+                                      _stream(stream)))
+
+
+def qspec_check_status(ws=None, stream=None):
+    """Synchronise the stream and raise on device-side errors (timeouts, invalid draft tokens)."""
+    _check("qspec_check_status", load().qspec_check_status(_ptr(ws), _stream(stream)))
+
+
+def qspec_status_string(code: int) -> str:
+    return load().qspec_status_string(int(code)).decode()
+
+
+def new_verify_workspace(B, gamma, V, device="cuda"):
+    """A zero-filled verify workspace of the required size (zero once; calls keep it ready)."""
+    n = qspec_verify_workspace_size(B, gamma, V)
+    if n == 0:
+        raise ValueError("invalid verify shape")
+    return torch.zeros(n, dtype=torch.uint8, device=device)

@@ -46,13 +46,20 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     NaN maps to the canonical quiet NaN 0x7FC0; +-inf and overflow map to +-inf.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    rounded = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
-    nan = np.isnan(x)
-    if nan.any():
-        rounded = np.where(nan, np.uint16(0x7FC0), rounded)
-    return rounded
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint16)
+    step = 1 << 24
+    for i in range(0, flat.size, step):  # bounded temporaries for large tensors
+        f = flat[i:i + step]
+        u = f.view(np.uint32)
+        nan = np.isnan(f)
+        # finite inputs: u + 0x7FFF + lsb stays below 2**32, so uint32 arithmetic is exact
+        r = ((np.where(nan, np.uint32(0), u) + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))
+             >> np.uint32(16)).astype(np.uint16)
+        if nan.any():
+            r = np.where(nan, np.uint16(0x7FC0), r)
+        out[i:i + step] = r
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

@@ -1,0 +1,120 @@
+"""The C-ABI library loads and exports every entry point of include/qspec.h; host-side argument
+checks reject bad calls before anything reaches a GPU (no compute is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qspec.h")
+
+
+def declared_symbols():
+    src = open(HEADER, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qspec_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+    return q.load()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ["qspec_pack_weights", "qspec_linear_w4a16", "qspec_linear_w4a4", "qspec_linear_workspace_size",
+                 "qspec_verify_greedy",
+                 "qspec_verify_sample", "qspec_verify_workspace_size", "qspec_check_status",
+                 "qspec_status_string"]:
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_declared_symbol():
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+    for name in declared_symbols():
+        assert name in q.SIGNATURES, name
+        assert callable(getattr(q, name, None)), name
+
+
+def test_status_strings(lib):
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+    for code, name in q.STATUS.items():
+        assert lib.qspec_status_string(code).decode() == name
+    assert lib.qspec_status_string(99).decode() == "QSPEC_ERR_UNKNOWN"
+
+
+FAKE = 1 << 20          # a 16-byte-aligned stand-in address; never dereferenced (checks fail first)
+
+
+def test_pack_argument_checks(lib):
+    assert lib.qspec_pack_weights(None, 8, 128, FAKE, FAKE, None) == 1
+    assert lib.qspec_pack_weights(FAKE, 0, 128, FAKE, FAKE, None) == 1
+    assert lib.qspec_pack_weights(FAKE, 8, 100, FAKE, FAKE, None) == 2
+    assert lib.qspec_pack_weights(FAKE + 8, 8, 128, FAKE, FAKE, None) == 3
+
+
+def test_linear_argument_checks(lib):
+    f16, f4 = lib.qspec_linear_w4a16, lib.qspec_linear_w4a4
+    W = 1 << 16
+    assert f16(FAKE, FAKE, FAKE, 4, 512, 256, None, FAKE, W, None) == 1
+    assert f16(FAKE, FAKE, FAKE, 0, 512, 256, FAKE, FAKE, W, None) == 1
+    assert f16(FAKE, FAKE, FAKE, 4097, 512, 256, FAKE, FAKE, W, None) == 2    # M above the limit
+    assert f16(FAKE, FAKE, FAKE, 4, 510, 256, FAKE, FAKE, W, None) == 2       # N % 8 != 0
+    assert f16(FAKE, FAKE, FAKE, 4, 512, 200, FAKE, FAKE, W, None) == 2       # K % 128 != 0
+    assert f16(FAKE, FAKE + 4, FAKE, 4, 512, 256, FAKE, FAKE, W, None) == 3
+    assert f16(FAKE, FAKE, FAKE, 4, 512, 256, FAKE, None, W, None) == 4       # no workspace
+    assert f16(FAKE, FAKE, FAKE, 4, 512, 256, FAKE, FAKE + 8, W, None) == 3
+    assert f4(FAKE, FAKE, FAKE, 4, 512, 256, FAKE, FAKE + 1, None, None, FAKE, W, None) == 3
+    assert f4(FAKE, FAKE, FAKE, 4, 512, 256, FAKE, None, None, FAKE + 2, FAKE, W, None) == 3
+    assert f4(FAKE, FAKE, FAKE, 4, 512, 384 + 1, FAKE, None, None, None, FAKE, W, None) == 2
+    assert f4(FAKE, FAKE, FAKE, 4, 512, 256, FAKE, None, None, None, None, W, None) == 4
+
+
+def test_linear_workspace_size_rejects_bad_shapes(lib):
+    assert lib.qspec_linear_workspace_size(0, 512, 256) == 0
+    assert lib.qspec_linear_workspace_size(4, 510, 256) == 0
+    assert lib.qspec_linear_workspace_size(4, 512, 200) == 0
+    assert lib.qspec_linear_workspace_size(4097, 512, 256) == 0
+
+
+def test_verify_workspace_size(lib):
+    assert lib.qspec_verify_workspace_size(0, 3, 1024) == 0
+    assert lib.qspec_verify_workspace_size(1, 0, 1024) == 0
+    assert lib.qspec_verify_workspace_size(1, 17, 1024) == 0
+    assert lib.qspec_verify_workspace_size(1, 3, 1) == 0
+    small = lib.qspec_verify_workspace_size(1, 3, 1024)
+    big = lib.qspec_verify_workspace_size(64, 7, 152064)
+    assert 0 < small < big and small % 256 == 0 and big % 256 == 0
+
+
+def test_verify_argument_checks(lib):
+    g = lib.qspec_verify_greedy
+    need = lib.qspec_verify_workspace_size(2, 3, 1024)
+    assert g(FAKE, FAKE, 2, 3, 1024, FAKE, FAKE, None, FAKE, need - 1, None) == 4
+    assert g(FAKE, FAKE, 2, 3, 1024, FAKE, FAKE, None, None, need, None) == 4
+    assert g(FAKE, FAKE, 2, 17, 1024, FAKE, FAKE, None, FAKE, need, None) == 2
+    assert g(FAKE, FAKE, 2, 3, 1, FAKE, FAKE, None, FAKE, need, None) == 2
+    assert g(None, FAKE, 2, 3, 1024, FAKE, FAKE, None, FAKE, need, None) == 1
+    assert g(FAKE, FAKE, 2, 3, 1024, FAKE + 4, FAKE, None, FAKE, need, None) == 3
+    s = lib.qspec_verify_sample
+    assert s(FAKE, None, FAKE, FAKE, FAKE, 2, 3, 1024, FAKE, FAKE, None, None, None, FAKE, need, None) == 1
+    assert s(FAKE, FAKE, FAKE, FAKE + 8, FAKE, 2, 3, 1024, FAKE, FAKE, None, None, None, FAKE, need, None) == 3
+    assert s(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 1024, FAKE, FAKE, None, None, None, FAKE, 16, None) == 4
+
+
+def test_product_path_has_no_fallback():
+    """The binding never imports the oracle and fails loudly without the library."""
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+    src = open(q.__file__, encoding="utf-8").read()
+    assert "oracle" not in src.replace("no fallback", "")
+    with pytest.raises(RuntimeError):
+        q.load(os.path.join(ROOT, "does_not_exist.so"))

@@ -29,7 +29,7 @@ MUTATIONS = [
     ("w4a4 groups strided", 'acc = np.einsum("mgk,ngk->mng", qa.reshape(M, G, GROUP), codes.reshape(N, G, GROUP))',
      'acc = np.einsum("mkg,nkg->mng", qa.reshape(M, GROUP, G), codes.reshape(N, GROUP, G))'),
     ("softmax without max shift", "e = np.exp(l - m)", "e = np.exp(l)"),
-    ("argmax takes the last tie", "for j in range(v.shape[0]):", "for j in reversed(range(v.shape[0])):"),
+    ("argmax takes the last tie", "return int(hits[0])", "return int(hits[-1])"),
     ("greedy drops the target token", "out[b, k] = t[b, k]", "out[b, k] = t[b, k] if k < gamma else -1"),
     ("greedy compares with the next position", "int(d[b, k]) == int(t[b, k])", "int(d[b, k]) == int(t[b, k + 1])"),
     ("accept test not strict", "if not (float(u_acc[i]) < a[i]):", "if not (float(u_acc[i]) <= a[i]):"),

@@ -179,6 +179,31 @@ qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const uint16_t* dra
                                  qspec_stream_t stream);
 
 /*
+ * qspec_verify_greedy_noalloc -- qspec_verify_greedy for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart of this entry point.  Some callers cannot call cudaMalloc where they
+ * verify: code running while a CUDA graph is captured, plug-ins executing inside another runtime's
+ * fixed memory plan, or C hosts with no allocator at hand.  This variant takes no workspace: its
+ * scratch (error word, per-sequence tickets, per-chunk partial argmaxes) is a fixed array of
+ * QSPEC_NOALLOC_SCRATCH_BYTES of device memory inside the library, which every GPU that loads the
+ * library holds until the process exits.  It allocates nothing and calls no allocating routine.
+ *
+ *   Arguments and results as qspec_verify_greedy (bit-identical outputs), without ws / ws_bytes.
+ *   Shapes whose scratch would exceed QSPEC_NOALLOC_SCRATCH_BYTES are rejected with
+ *   QSPEC_ERR_UNSUPPORTED_SHAPE before anything is enqueued (B*(gamma+1) up to about 32 000 rows fit).
+ *   The first call on a device looks up the array's device address (once per device, with that
+ *   device current); make that first call before any stream capture.
+ *   Every call shares the one array and clears its error word and tickets on `stream` first, so
+ *   calls that overlap on the GPU (different streams, or concurrent graphs) race and must not be
+ *   issued.  Draft-token range errors are not reported by qspec_check_status for this variant;
+ *   out-of-range tokens simply never match.
+ */
+#define QSPEC_NOALLOC_SCRATCH_BYTES (256 * 1024)
+qspec_status qspec_verify_greedy_noalloc(const uint16_t* tgt_logits, const int32_t* draft_tok,
+                                         int32_t B, int32_t gamma, int32_t V, int32_t* accept_len,
+                                         int32_t* out_tok, int32_t* tgt_argmax, qspec_stream_t stream);
+
+/*
  * qspec_check_status -- synchronises `stream`, then reports (and clears) the error words that the
  * kernels set on the device: the verify workspace's word when `ws` is not NULL, and the library's
  * own word for the linear kernels of the current device.  QSPEC_ERR_TIMEOUT if a kernel gave up a

@@ -14,6 +14,8 @@
 #include <limits.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace qspec {
@@ -677,4 +679,78 @@ extern "C" qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const ui
     e = cudaLaunchKernelEx(&cfg, sample_pass2_kernel<false>, tgt_logits, draft_logits, u_resample, int(B),
                            int(gamma), int(V), L.chunks2, w, out_tok);
   return e == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ allocation-free greedy verify
+//
+// Some callers cannot allocate device memory at the point where they verify: code that runs while
+// a CUDA graph is being captured, plug-ins that execute inside another runtime's memory plan (a
+// serving engine that forbids allocation during a decode step), or plain C hosts without access to
+// an allocator.  For them, qspec_verify_greedy_noalloc uses scratch memory that lives inside this
+// library: a fixed array of device memory that every GPU loading the library holds until exit.
+// The pages have no counterpart of this; it is a deployment convenience only.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = QSPEC_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  cudaGetSymbolAddress runs once per
+// device, with that device current, on the first call made there.
+qspec_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QSPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return QSPEC_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return QSPEC_OK;
+}
+
+}  // namespace
+
+extern "C" qspec_status qspec_verify_greedy_noalloc(const uint16_t* tgt_logits, const int32_t* draft_tok,
+                                                    int32_t B, int32_t gamma, int32_t V,
+                                                    int32_t* accept_len, int32_t* out_tok,
+                                                    int32_t* tgt_argmax, qspec_stream_t stream) {
+  if (!tgt_logits || !draft_tok || !accept_len || !out_tok) return QSPEC_ERR_INVALID_ARG;
+  if (B <= 0 || gamma <= 0 || V <= 0) return QSPEC_ERR_INVALID_ARG;
+  if (gamma > QSPEC_MAX_GAMMA || V < 2 || V > QSPEC_MAX_V ||
+      int64_t(B) * (gamma + 1) * int64_t(V) >= (int64_t(1) << 40))
+    return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(tgt_logits) || !aligned16(draft_tok) || !aligned16(accept_len) || !aligned16(out_tok) ||
+      (tgt_argmax && !aligned16(tgt_argmax)))
+    return QSPEC_ERR_MISALIGNED;
+  // compact layout: error word, per-sequence tickets, per-(row, chunk) partial argmaxes
+  const Plan plan = plan_rows(int64_t(B) * (gamma + 1), V);
+  const size_t off_cnt = 256;
+  const size_t off_part = align256(off_cnt + sizeof(unsigned int) * size_t(B));
+  const size_t need = off_part + sizeof(float2) * size_t(B) * (gamma + 1) * plan.chunks;
+  if (need > kNoAllocScratchBytes) return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  void* base = nullptr;
+  const qspec_status st = noalloc_scratch(&base);
+  if (st != QSPEC_OK) return st;
+  char* p = static_cast<char*>(base);
+  WS w{};
+  w.err = reinterpret_cast<unsigned int*>(p);
+  w.cnt1 = reinterpret_cast<unsigned int*>(p + off_cnt);
+  w.part1 = reinterpret_cast<float2*>(p + off_part);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the error word and the tickets must start at 0
+  if (cudaMemsetAsync(p, 0, off_part, s) != cudaSuccess) return QSPEC_ERR_CUDA;
+  const int64_t blocks = int64_t(B) * (gamma + 1) * plan.chunks;
+  if (V % 8 == 0)
+    greedy_kernel<true><<<unsigned(blocks), kThreads, 0, s>>>(tgt_logits, draft_tok, gamma, V, plan, w,
+                                                              accept_len, out_tok, tgt_argmax);
+  else
+    greedy_kernel<false><<<unsigned(blocks), kThreads, 0, s>>>(tgt_logits, draft_tok, gamma, V, plan, w,
+                                                               accept_len, out_tok, tgt_argmax);
+  return launch_status();
 }

@@ -37,6 +37,7 @@ SIGNATURES = {
     "qspec_verify_greedy": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qspec_verify_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                            ctypes.c_size_t, _P]),
+    "qspec_verify_greedy_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
     "qspec_check_status": (ctypes.c_int, [_P, _P]),
     "qspec_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -156,6 +157,17 @@ def qspec_verify_greedy(tgt_logits, draft_tok, accept_len, out_tok, ws, tgt_argm
     _check("qspec_verify_greedy",
            load().qspec_verify_greedy(_ptr(tgt_logits), _ptr(draft_tok), B, G1 - 1, V, _ptr(accept_len),
                                       _ptr(out_tok), _ptr(tgt_argmax), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def qspec_verify_greedy_noalloc(tgt_logits, draft_tok, accept_len, out_tok, tgt_argmax=None, stream=None):
+    """Greedy verify without a workspace (scratch inside the library; for callers that cannot allocate)."""
+    _dt(tgt_logits, torch.bfloat16, "tgt_logits"); _dt(draft_tok, torch.int32, "draft_tok")
+    _dt(accept_len, torch.int32, "accept_len"); _dt(out_tok, torch.int32, "out_tok")
+    _dt(tgt_argmax, torch.int32, "tgt_argmax")
+    B, G1, V = tgt_logits.shape
+    _check("qspec_verify_greedy_noalloc",
+           load().qspec_verify_greedy_noalloc(_ptr(tgt_logits), _ptr(draft_tok), B, G1 - 1, V, _ptr(accept_len),
+                                              _ptr(out_tok), _ptr(tgt_argmax), _stream(stream)))
 
 
 def qspec_verify_sample(tgt_logits, draft_logits, draft_tok, u_accept, u_resample, accept_len, out_tok, ws,

@@ -476,8 +476,68 @@ def gpu_arm(args, rank, world):
     return result
 
 
+def profile_case(spec, reps):
+    """Run one kernel of the step repeatedly (for profilers): LAYER:MODE:M, e.g. lm_head:a4:1,
+    or verify:greedy / verify:sample on the step's logits."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as g
+    g.build()
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+    from quantized_speculative_decoding_qspec_gb300 import synthetic as syn
+    dev = torch.device("cuda", 0)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    parts = spec.split(":")
+    if parts[0] == "verify":
+        vd = verify_data()
+        tgt, drf = bf(vd["tgt"]), bf(vd["drf"])
+        d = torch.from_numpy(vd["d_greedy" if parts[1] == "greedy" else "d_sample"]).to(dev)
+        ua, ur = torch.from_numpy(vd["u_acc"]).to(dev), torch.from_numpy(vd["u_res"]).to(dev)
+        ws = q.new_verify_workspace(1, GAMMA, VOCAB, device=dev)
+        n = torch.empty(1, dtype=torch.int32, device=dev)
+        o = torch.empty(1, GAMMA + 1, dtype=torch.int32, device=dev)
+        fn = ((lambda: q.qspec_verify_greedy(tgt, d, n, o, ws)) if parts[1] == "greedy"
+              else (lambda: q.qspec_verify_sample(tgt, drf, d, ua, ur, n, o, ws)))
+        nbytes = verify_bytes(1, GAMMA, VOCAB, parts[1] != "greedy")
+    else:
+        name, mode, M = parts[0], parts[1], int(parts[2])
+        li = [l[0] for l in LAYERS].index(name)
+        _, N, K = LAYERS[li]
+        W = bf(syn.weights(N, K, 1, layer=li))
+        Wp = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+        S = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+        q.qspec_pack_weights(W, Wp, S)
+        del W
+        x = bf(syn.activations(M, K, 1, step=10 * li))
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        ws = q.new_linear_workspace(M, N, K, device=dev)
+        fn = ((lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws)) if mode == "a4"
+              else (lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws)))
+        nbytes = linear_bytes(M, N, K)
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+    q.qspec_check_status()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / reps
+    print(json.dumps({"case": spec, "us_per_launch": round(t * 1e6, 2), "GB_s": round(nbytes / t / 1e9, 1),
+                      "note": "eager back-to-back launches; inputs resident"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", default=None,
+                    help="run only one kernel of the step, e.g. lm_head:a4:1 or verify:greedy (for ncu)")
+    ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
@@ -490,6 +550,9 @@ def main():
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.profile_case:
+        profile_case(args.profile_case, args.reps)
+        return
 
     if args.impl == "reference":
         if rank != 0:

@@ -85,26 +85,27 @@ struct TcArgs {
   float* xs_out;
 };
 
+constexpr uint32_t kSuspendNs = 2000;  // hardware suspend per try_wait while a phase is incomplete
+
 // Bounded wait: false if it gave up (then the whole CTA runs in abort mode).
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  if (*abort_flag) return false;
+  if (mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (true) {
     if (*abort_flag) return false;
+    if (mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
     if (clock64() - t0 > kWaitLimit) {
       *abort_flag = 1;
       atomicOr(&g_linear_error, 1u);
       return false;
     }
   }
-  return true;
 }
 
 // Wait that ignores the abort flag (used to let in-flight copies land before exit); bounded.
 __device__ __forceinline__ void wait_bar_final(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_hint(bar, parity, kSuspendNs)) {
     if (clock64() - t0 > kWaitLimit) {
       atomicOr(&g_linear_error, 1u);
       return;
@@ -112,28 +113,46 @@ __device__ __forceinline__ void wait_bar_final(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Stages of one CTA's unit range [u_beg, u_end): a stage is up to two consecutive groups of one tile.
+// Stages of one CTA's unit range [u_beg, u_end): a stage is up to two consecutive groups of one
+// tile.  Tiles are numbered n-major (tile = n_tile * T_m + m_tile); everything is advanced
+// incrementally in 32-bit arithmetic (one division per CTA).
 struct StageIter {
-  long long u, u_beg, u_end;
-  int G;
-  long long tile;
-  int g, ng;
-  bool last;  // last stage of this tile within the CTA
-  __device__ StageIter(long long ub, long long ue, int G_) : u(ub), u_beg(ub), u_end(ue), G(G_) {}
+  uint32_t u, u_end, G, T_m;
+  uint32_t tile, g, n_tile, m_tile;  // current position
+  uint32_t cur_g, cur_ng, cur_tile, cur_n_tile, cur_m_tile;
+  bool cur_last;
+  __device__ StageIter(uint32_t ub, uint32_t ue, uint32_t G_, uint32_t T_m_) : u(ub), u_end(ue), G(G_), T_m(T_m_) {
+    tile = ub / G_;
+    g = ub - tile * G_;
+    n_tile = tile / T_m_;
+    m_tile = tile - n_tile * T_m_;
+  }
   __device__ bool next() {
     if (u >= u_end) return false;
-    tile = u / G;
-    g = static_cast<int>(u - tile * G);
-    const long long tile_end = min((tile + 1) * static_cast<long long>(G), u_end);
-    ng = static_cast<int>(min(2LL, tile_end - u));
-    u += ng;
-    last = u == tile_end;
+    cur_g = g;
+    cur_tile = tile;
+    cur_n_tile = n_tile;
+    cur_m_tile = m_tile;
+    const uint32_t left_tile = G - g, left_cta = u_end - u;
+    const uint32_t left = left_tile < left_cta ? left_tile : left_cta;
+    cur_ng = left < 2 ? left : 2;
+    cur_last = cur_ng == left;
+    u += cur_ng;
+    g += cur_ng;
+    if (g == G) {
+      g = 0;
+      ++tile;
+      if (++m_tile == T_m) {
+        m_tile = 0;
+        ++n_tile;
+      }
+    }
     return true;
   }
 };
 
-__device__ __forceinline__ long long owner_of(long long u, long long U, long long P) {
-  return ((u + 1) * P - 1) / U;
+__device__ __forceinline__ uint32_t owner_of(uint32_t u, uint32_t U, uint32_t P) {
+  return static_cast<uint32_t>(((static_cast<uint64_t>(u) + 1) * P - 1) / U);
 }
 
 // 8 INT4 codes (one little-endian word, k = 8w + i in bits 4i..4i+3) -> 4 bf16x2 words holding
@@ -209,28 +228,30 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   grid_launch_dependents();
   grid_dependency_wait();
 
-  const long long P = gridDim.x, c = blockIdx.x;
-  const long long u_beg = c * a.U / P, u_end = (c + 1) * a.U / P;
+  const uint32_t P = gridDim.x, c = blockIdx.x;
+  const uint32_t U = static_cast<uint32_t>(a.U);
+  const uint32_t u_beg = static_cast<uint32_t>(static_cast<uint64_t>(c) * U / P);
+  const uint32_t u_end = static_cast<uint32_t>(static_cast<uint64_t>(c + 1) * U / P);
   const int G = a.G;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       fence_proxy_async_global();
-      StageIter it(u_beg, u_end, G);
+      StageIter it(u_beg, u_end, G, a.T_m);
       int s = 0, issued = 0;
       while (it.next()) {
         const int slot = s % NS;
         if (s >= NS) wait_bar(empty + slot, ((s / NS) - 1) & 1, abort_flag);
         if (!*abort_flag) {
           ++issued;
-          const int n_tile = static_cast<int>(it.tile / a.T_m), m_tile = static_cast<int>(it.tile % a.T_m);
           uint8_t* st = ring + slot * SB;
           mbar_arrive_expect_tx(full + slot, SB);
-          tma_load_2d(st, &tmW, full + slot, it.g * 64, n_tile * 128);
+          tma_load_2d(st, &tmW, full + slot, static_cast<int>(it.cur_g * 64), static_cast<int>(it.cur_n_tile * 128));
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tma_load_2d(st + kWBytes + j * (NM * 128), &tmX, full + slot, it.g * 128 + 64 * j, m_tile * a.NMrows);
+            tma_load_2d(st + kWBytes + j * (NM * 128), &tmX, full + slot, static_cast<int>(it.cur_g * 128 + 64 * j),
+                        static_cast<int>(it.cur_m_tile * a.NMrows));
         }
         ++s;
       }
@@ -241,7 +262,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, NM);
-      StageIter it(u_beg, u_end, G);
+      StageIter it(u_beg, u_end, G, a.T_m);
       int s = 0;
       while (it.next()) {
         const int slot = s % NS, pa = s & 1;
@@ -252,7 +273,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           tc_fence_after();
           const uint32_t a_base = tmem + pa * 128;
           const uint32_t b_base = smem_u32(ring + slot * SB + kWBytes);
-          for (int j = 0; j < it.ng; ++j) {
+          for (int j = 0; j < static_cast<int>(it.cur_ng); ++j) {
             const uint32_t d = tmem + 256 + (pa * 2 + j) * NM;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -272,29 +293,66 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ group-scale stager
-    StageIter it(u_beg, u_end, G);
-    int s = 0;
-    while (it.next()) {
-      const int slot = s % NS;
-      if (s >= NS) wait_bar(empty + slot, ((s / NS) - 1) & 1, abort_flag);
-      const int n0 = static_cast<int>(it.tile / a.T_m) * 128;
-      __half* dst = sc + slot * 256;
+    // Lane l stages rows 4l..4l+3 of the tile (two groups each).  Loads run two batches of
+    // kScaleBatch stages ahead of the stores so that their latency overlaps the weight stream.
+    constexpr int kScaleBatch = 4;
+    struct Batch {
+      int n0[kScaleBatch], ng[kScaleBatch];
+      int count;
+      __half v[kScaleBatch][8];
+    };
+    StageIter it(u_beg, u_end, G, a.T_m);
+    auto fetch = [&](Batch& b) {
+      b.count = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = lane * 4 + i;
-        const int n = n0 + r;
-        __half s0 = __ushort_as_half(0), s1 = __ushort_as_half(0);
-        if (n < a.N) {
-          const __half* srow = a.S + static_cast<long long>(n) * G + it.g;
-          s0 = __ldg(srow);
-          if (it.ng == 2) s1 = __ldg(srow + 1);
+      for (int j = 0; j < kScaleBatch; ++j) {
+        b.ng[j] = 0;
+        b.n0[j] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) b.v[j][i] = __ushort_as_half(0);
+        if (b.count == j && it.next()) {
+          b.count = j + 1;
+          b.ng[j] = static_cast<int>(it.cur_ng);
+          b.n0[j] = static_cast<int>(it.cur_n_tile) * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int n = b.n0[j] + lane * 4 + i;
+            if (n < a.N) {
+              const __half* srow = a.S + static_cast<long long>(n) * G + it.cur_g;
+              b.v[j][2 * i] = __ldg(srow);
+              if (it.cur_ng == 2) b.v[j][2 * i + 1] = __ldg(srow + 1);
+            }
+          }
         }
-        dst[r] = s0;
-        dst[128 + r] = s1;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(full + slot);
-      ++s;
+    };
+    int s = 0;
+    auto store = [&](const Batch& b) {
+#pragma unroll
+      for (int j = 0; j < kScaleBatch; ++j) {
+        if (j < b.count) {
+          const int slot = s % NS;
+          if (s >= NS) wait_bar(empty + slot, ((s / NS) - 1) & 1, abort_flag);
+          __half* dst = sc + slot * 256;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            dst[lane * 4 + i] = b.v[j][2 * i];
+            dst[128 + lane * 4 + i] = b.v[j][2 * i + 1];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full + slot);
+          ++s;
+        }
+      }
+      return b.count == kScaleBatch;
+    };
+    Batch A, B;
+    fetch(A);
+    while (true) {
+      fetch(B);
+      if (!store(A)) break;
+      fetch(A);
+      if (!store(B)) break;
     }
   } else {
     // ------------------------------------------------------------------ workers: dequant + drain
@@ -343,7 +401,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
     struct Pending {
       int s, ng, g;
-      long long tile;
+      uint32_t tile;
+      int n_tile, m_tile;
       bool last;
       float s0, s1;
     } prev{};
@@ -377,8 +436,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       }
       if constexpr (MODE != kA16) {
         if (a.acc_out) {
-          const int n = static_cast<int>(p.tile / a.T_m) * 128 + row;
-          const int m0 = static_cast<int>(p.tile % a.T_m) * a.NMrows + h * HALF;
+          const int n = p.n_tile * 128 + row;
+          const int m0 = p.m_tile * a.NMrows + h * HALF;
 #pragma unroll
           for (int t = 0; t < HALF; ++t) {
             const int m = m0 + t;
@@ -398,9 +457,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       else return 1.0f;
     };
 
-    auto store_y = [&](long long tile, const float* v) {
-      const int n = static_cast<int>(tile / a.T_m) * 128 + row;
-      const int m0 = static_cast<int>(tile % a.T_m) * a.NMrows + h * HALF;
+    auto store_y = [&](const Pending& p, const float* v) {
+      const int n = p.n_tile * 128 + row;
+      const int m0 = p.m_tile * a.NMrows + h * HALF;
 #pragma unroll
       for (int t = 0; t < HALF; ++t) {
         const int m = m0 + t;
@@ -412,14 +471,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       }
     };
 
-    auto epilogue = [&](long long tile) {
-      const long long c_first = owner_of(tile * G, a.U, P);
-      const long long c_last = owner_of((tile + 1) * G - 1, a.U, P);
+    auto epilogue = [&](const Pending& p) {
+      const uint32_t tile = p.tile;
+      const uint32_t c_first = owner_of(tile * G, U, P);
+      const uint32_t c_last = owner_of((tile + 1) * G - 1, U, P);
       if (c_first == c_last) {
-        if (!*abort_flag) store_y(tile, acc);
+        if (!*abort_flag) store_y(p, acc);
       } else {
         const int my_slot = (tile == u_beg / G) ? 0 : 1;
-        float* part = a.partial + ((c * 2 + my_slot) * 128 + row) * NM + h * HALF;
+        float* part = a.partial + ((static_cast<size_t>(c) * 2 + my_slot) * 128 + row) * NM + h * HALF;
 #pragma unroll
         for (int t = 0; t < HALF; t += 4) *reinterpret_cast<float4*>(part + t) = make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
         __threadfence();
@@ -434,9 +494,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           float sum[HALF];
 #pragma unroll
           for (int t = 0; t < HALF; ++t) sum[t] = 0.0f;
-          for (long long cc = c_first; cc <= c_last; ++cc) {
-            const int sl = (tile == (cc * a.U / P) / G) ? 0 : 1;
-            const float* src = a.partial + ((cc * 2 + sl) * 128 + row) * NM + h * HALF;
+          for (uint32_t cc = c_first; cc <= c_last; ++cc) {
+            const uint32_t cc_beg = static_cast<uint32_t>(static_cast<uint64_t>(cc) * U / P);
+            const int sl = (tile == cc_beg / G) ? 0 : 1;
+            const float* src = a.partial + ((static_cast<size_t>(cc) * 2 + sl) * 128 + row) * NM + h * HALF;
 #pragma unroll
             for (int t = 0; t < HALF; t += 4) {
               const float4 v = __ldcg(reinterpret_cast<const float4*>(src + t));
@@ -446,7 +507,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
               sum[t + 3] += v.w;
             }
           }
-          if (!*abort_flag) store_y(tile, sum);
+          if (!*abort_flag) store_y(p, sum);
           if (wt == 0) a.ticket[tile] = 0;
         }
       }
@@ -454,13 +515,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       for (int t = 0; t < HALF; ++t) acc[t] = 0.0f;
     };
 
-    StageIter it(u_beg, u_end, G);
+    StageIter it(u_beg, u_end, G, a.T_m);
     int s = 0;
     while (it.next()) {
       const int slot = s % NS, pa = s & 1;
       bool ok = wait_bar(full + slot, (s / NS) & 1, abort_flag);
       if (s >= 2) ok = wait_bar(afree + pa, ((s >> 1) - 1) & 1, abort_flag) && ok;
-      Pending cur{s, it.ng, it.g, it.tile, it.last, 0.0f, 0.0f};
+      Pending cur{s, static_cast<int>(it.cur_ng), static_cast<int>(it.cur_g), it.cur_tile,
+                  static_cast<int>(it.cur_n_tile), static_cast<int>(it.cur_m_tile), it.cur_last, 0.0f, 0.0f};
       if (ok && !*abort_flag) {
         cur.s0 = __half2float(sc[slot * 256 + row]);
         cur.s1 = __half2float(sc[slot * 256 + 128 + row]);
@@ -479,7 +541,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
           fence_proxy_async_smem();
         }
-        if (h < it.ng) {
+        if (h < static_cast<int>(it.cur_ng)) {
           const uint8_t* wrow = st + row * 128;
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
@@ -502,7 +564,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       }
       if (has_prev) {
         drain(prev);
-        if (prev.last) epilogue(prev.tile);
+        if (prev.last) epilogue(prev);
       }
       prev = cur;
       has_prev = true;
@@ -510,7 +572,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     }
     if (has_prev) {
       drain(prev);
-      if (prev.last) epilogue(prev.tile);
+      if (prev.last) epilogue(prev);
     }
   }
 
@@ -631,8 +693,11 @@ qspec_status launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcA
 
 }  // namespace
 
-bool linear_tc_supported(bool, int M, int N, int K) {
-  return M >= 1 && M <= QSPEC_MAX_M && N >= 8 && K >= kGroup && encode_fn() != nullptr;
+bool linear_tc_supported(bool a4, int M, int N, int K) {
+  if (M < 1 || M > QSPEC_MAX_M || N < 8 || K < kGroup) return false;
+  const int NM = pick_nm(a4, M);
+  const long long U = (static_cast<long long>(N) + 127) / 128 * ((M + NM - 1) / NM) * (K / kGroup);
+  return U < (1LL << 31) && encode_fn() != nullptr;  // the device side counts units in 32 bits
 }
 
 size_t linear_tc_workspace_size(bool a4, int M, int N, int K) {

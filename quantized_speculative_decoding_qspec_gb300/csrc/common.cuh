@@ -7,6 +7,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "qspec.h"
 
 namespace qspec {
@@ -43,6 +45,25 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
+}
+
+// Launch with programmatic dependent launch allowed: the kernel may start while the previous
+// kernel in the stream drains; it must execute griddepcontrol.wait before touching global memory
+// that the previous kernel writes or reads.
+template <typename... KArgs, typename... Args>
+inline qspec_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                               Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
 }
 
 }  // namespace qspec

@@ -43,7 +43,13 @@ using namespace ptx;
 
 constexpr int kWorkerWarps = 8;
 constexpr int kFirstWorker = 3;
-constexpr int kThreadsTC = (kFirstWorker + kWorkerWarps) * 32;
+constexpr int kFirstExtraIssuer = kFirstWorker + kWorkerWarps;
+// Accumulator chains per 128-channel group: a stage's MMAs are spread over 2 * chains issuing
+// warps with separate TMEM accumulators (one thread issuing back-to-back MMAs is latency-bound at
+// these narrow N); the drain adds the chains.  TMEM: 256 columns of A + 2 x 2 x chains x NM of D.
+__host__ __device__ constexpr int tc_chains(int NM) { return NM * 2 <= 64 ? 2 : 1; }
+__host__ __device__ constexpr int tc_issuers(int NM) { return 2 * tc_chains(NM); }
+__host__ __device__ constexpr int tc_threads(int NM) { return (kFirstExtraIssuer + tc_issuers(NM) - 1) * 32; }
 constexpr int kWBytes = 128 * 128;           // one stage of packed weights: 128 rows x 256 channels
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (about 2 s) before a wait gives up
@@ -172,12 +178,14 @@ __device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t* out) {
 }
 
 template <int NM, int MODE>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(tc_threads(NM), 1)
     linear_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                      const TcArgs a) {
   constexpr int NS = num_stages(NM);
   constexpr int SB = stage_bytes(NM);
   constexpr int HALF = NM / 2;
+  constexpr int CH = tc_chains(NM);
+  constexpr int NI = tc_issuers(NM);
   extern __shared__ uint8_t smem_raw[];
   // the 128-byte swizzle wants 1024-byte aligned tiles (alignment of the shared-window offset)
   uint8_t* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -196,15 +204,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full + i, 2);                  // producer (expect_tx) + scale warp
-      mbar_init(empty + i, kWorkerWarps + 1);  // worker warps + MMA commit
+      mbar_init(empty + i, kWorkerWarps + NI);  // worker warps + one commit per issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(afull + i, kWorkerWarps);
-      mbar_init(afree + i, 1);
-      mbar_init(dfull + i, 1);
+      mbar_init(afree + i, NI);
+      mbar_init(dfull + i, NI);
       mbar_init(dfree + i, kWorkerWarps);
     }
-    mbar_init(done, 1);
+    mbar_init(done, NI);
     misc->abort_flag = 0;
     misc->last = 0;
     for (int i = 0; i < kFusedMaxM; ++i) misc->amax_bits[i] = 0;
@@ -258,8 +266,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // nothing may still be copying into shared memory when the CTA exits
       for (int t = (issued > NS ? issued - NS : 0); t < issued; ++t) wait_bar_final(full + t % NS, (t / NS) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp >= kFirstExtraIssuer) {
+    // ------------------------------------------------------------------ MMA issuers
+    // issuer i handles group i / CH of each stage and the 16-channel steps kk = i % CH (mod CH)
+    const int issuer = warp == 1 ? 0 : warp - kFirstExtraIssuer + 1;
+    const int jg = issuer / CH, ch = issuer % CH;
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, NM);
       StageIter it(u_beg, u_end, G, a.T_m);
@@ -269,18 +280,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         bool ok = wait_bar(afull + pa, (s >> 1) & 1, abort_flag);
         if (s >= 2) ok = wait_bar(dfree + pa, ((s >> 1) - 1) & 1, abort_flag) && ok;
         ok = wait_bar(full + slot, (s / NS) & 1, abort_flag) && ok;
-        if (ok && !*abort_flag) {
+        if (ok && !*abort_flag && jg < static_cast<int>(it.cur_ng)) {
           tc_fence_after();
           const uint32_t a_base = tmem + pa * 128;
           const uint32_t b_base = smem_u32(ring + slot * SB + kWBytes);
-          for (int j = 0; j < static_cast<int>(it.cur_ng); ++j) {
-            const uint32_t d = tmem + 256 + (pa * 2 + j) * NM;
+          const uint32_t d = tmem + 256 + ((pa * 2 + jg) * CH + ch) * NM;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const int kb = j * 8 + kk;  // 16-channel step within the stage
-              const uint64_t bd = smem_desc_sw128(b_base + (kb >> 2) * (NM * 128) + (kb & 3) * 32);
-              mma_bf16_ts(d, a_base + kb * 8, bd, idesc, kk > 0 ? 1u : 0u);
-            }
+          for (int kk = ch; kk < 8; kk += CH) {
+            const int kb = jg * 8 + kk;  // 16-channel step within the stage
+            const uint64_t bd = smem_desc_sw128(b_base + (kb >> 2) * (NM * 128) + (kb & 3) * 32);
+            mma_bf16_ts(d, a_base + kb * 8, bd, idesc, kk >= CH ? 1u : 0u);
           }
         }
         mma_commit(empty + slot);
@@ -414,15 +423,28 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       tc_fence_after();
       uint32_t d0[HALF], d1[HALF];
       if (ok) {
+        // chain 0 of each group, then the other chains into e0 / e1 (added below)
+        uint32_t e0[HALF], e1[HALF];
 #pragma unroll
-        for (int c8 = 0; c8 < HALF / 8; ++c8)
-          tmem_ld8(tmem + lane_base + 256 + (pa * 2 + 0) * NM + h * HALF + 8 * c8, d0 + 8 * c8);
+        for (int c8 = 0; c8 < HALF / 8; ++c8) {
+          tmem_ld8(tmem + lane_base + 256 + ((pa * 2 + 0) * CH) * NM + h * HALF + 8 * c8, d0 + 8 * c8);
+          if (CH > 1) tmem_ld8(tmem + lane_base + 256 + ((pa * 2 + 0) * CH + 1) * NM + h * HALF + 8 * c8, e0 + 8 * c8);
+        }
         if (p.ng == 2) {
 #pragma unroll
-          for (int c8 = 0; c8 < HALF / 8; ++c8)
-            tmem_ld8(tmem + lane_base + 256 + (pa * 2 + 1) * NM + h * HALF + 8 * c8, d1 + 8 * c8);
+          for (int c8 = 0; c8 < HALF / 8; ++c8) {
+            tmem_ld8(tmem + lane_base + 256 + ((pa * 2 + 1) * CH) * NM + h * HALF + 8 * c8, d1 + 8 * c8);
+            if (CH > 1) tmem_ld8(tmem + lane_base + 256 + ((pa * 2 + 1) * CH + 1) * NM + h * HALF + 8 * c8, e1 + 8 * c8);
+          }
         }
         tmem_wait_ld();
+        if (CH > 1) {
+#pragma unroll
+          for (int t = 0; t < HALF; ++t) {
+            d0[t] = __float_as_uint(__uint_as_float(d0[t]) + __uint_as_float(e0[t]));
+            if (p.ng == 2) d1[t] = __float_as_uint(__uint_as_float(d1[t]) + __uint_as_float(e1[t]));
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -680,7 +702,7 @@ qspec_status launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcA
     return QSPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P);
-  cfg.blockDim = dim3(kThreadsTC);
+  cfg.blockDim = dim3(tc_threads(NM));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -22,6 +22,7 @@ namespace qspec {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kUnroll = 8;        // 16-byte loads in flight per thread in the streaming passes
 constexpr int kPlanCTAs = 608;    // about 4 CTAs per SM on a 152-SM part
 constexpr int kMinChunk = 2048;   // elements per CTA at least (4 KB of bf16)
 constexpr int kSeg2 = 8;          // pass 2: contiguous elements per thread
@@ -128,15 +129,15 @@ __device__ __forceinline__ void scan_argmax(const uint16_t* __restrict__ rp, int
   if (kVec) {
     const int nv = (end - beg) >> 3;
     const uint4* vp = reinterpret_cast<const uint4*>(rp + beg);
-    for (int v0 = threadIdx.x; v0 < nv; v0 += 4 * kThreads) {
-      uint4 u[4];
+    for (int v0 = threadIdx.x; v0 < nv; v0 += kUnroll * kThreads) {
+      uint4 u[kUnroll];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < kUnroll; ++t) {
         const int v = v0 + t * kThreads;
         u[t] = v < nv ? ld_stream_v4(vp + v) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < kUnroll; ++t) {
         const int v = v0 + t * kThreads;
         if (v < nv) {
           const int i0 = beg + 8 * v;
@@ -162,6 +163,8 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(const uint16_t* __rest
                                                           int32_t* __restrict__ accept_len,
                                                           int32_t* __restrict__ out_tok,
                                                           int32_t* __restrict__ tgt_argmax) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row = blockIdx.x / plan.chunks;
   const int c = blockIdx.x % plan.chunks;
   const int beg = c * plan.chunk_len;
@@ -270,15 +273,15 @@ __device__ __forceinline__ MS scan_ms(const uint16_t* __restrict__ rp, int beg, 
   if (kVec) {
     const int nv = (end - beg) >> 3;
     const uint4* vp = reinterpret_cast<const uint4*>(rp + beg);
-    for (int v0 = threadIdx.x; v0 < nv; v0 += 4 * kThreads) {
-      uint4 u[4];
+    for (int v0 = threadIdx.x; v0 < nv; v0 += kUnroll * kThreads) {
+      uint4 u[kUnroll];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < kUnroll; ++t) {
         const int v = v0 + t * kThreads;
         u[t] = v < nv ? ld_stream_v4(vp + v) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < kUnroll; ++t) {
         if (v0 + t * kThreads < nv) {
           const uint32_t w[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
           float f[8];
@@ -309,6 +312,7 @@ __global__ void __launch_bounds__(kThreads) sample_pass1_kernel(
     const float* __restrict__ u_acc, int B, int gamma, int V, Plan plan, WS ws,
     int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tok, float* __restrict__ accept_prob,
     float* __restrict__ p_tok, float* __restrict__ q_tok) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row = blockIdx.x / plan.chunks;
   const int c = blockIdx.x % plan.chunks;
   const int G1 = gamma + 1;
@@ -535,6 +539,8 @@ __global__ void __launch_bounds__(kThreads) sample_pass2_kernel(
   if (!s_last) return;
   __threadfence();
 
+  constexpr int kParts = 1024;
+  __shared__ float s_parts[kParts];
   __shared__ float s_R;
   __shared__ int s_c, s_fallback;
   __shared__ float s_before;
@@ -549,20 +555,38 @@ __global__ void __launch_bounds__(kThreads) sample_pass2_kernel(
       }
       __syncthreads();
     }
-    if (threadIdx.x == 0) {
-      float R = 0.0f;
-      for (int cc = 0; cc < chunks2; ++cc) R += __ldcg(ws.part2 + int64_t(b) * chunks2 + cc);
-      s_R = R;
+    // Chunk sums are staged in shared memory by all threads (one tile of kParts at a time) and
+    // walked in chunk order by thread 0: R first, then the chunk where the running sum passes u*R.
+    float R = 0.0f, cum = 0.0f, before = 0.0f;
+    int found = -1, last_pos = -1;
+    for (int pass = 0; pass < 2; ++pass) {
       const float target = u * R;
-      float cum = 0.0f;
-      int found = -1, last_pos = -1;
-      float before = 0.0f;
-      for (int cc = 0; cc < chunks2; ++cc) {
-        const float rc2 = __ldcg(ws.part2 + int64_t(b) * chunks2 + cc);
-        if (rc2 > 0.0f) last_pos = cc;
-        if (found < 0 && cum + rc2 > target) { found = cc; before = cum; }
-        cum += rc2;
+      for (int t0 = 0; t0 < chunks2; t0 += kParts) {
+        const int cnt = min(kParts, chunks2 - t0);
+        for (int i = threadIdx.x; i < cnt; i += kThreads) s_parts[i] = __ldcg(ws.part2 + int64_t(b) * chunks2 + t0 + i);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          for (int i = 0; i < cnt; ++i) {
+            const float rc2 = s_parts[i];
+            if (pass == 0) {
+              R += rc2;
+            } else {
+              if (rc2 > 0.0f) last_pos = t0 + i;
+              if (found < 0 && cum + rc2 > target) {
+                found = t0 + i;
+                before = cum;
+              }
+              cum += rc2;
+            }
+          }
+        }
+        __syncthreads();
       }
+      if (threadIdx.x == 0 && pass == 0) s_R = R;
+      __syncthreads();
+      R = s_R;
+    }
+    if (threadIdx.x == 0) {
       s_fallback = found < 0;
       s_c = found < 0 ? last_pos : found;
       s_before = before;
@@ -624,12 +648,10 @@ extern "C" qspec_status qspec_verify_greedy(const uint16_t* tgt_logits, const in
   const int64_t blocks = int64_t(B) * (gamma + 1) * L.pg.chunks;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (V % 8 == 0)
-    greedy_kernel<true><<<unsigned(blocks), kThreads, 0, s>>>(tgt_logits, draft_tok, gamma, V, L.pg, w,
-                                                              accept_len, out_tok, tgt_argmax);
-  else
-    greedy_kernel<false><<<unsigned(blocks), kThreads, 0, s>>>(tgt_logits, draft_tok, gamma, V, L.pg, w,
-                                                               accept_len, out_tok, tgt_argmax);
-  return launch_status();
+    return launch_pdl(greedy_kernel<true>, dim3(unsigned(blocks)), dim3(kThreads), 0, s, tgt_logits, draft_tok,
+                      int(gamma), int(V), L.pg, w, accept_len, out_tok, tgt_argmax);
+  return launch_pdl(greedy_kernel<false>, dim3(unsigned(blocks)), dim3(kThreads), 0, s, tgt_logits, draft_tok,
+                    int(gamma), int(V), L.pg, w, accept_len, out_tok, tgt_argmax);
 }
 
 extern "C" qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const uint16_t* draft_logits,
@@ -649,15 +671,14 @@ extern "C" qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const ui
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t blocks1 = int64_t(B) * (2 * gamma + 1) * L.p1.chunks;
   const bool vec = V % 8 == 0;
-  if (vec)
-    sample_pass1_kernel<true><<<unsigned(blocks1), kThreads, 0, s>>>(
-        tgt_logits, draft_logits, draft_tok, u_accept, B, gamma, V, L.p1, w, accept_len, out_tok,
-        accept_prob, p_tok, q_tok);
-  else
-    sample_pass1_kernel<false><<<unsigned(blocks1), kThreads, 0, s>>>(
-        tgt_logits, draft_logits, draft_tok, u_accept, B, gamma, V, L.p1, w, accept_len, out_tok,
-        accept_prob, p_tok, q_tok);
-  if (cudaGetLastError() != cudaSuccess) return QSPEC_ERR_CUDA;
+  const qspec_status st1 =
+      vec ? launch_pdl(sample_pass1_kernel<true>, dim3(unsigned(blocks1)), dim3(kThreads), 0, s, tgt_logits,
+                       draft_logits, draft_tok, u_accept, int(B), int(gamma), int(V), L.p1, w, accept_len, out_tok,
+                       accept_prob, p_tok, q_tok)
+          : launch_pdl(sample_pass1_kernel<false>, dim3(unsigned(blocks1)), dim3(kThreads), 0, s, tgt_logits,
+                       draft_logits, draft_tok, u_accept, int(B), int(gamma), int(V), L.p1, w, accept_len, out_tok,
+                       accept_prob, p_tok, q_tok);
+  if (st1 != QSPEC_OK) return st1;
 
   // Pass 2 with programmatic dependent launch: its CTAs are scheduled while pass 1 drains and
   // wait (griddepcontrol.wait) for pass 1 to complete before reading the workspace.

@@ -49,7 +49,7 @@ def check_greedy(q, tgt_bits, d):
     return rn
 
 
-@pytest.mark.parametrize("B,gamma,V,sigma", [(1, 3, 1024, 0.5), (16, 3, 128256, 0.5), (4, 1, 32000, 1.0),
+@pytest.mark.parametrize("B,gamma,V,sigma", [(1, 3, 1024, 0.5), (1, 3, 128256, 0.5), (16, 3, 128256, 0.5), (4, 1, 32000, 1.0),
                                              (3, 16, 4096, 0.25), (2, 7, 152064, 0.5), (5, 3, 1001, 0.5),
                                              (7, 2, 2, 1.0), (1, 5, 9, 0.5)])
 def test_greedy_parity(q, B, gamma, V, sigma):
@@ -138,7 +138,7 @@ def compare_sample(got, ref, u_acc):
     return exact
 
 
-SAMPLE_CASES = [(1, 3, 1024, 0.5), (8, 3, 32000, 0.5), (8, 1, 128256, 1.0), (4, 7, 152064, 0.25),
+SAMPLE_CASES = [(1, 3, 1024, 0.5), (1, 3, 128256, 0.5), (8, 3, 32000, 0.5), (8, 1, 128256, 1.0), (4, 7, 152064, 0.25),
                 (8, 5, 32000, 1.0), (2, 16, 4096, 0.5), (3, 3, 1001, 0.5), (5, 2, 2, 1.0), (64, 3, 32000, 0.5)]
 
 

@@ -7,14 +7,16 @@
 //  * activations are quantised per token once per CTA (amax over all K, s_a = amax / 7 in fp32,
 //    codes = clamp(rint(x / s_a), -8, 7)) and kept in shared memory, pre-arranged so that one
 //    32-bit word of packed weight nibbles meets two 32-bit words of activation codes;
-//  * a weight word w (codes k0..k7 as two's complement nibbles) becomes two byte vectors with one
-//    LOP3 each: ((w >> {0,4}) & 0x0F0F0F0F) ^ 0x08080808 = code + 8 in 0..15; dp4a sums
-//    (code + 8) * a, and 8 * sum(a) over the same 32 channels is subtracted, so every 128-channel
-//    group sum is the exact integer sum of code * a;
+//  * a weight word w (codes k0..k7 as two's complement nibbles) becomes two vectors of signed
+//    bytes by moving each nibble into the high half of its byte: (w << 4) & 0xF0F0F0F0 holds the
+//    even channels, w & 0xF0F0F0F0 the odd ones, each byte equal to 16 * code; dp4a against the
+//    activation codes gives 16 * sum(code * a) exactly, and the 1/16 is folded into the fp32 group
+//    scale, so every 128-channel group sum is the exact integer sum of code * a;
 //  * y[m, n] = s_a[m] * sum_g s[n, g] * acc[m, n, g] in fp32, rounded to bf16 once.
 //
-// Work split: a warp covers 4 weight rows x 8 lanes along K, so each load instruction reads four
-// contiguous 128-byte row segments and the activation words are broadcast to 4 lanes.  KS warps of
+// Work split: a warp covers RPW weight rows x (32 / RPW) lanes along K (RPW = 1 for one token, 4
+// for three or four), so each load instruction reads RPW contiguous row segments and each
+// activation word is broadcast to RPW lanes.  KS warps of
 // a CTA share one group of rows and split K (KS = 1 for wide layers, up to 8 for narrow ones); CTAs
 // loop over row groups.  Memory-bound on the packed weights: 0.5 B + 1/64 B per weight.
 #include <algorithm>
@@ -27,6 +29,9 @@ namespace {
 
 constexpr int kThreads = 256;  // 8 warps
 constexpr int kBatch = 4;      // chunks loaded per lane before they are consumed
+// Rows per warp: fewer rows give longer contiguous segments per load instruction; more rows share
+// each activation word between more lanes (shared-memory traffic per weight is M / RPW bytes).
+constexpr int kRowsPerWarpM1 = 1;
 
 __device__ __forceinline__ int dp4a_s32(uint32_t a, uint32_t b, int c) {
   return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
@@ -107,7 +112,7 @@ __device__ void quantise_tokens(const uint16_t* __restrict__ x, int K, uint32_t*
   __syncthreads();
 }
 
-template <int M>
+template <int M, int RPW>
 __global__ void __launch_bounds__(kThreads, 3) gemv_a4_kernel(const uint16_t* __restrict__ x,
                                                              const uint8_t* __restrict__ Wp,
                                                              const __half* __restrict__ S, int N, int K, int KS,
@@ -118,38 +123,40 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_a4_kernel(const uint16_t* __
   const int C = K / 32;  // 32-channel chunks per row
   const int G = K / kGroup;
   uint32_t* codes = reinterpret_cast<uint32_t*>(sm);                          // [M][C][8]
-  int* csum = reinterpret_cast<int*>(codes + static_cast<size_t>(M) * C * 8);  // [M][C]
-  float* red = reinterpret_cast<float*>(csum + M * C);                         // [8 warps][4 rows][M]
+  int* csum = reinterpret_cast<int*>(codes + static_cast<size_t>(M) * C * 8);  // [M][C] (quantiser scratch)
+  float* red = reinterpret_cast<float*>(csum + M * C);                         // [8 warps][RPW rows][M]
   __shared__ unsigned int amax_bits[M];
   __shared__ float s_a[M];
 
+  constexpr int LPR = 32 / RPW;  // lanes per row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = lane >> 3, kl = lane & 7;
+  const int r = lane / LPR, kl = lane % LPR;
   const int wg = warp / KS, ks = warp - wg * KS;  // row group within the CTA, K slice
   const int groups_per_cta = 8 / KS;
   const int cs = C / KS;  // chunks per K slice (a multiple of 4: slices hold whole groups)
   const int c_beg = ks * cs, c_end = c_beg + cs;
-  const long long row_step = static_cast<long long>(gridDim.x) * groups_per_cta * 4;
-  const long long cta_first = static_cast<long long>(blockIdx.x) * groups_per_cta * 4;
-  // Every warp of the CTA walks the same sequence of (row-group iteration, batch) items, so the
-  // CTA-level reductions and every full-warp shuffle are reached by all lanes.
-  const int nb = (cs + 8 * kBatch - 1) / (8 * kBatch);  // batches per row group
-  const long long iters = cta_first < N ? (N - cta_first + row_step - 1) / row_step : 0;
-  const long long items = iters * nb;
+  const int row_step = gridDim.x * groups_per_cta * RPW;
+  const int cta_first = blockIdx.x * groups_per_cta * RPW;
+  // Every warp of the CTA walks the same (row-group iteration, batch) items, so the CTA-level
+  // reductions and every full-warp shuffle are reached by all lanes.
+  const int nb = (cs + LPR * kBatch - 1) / (LPR * kBatch);  // batches per row group
+  const int iters = cta_first < N ? (N - cta_first + row_step - 1) / row_step : 0;
+  const size_t row_bytes = static_cast<size_t>(K) / 2;
 
-  auto load_item = [&](long long i, uint4 (&wv)[kBatch], float (&sg)[kBatch]) {
-    const long long it = i / nb;
-    const int bi = static_cast<int>(i - it * nb);
-    const long long n = cta_first + it * row_step + wg * 4 + r;
-    const bool valid = i < items && n < N;
-    const uint8_t* wrow = Wp + (valid ? n : 0) * (K / 2);
-    const __half* srow = S + (valid ? n : 0) * G;
+  // item cursor (iteration, batch) advanced without divisions
+  auto load_item = [&](int it, int bi, uint4 (&wv)[kBatch], float (&sg)[kBatch]) {
+    const int n = cta_first + it * row_step + wg * RPW + r;
+    const bool valid = it < iters && n < N;
+    const uint8_t* wrow = Wp + (valid ? static_cast<size_t>(n) : 0) * row_bytes;
+    const __half* srow = S + (valid ? static_cast<size_t>(n) : 0) * G;
+    const int cb = c_beg + bi * LPR * kBatch + kl;
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
-      const int c = c_beg + bi * 8 * kBatch + kl + 8 * b;
+      const int c = cb + LPR * b;
       const bool ok = valid && c < c_end;
       wv[b] = ok ? ld_stream_v4(wrow + 16 * c) : make_uint4(0, 0, 0, 0);
-      sg[b] = ok ? __half2float(srow[c >> 2]) : 0.0f;
+      // the nibble sits in the high half of each byte below, so every product is 16x too large
+      sg[b] = ok ? __half2float(srow[c >> 2]) * 0.0625f : 0.0f;
     }
   };
 
@@ -157,34 +164,34 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_a4_kernel(const uint16_t* __
   float sa_[kBatch], sb_[kBatch];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  load_item(0, wa, sa_);  // the first weights are in flight while the activations are quantised
+  load_item(0, 0, wa, sa_);  // the first weights are in flight while the activations are quantised
   quantise_tokens<M>(x, K, codes, csum, s_a, amax_bits, xq_out, xs_out);
 
   float yacc[M];
 #pragma unroll
   for (int m = 0; m < M; ++m) yacc[m] = 0.0f;
 
-  auto consume = [&](long long i, const uint4 (&wv)[kBatch], const float (&sg)[kBatch]) {
-    const long long it = i / nb;
-    const int bi = static_cast<int>(i - it * nb);
-    const long long n = cta_first + it * row_step + wg * 4 + r;
+  auto consume = [&](int it, int bi, const uint4 (&wv)[kBatch], const float (&sg)[kBatch]) {
+    const int n = cta_first + it * row_step + wg * RPW + r;
     const bool valid = n < N;
+    const int cb = c_beg + bi * LPR * kBatch + kl;
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
-      const int c = c_beg + bi * 8 * kBatch + kl + 8 * b;
+      const int c = cb + LPR * b;
       const bool in = c < c_end;  // uniform across each 4-lane set that shares a 128-channel group
       const uint32_t w[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
+      // signed bytes 16 * code: even channels shifted into the high nibble, odd ones masked there
       uint32_t ev[4], od[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        ev[t] = (w[t] & 0x0F0F0F0Fu) ^ 0x08080808u;
-        od[t] = ((w[t] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+        ev[t] = (w[t] << 4) & 0xF0F0F0F0u;
+        od[t] = w[t] & 0xF0F0F0F0u;
       }
 #pragma unroll
       for (int m = 0; m < M; ++m) {
         int acc = 0;
         if (in) {
-          const uint4* ap = reinterpret_cast<const uint4*>(codes + (static_cast<long long>(m) * C + c) * 8);
+          const uint4* ap = reinterpret_cast<const uint4*>(codes + (m * C + c) * 8);
           const uint4 a0 = ap[0], a1 = ap[1];
           acc = dp4a_s32(ev[0], a0.x, acc);
           acc = dp4a_s32(od[0], a0.y, acc);
@@ -194,43 +201,42 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_a4_kernel(const uint16_t* __
           acc = dp4a_s32(od[2], a1.y, acc);
           acc = dp4a_s32(ev[3], a1.z, acc);
           acc = dp4a_s32(od[3], a1.w, acc);
-          acc -= 8 * csum[m * C + c];
         }
         if (acc_out) {  // exact 128-channel group sum over the 4 lanes of the group (all lanes shuffle)
           int gsum = acc + __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
           gsum += __shfl_xor_sync(0xFFFFFFFFu, gsum, 2);
-          if (in && valid && (kl & 3) == 0) acc_out[(static_cast<long long>(m) * N + n) * G + (c >> 2)] = gsum;
+          if (in && valid && (kl & 3) == 0)
+            acc_out[(static_cast<size_t>(m) * N + n) * G + (c >> 2)] = gsum >> 4;  // exact: a multiple of 16
         }
         yacc[m] = fmaf(sg[b], static_cast<float>(acc), yacc[m]);
       }
     }
     if (bi != nb - 1) return;
-    // end of the row group: reduce over the 8 K-lanes of each row, then over the KS warps
+    // end of the row group: reduce over the lanes of each row, then over the KS warps
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       float v = yacc[m];
-      v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-      v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-      v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+#pragma unroll
+      for (int off = 1; off < LPR; off <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
       yacc[m] = v;
     }
     if (KS == 1) {
       if (kl == 0 && valid) {
 #pragma unroll
-        for (int m = 0; m < M; ++m) y[static_cast<long long>(m) * N + n] = f32_to_bf16_bits(yacc[m] * s_a[m]);
+        for (int m = 0; m < M; ++m) y[static_cast<size_t>(m) * N + n] = f32_to_bf16_bits(yacc[m] * s_a[m]);
       }
     } else {
       if (kl == 0) {
 #pragma unroll
-        for (int m = 0; m < M; ++m) red[(warp * 4 + r) * M + m] = yacc[m];
+        for (int m = 0; m < M; ++m) red[(warp * RPW + r) * M + m] = yacc[m];
       }
       __syncthreads();
       if (ks == 0 && kl == 0 && valid) {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
           float v = 0.0f;
-          for (int j = 0; j < KS; ++j) v += red[((wg * KS + j) * 4 + r) * M + m];
-          y[static_cast<long long>(m) * N + n] = f32_to_bf16_bits(v * s_a[m]);
+          for (int j = 0; j < KS; ++j) v += red[((wg * KS + j) * RPW + r) * M + m];
+          y[static_cast<size_t>(m) * N + n] = f32_to_bf16_bits(v * s_a[m]);
         }
       }
       __syncthreads();
@@ -240,28 +246,41 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_a4_kernel(const uint16_t* __
   };
 
   // two register batches: the next item's loads are issued before the current one is consumed
-  for (long long i = 0; i < items; i += 2) {
-    load_item(i + 1, wb, sb_);
-    consume(i, wa, sa_);
-    if (i + 1 >= items) break;
-    load_item(i + 2, wa, sa_);
-    consume(i + 1, wb, sb_);
+  int it = 0, bi = 0;
+  auto advance = [&](int& i_, int& b_) {
+    if (++b_ == nb) {
+      b_ = 0;
+      ++i_;
+    }
+  };
+  while (it < iters) {
+    int it1 = it, bi1 = bi;
+    advance(it1, bi1);
+    load_item(it1, bi1, wb, sb_);
+    consume(it, bi, wa, sa_);
+    if (it1 >= iters) break;
+    int it2 = it1, bi2 = bi1;
+    advance(it2, bi2);
+    load_item(it2, bi2, wa, sa_);
+    consume(it1, bi1, wb, sb_);
+    it = it2;
+    bi = bi2;
   }
 }
 
-template <int M>
+template <int M, int RPW>
 qspec_status launch_gemv_a4(const uint16_t* x, const uint8_t* Wp, const __half* S, int N, int K, uint16_t* y,
                             int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream) {
   const int C = K / 32, G = K / kGroup;
   // split K over up to 8 warps when the layer has too few row groups to fill the GPU
-  const long long row_groups = (static_cast<long long>(N) + 3) / 4;
+  const long long row_groups = (static_cast<long long>(N) + RPW - 1) / RPW;
   const int sms = num_sms();
   int KS = 1;
   while (KS < 8 && row_groups / (8 / KS) < 3LL * sms && G % (KS * 2) == 0) KS *= 2;
   const long long ctas_needed = (row_groups + (8 / KS) - 1) / (8 / KS);
   const int grid = static_cast<int>(std::min<long long>(ctas_needed, 3LL * sms));  // resident CTAs per SM: 3
-  const size_t smem = static_cast<size_t>(M) * C * 32 + static_cast<size_t>(M) * C * 4 + 8 * 4 * M * sizeof(float);
-  auto kern = gemv_a4_kernel<M>;
+  const size_t smem = static_cast<size_t>(M) * C * 32 + static_cast<size_t>(M) * C * 4 + 8 * RPW * M * sizeof(float);
+  auto kern = gemv_a4_kernel<M, RPW>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return QSPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -290,10 +309,10 @@ qspec_status gemv_a4(const uint16_t* x, const uint8_t* Wp, const uint16_t* S, in
                      int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream) {
   const __half* Sh = reinterpret_cast<const __half*>(S);
   switch (M) {
-    case 1: return launch_gemv_a4<1>(x, Wp, Sh, N, K, y, xq_out, xs_out, acc_out, stream);
-    case 2: return launch_gemv_a4<2>(x, Wp, Sh, N, K, y, xq_out, xs_out, acc_out, stream);
-    case 3: return launch_gemv_a4<3>(x, Wp, Sh, N, K, y, xq_out, xs_out, acc_out, stream);
-    default: return launch_gemv_a4<4>(x, Wp, Sh, N, K, y, xq_out, xs_out, acc_out, stream);
+    case 1: return launch_gemv_a4<1, kRowsPerWarpM1>(x, Wp, Sh, N, K, y, xq_out, xs_out, acc_out, stream);
+    case 2: return launch_gemv_a4<2, 2>(x, Wp, Sh, N, K, y, xq_out, xs_out, acc_out, stream);
+    case 3: return launch_gemv_a4<3, 4>(x, Wp, Sh, N, K, y, xq_out, xs_out, acc_out, stream);
+    default: return launch_gemv_a4<4, 4>(x, Wp, Sh, N, K, y, xq_out, xs_out, acc_out, stream);
   }
 }
 

@@ -323,20 +323,28 @@ def gpu_arm(args, rank, world):
 
     # ---- CUDA graphs: one plain graph for the timed loop; a pool of instrumented graphs whose
     # external events time every kernel of the last steps of the timed region
-    side = torch.cuda.Stream(device=dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=side):
-        step()
+    # (--eager: the same launches issued directly, for profilers that do not follow stream capture)
     n_inst = min(args.steps, args.timed_graphs)
     inst = []
-    for _ in range(n_inst):
-        gi = torch.cuda.CUDAGraph()
-        timers = []
-        with torch.cuda.graph(gi, stream=side):
-            step(timers)
-        inst.append((gi, timers))
+    if args.eager:
+        replay = step
+        for _ in range(n_inst):
+            timers = []
+            inst.append((lambda t=timers: step(t), timers))
+    else:
+        side = torch.cuda.Stream(device=dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step()
+        replay = graph.replay
+        for _ in range(n_inst):
+            gi = torch.cuda.CUDAGraph()
+            timers = []
+            with torch.cuda.graph(gi, stream=side):
+                step(timers)
+            inst.append((gi.replay, timers))
     for _ in range(3):
-        graph.replay()
+        replay()
     torch.cuda.synchronize()
 
     dist = world > 1
@@ -351,9 +359,9 @@ def gpu_arm(args, rank, world):
         start.record()
         n_plain = args.steps - n_inst
         for _ in range(n_plain):
-            graph.replay()
-        for gi, _ in inst:
-            gi.replay()
+            replay()
+        for run_inst, _ in inst:
+            run_inst()
         stop.record()
         torch.cuda.synchronize()
         if dist:
@@ -447,7 +455,8 @@ def gpu_arm(args, rank, world):
         "data": "synthetic (seeded; random-init weights of the named shapes)",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (1.5 GB of packed weights streamed per step)",
-                   "timing": "CUDA graph replays of whole steps, CUDA events on the replay stream"},
+                   "timing": ("direct launches" if args.eager else "CUDA graph replays") +
+                             " of whole steps, CUDA events on the launching stream"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"kernel": kernel_names[dominant], "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": hbm_peak, "peak_source": peak_kind, "unit": "GB/s",
@@ -533,8 +542,116 @@ def profile_case(spec, reps):
                       "note": "eager back-to-back launches; inputs resident"}))
 
 
+LLAMA70B = [("qo", 8192, 8192), ("kv", 1024, 8192), ("gate_up", 28672, 8192), ("down", 8192, 28672),
+            ("lm_head", 32000, 8192)]
+
+
+def _graph_time(fn, reps=10, iters=5):
+    """Seconds per call of fn, from CUDA-graph replays of `reps` back-to-back calls."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3 / (reps * iters)
+
+
+def sweep_linear():
+    """Llama-2-70B-shaped linears, M swept 1..256 in both modes (the HBM-bound to tensor-bound
+    crossover): one JSON line per (layer, mode, M) with GB/s and TOPS."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as g
+    g.build()
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+    from quantized_speculative_decoding_qspec_gb300 import synthetic as syn
+    dev = torch.device("cuda", 0)
+    hbm, _ = peaks()
+    for li, (name, N, K) in enumerate(LLAMA70B):
+        W = torch.from_numpy(syn.weights(N, K, 3, layer=li).view(np.int16)).to(dev).view(torch.bfloat16)
+        Wp = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+        S = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+        q.qspec_pack_weights(W, Wp, S)
+        del W
+        for M in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+            x = torch.from_numpy(syn.activations(M, K, 3, step=M).view(np.int16)).to(dev).view(torch.bfloat16)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            ws = q.new_linear_workspace(M, N, K, device=dev)
+            for mode in ("a16", "a4"):
+                fn = ((lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws)) if mode == "a16"
+                      else (lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws)))
+                t = _graph_time(fn)
+                b = linear_bytes(M, N, K)
+                print(json.dumps({"sweep": "llama70b_linear", "layer": name, "N": N, "K": K, "M": M, "mode": mode,
+                                  "us": round(t * 1e6, 2), "GB_s": round(b / t / 1e9, 1),
+                                  "hbm_frac": round(b / t / 1e9 / hbm, 3),
+                                  "TOPS": round(2 * M * N * K / t / 1e12, 2)}), flush=True)
+        q.qspec_check_status()
+
+
+def sweep_sampling(quick=False):
+    """Sampling-verify sweep: gamma x batch x vocab x draft noise.  Per cell: time, logits GB/s,
+    positions/s, mean emitted tokens per sequence and call, and E[T] = (1 - a^(g+1)) / (1 - a)
+    at the measured mean acceptance probability a (the tutorial's constant-acceptance model)."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as g
+    g.build()
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+    from quantized_speculative_decoding_qspec_gb300 import synthetic as syn
+    dev = torch.device("cuda", 0)
+    hbm, _ = peaks()
+    gammas, batches = ((1, 3, 5, 7), (1, 8, 32, 64)) if not quick else ((3,), (8,))
+    vocabs, sigmas = ((32000, 128256, 152064), (0.25, 0.5, 1.0)) if not quick else ((32000,), (0.5,))
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    for gamma in gammas:
+        for B in batches:
+            for V in vocabs:
+                for sigma in sigmas:
+                    inp = syn.verify_inputs(B, gamma, V, sigma, workload_id=4, sampling=True)
+                    tgt, drf = bf(inp["tgt"]), bf(inp["drf"])
+                    d = torch.from_numpy(inp["d"]).to(dev)
+                    ua, ur = torch.from_numpy(inp["u_acc"]).to(dev), torch.from_numpy(inp["u_res"]).to(dev)
+                    ws = q.new_verify_workspace(B, gamma, V, device=dev)
+                    n = torch.empty(B, dtype=torch.int32, device=dev)
+                    o = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+                    a = torch.empty(B, gamma, dtype=torch.float32, device=dev)
+                    fn = lambda: q.qspec_verify_sample(tgt, drf, d, ua, ur, n, o, ws, accept_prob=a)
+                    t = _graph_time(fn, reps=10, iters=3)
+                    fn()
+                    q.qspec_check_status(ws)
+                    alpha = float(a.mean().item())
+                    et = (gamma + 1.0) if alpha >= 1.0 else (1 - alpha ** (gamma + 1)) / (1 - alpha)
+                    b = verify_bytes(B, gamma, V, True)
+                    print(json.dumps({"sweep": "sampling_verify", "gamma": gamma, "B": B, "V": V, "sigma": sigma,
+                                      "us": round(t * 1e6, 2), "GB_s": round(b / t / 1e9, 1),
+                                      "hbm_frac": round(b / t / 1e9 / hbm, 3),
+                                      "positions_per_s": round(B * (gamma + 1) / t, 1),
+                                      "tokens_per_call": round(float(n.float().mean().item()) + 1, 3),
+                                      "mean_accept_prob": round(alpha, 4), "E_T_at_mean_alpha": round(et, 3)}),
+                          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--sweep", choices=["linear", "sampling", "sampling-quick"], default=None,
+                    help="measurement sweeps instead of the step benchmark")
     ap.add_argument("--profile-case", default=None,
                     help="run only one kernel of the step, e.g. lm_head:a4:1 or verify:greedy (for ncu)")
     ap.add_argument("--reps", type=int, default=3)
@@ -546,12 +663,20 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="issue the step's launches directly instead of replaying CUDA graphs (for ncu)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.profile_case:
         profile_case(args.profile_case, args.reps)
+        return
+    if args.sweep == "linear":
+        sweep_linear()
+        return
+    if args.sweep in ("sampling", "sampling-quick"):
+        sweep_sampling(quick=args.sweep == "sampling-quick")
         return
 
     if args.impl == "reference":

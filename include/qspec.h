@@ -59,8 +59,10 @@ typedef enum {
  * for each row n and group g of 128 consecutive input channels,
  *     s[n,g]    = fp16( amax_g |W| / 7 )                   (fp32 IEEE division, round to fp16)
  *     code[n,k] = clamp( rint( W[n,k] / float(s[n,g]) ), -8, 7 )   (fp32 IEEE division, ties even)
- * with all codes 0 when s == 0.  Codes are two's complement nibbles: byte Wp[n, j] holds k = 2j in
- * bits 0..3 and k = 2j+1 in bits 4..7.  This packed format is the format both linear calls read.
+ * with all codes 0 when s == 0.  Codes are two's complement nibbles; the 32-bit little-endian word
+ * t of row n (bytes Wp[n, 4t..4t+3]) holds channels k = 8t..8t+7 with the even channels
+ * 8t+0, 2, 4, 6 in nibbles 0..3 (bits 0..15) and the odd channels 8t+1, 3, 5, 7 in nibbles 4..7
+ * (bits 16..31).  This packed format is the format both linear calls read.
  *
  *   W   [N, K] bf16 (input), K % 128 == 0, 1 <= N, N*K < 2^40
  *   Wp  [N, K/2] uint8 (output)

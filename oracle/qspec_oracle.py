@@ -23,8 +23,9 @@ Readings where the pages are silent (each is listed in the design notes of the r
 
 * Weight quantiser: symmetric, per group of 128 input channels along K, divisor 7, scale rounded to
   fp16 before the codes are formed, codes = clamp(rint(w / s), -8, 7) with ties to even, s == 0
-  gives all-zero codes.  Byte ``Wp[n, j]`` holds k = 2j in bits 0..3 and k = 2j+1 in bits 4..7
-  (two's complement nibbles).
+  gives all-zero codes.  Packed layout (the pages fix no bit order): each 32-bit little-endian
+  word t of a row holds k = 8t..8t+7 as two's complement nibbles, the even channels k = 8t+0,2,4,6
+  in nibbles 0..3 (bits 0..15) and the odd channels k = 8t+1,3,5,7 in nibbles 4..7 (bits 16..31).
 * Activation quantiser: one fp32 scale per token over all of K, s_a = amax / 7 (not rounded to
   fp16), codes = clamp(rint(x / s_a), -8, 7); s_a == 0 gives all-zero codes.
 * Greedy argmax compares bf16 logit values; ties (and +0 / -0) go to the lowest index.
@@ -109,23 +110,32 @@ def quantize_weights(W_bits):
     return codes.reshape(N, K), S
 
 
+# Nibble slot i (bits 4i..4i+3 of a little-endian 32-bit word) holds channel 8t + WORD_ORDER[i].
+WORD_ORDER = (0, 2, 4, 6, 1, 3, 5, 7)
+
+
 def pack_codes(codes) -> np.ndarray:
-    """int8 codes [N, K] -> uint8 [N, K/2]: byte j = (code[2j] & 0xF) | (code[2j+1] & 0xF) << 4."""
+    """int8 codes [N, K] -> uint8 [N, K/2]; word t holds k = 8t + WORD_ORDER[i] in nibble i."""
     c = np.asarray(codes, dtype=np.int8).astype(np.int16) & 0xF
-    lo = c[:, 0::2]
-    hi = c[:, 1::2]
-    return (lo | (hi << 4)).astype(np.uint8)
+    N, K = c.shape
+    blocks = c.reshape(N, K // 8, 8)
+    nib = blocks[:, :, list(WORD_ORDER)]                 # nibbles 0..7 of each word
+    byte = nib[:, :, 0::2] | (nib[:, :, 1::2] << 4)      # byte b = nibble 2b | nibble 2b+1 << 4
+    return byte.reshape(N, K // 2).astype(np.uint8)
 
 
 def unpack_codes(Wp) -> np.ndarray:
-    """uint8 [N, K/2] -> int8 codes [N, K] (two's complement nibbles, low nibble first)."""
+    """uint8 [N, K/2] -> int8 codes [N, K] (inverse of pack_codes)."""
     b = np.asarray(Wp, dtype=np.uint8).astype(np.int16)
     N, H = b.shape
-    out = np.empty((N, 2 * H), dtype=np.int16)
-    out[:, 0::2] = b & 0xF
-    out[:, 1::2] = (b >> 4) & 0xF
+    byte = b.reshape(N, H // 4, 4)
+    nib = np.empty((N, H // 4, 8), dtype=np.int16)
+    nib[:, :, 0::2] = byte & 0xF
+    nib[:, :, 1::2] = (byte >> 4) & 0xF
+    out = np.empty_like(nib)
+    out[:, :, list(WORD_ORDER)] = nib
     out = np.where(out >= 8, out - 16, out)
-    return out.astype(np.int8)
+    return out.reshape(N, 2 * H).astype(np.int8)
 
 
 def pack_weights(W_bits):

@@ -7,10 +7,11 @@
 //  * activations are quantised per token once per CTA (amax over all K, s_a = amax / 7 in fp32,
 //    codes = clamp(rint(x / s_a), -8, 7)) and kept in shared memory, pre-arranged so that one
 //    32-bit word of packed weight nibbles meets two 32-bit words of activation codes;
-//  * a weight word w (codes k0..k7 as two's complement nibbles) becomes two vectors of signed
-//    bytes by moving each nibble into the high half of its byte: (w << 4) & 0xF0F0F0F0 holds the
-//    even channels, w & 0xF0F0F0F0 the odd ones, each byte equal to 16 * code; dp4a against the
-//    activation codes gives 16 * sum(code * a) exactly, and the 1/16 is folded into the fp32 group
+//  * a weight word w (channels k0..k7 as two's complement nibbles in the packed order k0, k2, k4,
+//    k6, k1, k3, k5, k7) becomes two vectors of signed bytes by moving each nibble into the high
+//    half of its byte: (w << 4) & 0xF0F0F0F0 holds k0, k4, k1, k5 and w & 0xF0F0F0F0 holds k2, k6,
+//    k3, k7, each byte equal to 16 * code; dp4a against activation words laid out in the same
+//    channel order gives 16 * sum(code * a) exactly, and the 1/16 is folded into the fp32 group
 //    scale, so every 128-channel group sum is the exact integer sum of code * a;
 //  * y[m, n] = s_a[m] * sum_g s[n, g] * acc[m, n, g] in fp32, rounded to bf16 once.
 //
@@ -38,8 +39,8 @@ __device__ __forceinline__ int dp4a_s32(uint32_t a, uint32_t b, int c) {
 }
 
 // Per-token quantiser (step a3) into shared memory: codes per 32-channel chunk as 8 words
-// (word 2t holds k = 8t+0,2,4,6 and word 2t+1 holds k = 8t+1,3,5,7 as signed bytes) and the chunk
-// sum of the codes.
+// (word 2t holds k = 8t+0,4,1,5 and word 2t+1 holds k = 8t+2,6,3,7 as signed bytes, matching the
+// two byte vectors of a packed weight word) and the chunk sum of the codes.
 template <int M>
 __device__ void quantise_tokens(const uint16_t* __restrict__ x, int K, uint32_t* codes, int* csum, float* s_a,
                                 unsigned int* amax_bits, int8_t* __restrict__ xq_out, float* __restrict__ xs_out) {
@@ -92,9 +93,11 @@ __device__ void quantise_tokens(const uint16_t* __restrict__ x, int K, uint32_t*
       uint32_t ev = 0, od = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        ev |= (static_cast<uint32_t>(q[8 * t + 2 * j]) & 0xFFu) << (8 * j);
-        od |= (static_cast<uint32_t>(q[8 * t + 2 * j + 1]) & 0xFFu) << (8 * j);
-        sum += q[8 * t + 2 * j] + q[8 * t + 2 * j + 1];
+        // byte j of the even-nibble vector is channel 4(j & 1) + (j >> 1); of the odd one, that + 2
+        const int k = 8 * t + 4 * (j & 1) + (j >> 1);
+        ev |= (static_cast<uint32_t>(q[k]) & 0xFFu) << (8 * j);
+        od |= (static_cast<uint32_t>(q[k + 2]) & 0xFFu) << (8 * j);
+        sum += q[k] + q[k + 2];
       }
       out[2 * t] = ev;
       out[2 * t + 1] = od;
@@ -180,7 +183,8 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_a4_kernel(const uint16_t* __
       const int c = cb + LPR * b;
       const bool in = c < c_end;  // uniform across each 4-lane set that shares a 128-channel group
       const uint32_t w[4] = {wv[b].x, wv[b].y, wv[b].z, wv[b].w};
-      // signed bytes 16 * code: even channels shifted into the high nibble, odd ones masked there
+      // signed bytes 16 * code: nibbles 0, 2, 4, 6 shifted into the high half of their byte,
+      // nibbles 1, 3, 5, 7 masked there
       uint32_t ev[4], od[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -272,13 +276,15 @@ template <int M, int RPW>
 qspec_status launch_gemv_a4(const uint16_t* x, const uint8_t* Wp, const __half* S, int N, int K, uint16_t* y,
                             int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream) {
   const int C = K / 32, G = K / kGroup;
-  // split K over up to 8 warps when the layer has too few row groups to fill the GPU
+  // Split K over KS warps of a CTA only when whole rows per warp would leave the persistent grid
+  // (3 resident CTAs per SM) less than half filled: thinner K slices cost a CTA-wide reduction
+  // per row group, which measured slower than an uneven last iteration.
   const long long row_groups = (static_cast<long long>(N) + RPW - 1) / RPW;
-  const int sms = num_sms();
+  const long long resident = 3LL * num_sms();
   int KS = 1;
-  while (KS < 8 && row_groups / (8 / KS) < 3LL * sms && G % (KS * 2) == 0) KS *= 2;
+  while (KS < 8 && (row_groups + (8 / KS) - 1) / (8 / KS) < resident / 2 && G % (KS * 2) == 0) KS *= 2;
   const long long ctas_needed = (row_groups + (8 / KS) - 1) / (8 / KS);
-  const int grid = static_cast<int>(std::min<long long>(ctas_needed, 3LL * sms));  // resident CTAs per SM: 3
+  const int grid = static_cast<int>(std::min<long long>(ctas_needed, resident));
   const size_t smem = static_cast<size_t>(M) * C * 32 + static_cast<size_t>(M) * C * 4 + 8 * RPW * M * sizeof(float);
   auto kern = gemv_a4_kernel<M, RPW>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)

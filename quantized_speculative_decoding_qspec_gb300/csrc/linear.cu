@@ -25,8 +25,9 @@ __device__ __forceinline__ void unpack32(const uint4 w, float (&c)[32]) {
   for (int i = 0; i < 4; ++i) {
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
+      // nibble t holds channel 8i + 2t (t < 4) or 8i + 2(t - 4) + 1 (t >= 4)
       const int nib = static_cast<int>((words[i] >> (4 * t)) & 0xFu);
-      c[8 * i + t] = static_cast<float>(nib >= 8 ? nib - 16 : nib);
+      c[8 * i + (t < 4 ? 2 * t : 2 * (t - 4) + 1)] = static_cast<float>(nib >= 8 ? nib - 16 : nib);
     }
   }
 }

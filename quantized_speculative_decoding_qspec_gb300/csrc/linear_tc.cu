@@ -161,21 +161,30 @@ __device__ __forceinline__ uint32_t owner_of(uint32_t u, uint32_t U, uint32_t P)
   return static_cast<uint32_t>(((static_cast<uint64_t>(u) + 1) * P - 1) / U);
 }
 
-// 8 INT4 codes (one little-endian word, k = 8w + i in bits 4i..4i+3) -> 4 bf16x2 words holding
-// (k0,k1), (k2,k3), (k4,k5), (k6,k7).  Each pair is placed as (c + 8) in the low mantissa bits of
-// bf16 128.0 (exact), then 136 is subtracted: the codes come out exact.
+// One packed word (channels k0..k7 of a row as two's complement nibbles in the order k0, k2, k4,
+// k6, k1, k3, k5, k7) -> 4 bf16x2 words holding (k0,k1), (k2,k3), (k4,k5), (k6,k7): nibble pair
+// (i, i + 4) is shifted to bits 0..3 / 16..19 and its top bit flipped into the low mantissa bits of
+// bf16 128.0, giving exactly 136 + code.  With OFFSET the words are left at 136 + code (a second
+// MMA against a constant -136 operand removes the offset); otherwise 136 is subtracted here.
+template <bool OFFSET>
 __device__ __forceinline__ void codes_to_bf16x2(uint32_t w, uint32_t* out) {
-  const uint32_t hi = w >> 4;
   const __nv_bfloat162 off = __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308));
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t t = __byte_perm(w, hi, static_cast<uint32_t>(i | ((4 + i) << 8)));
     uint32_t v;
-    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(v) : "r"(t), "r"(0x000F000Fu), "r"(0x43084308u));
-    const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), off);
-    out[i] = *reinterpret_cast<const uint32_t*>(&r);
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(v) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(0x43084308u));
+    if constexpr (OFFSET) {
+      out[i] = v;
+    } else {
+      const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), off);
+      out[i] = *reinterpret_cast<const uint32_t*>(&r);
+    }
   }
 }
+
+// TMEM columns: 256 of A (two stage buffers), 2 x 2 x chains x NM of D, and, where they fit, 8 of a
+// constant -136 A operand for the offset form of the weight conversion.
+__host__ __device__ constexpr bool tc_offset(int NM) { return 256 + 4 * tc_chains(NM) * NM + 8 <= 512; }
 
 template <int NM, int MODE>
 __global__ void __launch_bounds__(tc_threads(NM), 1)
@@ -186,6 +195,10 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
   constexpr int HALF = NM / 2;
   constexpr int CH = tc_chains(NM);
   constexpr int NI = tc_issuers(NM);
+  constexpr int DB = 2;  // accumulator (D) buffers in TMEM
+  constexpr bool OFFSET = tc_offset(NM);
+  constexpr uint32_t kConstCol = 256 + DB * 2 * CH * NM;  // the -136 operand (OFFSET only)
+  static_assert(kConstCol + (OFFSET ? 8 : 0) <= kTmemCols, "TMEM columns");
   extern __shared__ uint8_t smem_raw[];
   // the 128-byte swizzle wants 1024-byte aligned tiles (alignment of the shared-window offset)
   uint8_t* ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -195,8 +208,8 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
   uint64_t* afull = empty + NS;
   uint64_t* afree = afull + 2;
   uint64_t* dfull = afree + 2;
-  uint64_t* dfree = dfull + 2;
-  uint64_t* done = dfree + 2;
+  uint64_t* dfree = dfull + DB;
+  uint64_t* done = dfree + DB;
   Misc* misc = reinterpret_cast<Misc*>(done + 1);
   volatile int* abort_flag = &misc->abort_flag;
 
@@ -209,6 +222,8 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(afull + i, kWorkerWarps);
       mbar_init(afree + i, NI);
+    }
+    for (int i = 0; i < DB; ++i) {
       mbar_init(dfull + i, NI);
       mbar_init(dfree + i, kWorkerWarps);
     }
@@ -276,25 +291,26 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
       StageIter it(u_beg, u_end, G, a.T_m);
       int s = 0;
       while (it.next()) {
-        const int slot = s % NS, pa = s & 1;
+        const int slot = s % NS, pa = s & 1, pd = s % DB;
         bool ok = wait_bar(afull + pa, (s >> 1) & 1, abort_flag);
-        if (s >= 2) ok = wait_bar(dfree + pa, ((s >> 1) - 1) & 1, abort_flag) && ok;
+        if (s >= DB) ok = wait_bar(dfree + pd, ((s / DB) - 1) & 1, abort_flag) && ok;
         ok = wait_bar(full + slot, (s / NS) & 1, abort_flag) && ok;
         if (ok && !*abort_flag && jg < static_cast<int>(it.cur_ng)) {
           tc_fence_after();
           const uint32_t a_base = tmem + pa * 128;
           const uint32_t b_base = smem_u32(ring + slot * SB + kWBytes);
-          const uint32_t d = tmem + 256 + ((pa * 2 + jg) * CH + ch) * NM;
+          const uint32_t d = tmem + 256 + ((pd * 2 + jg) * CH + ch) * NM;
 #pragma unroll
           for (int kk = ch; kk < 8; kk += CH) {
             const int kb = jg * 8 + kk;  // 16-channel step within the stage
             const uint64_t bd = smem_desc_sw128(b_base + (kb >> 2) * (NM * 128) + (kb & 3) * 32);
             mma_bf16_ts(d, a_base + kb * 8, bd, idesc, kk >= CH ? 1u : 0u);
+            if constexpr (OFFSET) mma_bf16_ts(d, tmem + kConstCol, bd, idesc, 1u);
           }
         }
         mma_commit(empty + slot);
         mma_commit(afree + pa);
-        mma_commit(dfull + pa);
+        mma_commit(dfull + pd);
         ++s;
       }
       mma_commit(done);
@@ -404,6 +420,16 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
       }
     }
 
+    if constexpr (OFFSET) {
+      // the constant A operand: -136 (bf16 0xC308) in every element of this warp's 32 lanes
+      if (h == 0) {
+        const uint32_t neg136[8] = {0xC308C308u, 0xC308C308u, 0xC308C308u, 0xC308C308u,
+                                    0xC308C308u, 0xC308C308u, 0xC308C308u, 0xC308C308u};
+        tmem_st8(tmem + lane_base + kConstCol, neg136);
+        tmem_wait_st();  // ordered before the MMAs by the first stage's afull hand-over
+      }
+    }
+
     float acc[HALF];
 #pragma unroll
     for (int t = 0; t < HALF; ++t) acc[t] = 0.0f;
@@ -414,47 +440,58 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
       int n_tile, m_tile;
       bool last;
       float s0, s1;
-    } prev{};
-    bool has_prev = false;
+    };
 
-    auto drain = [&](const Pending& p) {
-      const int pa = p.s & 1;
-      const bool ok = wait_bar(dfull + pa, (p.s >> 1) & 1, abort_flag);
+    // Accumulator registers of one stage between issuing its TMEM loads and using them: chain 0
+    // of each group in d0 / d1, the second chain (CH = 2) in e0 / e1.
+    struct DrainRegs {
+      uint32_t d0[HALF], d1[HALF], e0[CH > 1 ? HALF : 1], e1[CH > 1 ? HALF : 1];
+    };
+
+    // Waits for the stage's MMAs and issues its TMEM loads (not yet waited for).
+    auto drain_issue = [&](const Pending& p, DrainRegs& r) -> bool {
+      const int pd = p.s % DB;
+      const bool ok = wait_bar(dfull + pd, (p.s / DB) & 1, abort_flag);
       tc_fence_after();
-      uint32_t d0[HALF], d1[HALF];
       if (ok) {
-        // chain 0 of each group, then the other chains into e0 / e1 (added below)
-        uint32_t e0[HALF], e1[HALF];
+        const uint32_t dcol = tmem + lane_base + 256 + pd * 2 * CH * NM + h * HALF;
 #pragma unroll
         for (int c8 = 0; c8 < HALF / 8; ++c8) {
-          tmem_ld8(tmem + lane_base + 256 + ((pa * 2 + 0) * CH) * NM + h * HALF + 8 * c8, d0 + 8 * c8);
-          if (CH > 1) tmem_ld8(tmem + lane_base + 256 + ((pa * 2 + 0) * CH + 1) * NM + h * HALF + 8 * c8, e0 + 8 * c8);
+          tmem_ld8(dcol + 8 * c8, r.d0 + 8 * c8);
+          if constexpr (CH > 1) tmem_ld8(dcol + NM + 8 * c8, r.e0 + 8 * c8);
         }
         if (p.ng == 2) {
 #pragma unroll
           for (int c8 = 0; c8 < HALF / 8; ++c8) {
-            tmem_ld8(tmem + lane_base + 256 + ((pa * 2 + 1) * CH) * NM + h * HALF + 8 * c8, d1 + 8 * c8);
-            if (CH > 1) tmem_ld8(tmem + lane_base + 256 + ((pa * 2 + 1) * CH + 1) * NM + h * HALF + 8 * c8, e1 + 8 * c8);
+            tmem_ld8(dcol + CH * NM + 8 * c8, r.d1 + 8 * c8);
+            if constexpr (CH > 1) tmem_ld8(dcol + CH * NM + NM + 8 * c8, r.e1 + 8 * c8);
           }
         }
+      }
+      return ok;
+    };
+
+    // Completes the loads, releases the D buffer and adds s[n, g] * D into the running sums.
+    auto drain_finish = [&](const Pending& p, DrainRegs& r, bool ok) {
+      if (ok) {
         tmem_wait_ld();
-        if (CH > 1) {
+        if constexpr (CH > 1) {
 #pragma unroll
           for (int t = 0; t < HALF; ++t) {
-            d0[t] = __float_as_uint(__uint_as_float(d0[t]) + __uint_as_float(e0[t]));
-            if (p.ng == 2) d1[t] = __float_as_uint(__uint_as_float(d1[t]) + __uint_as_float(e1[t]));
+            r.d0[t] = __float_as_uint(__uint_as_float(r.d0[t]) + __uint_as_float(r.e0[t]));
+            if (p.ng == 2) r.d1[t] = __float_as_uint(__uint_as_float(r.d1[t]) + __uint_as_float(r.e1[t]));
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dfree + pa);
+      if (lane == 0) mbar_arrive(dfree + p.s % DB);
       if (!ok || *abort_flag) return;
 #pragma unroll
-      for (int t = 0; t < HALF; ++t) acc[t] = fmaf(p.s0, __uint_as_float(d0[t]), acc[t]);
+      for (int t = 0; t < HALF; ++t) acc[t] = fmaf(p.s0, __uint_as_float(r.d0[t]), acc[t]);
       if (p.ng == 2) {
 #pragma unroll
-        for (int t = 0; t < HALF; ++t) acc[t] = fmaf(p.s1, __uint_as_float(d1[t]), acc[t]);
+        for (int t = 0; t < HALF; ++t) acc[t] = fmaf(p.s1, __uint_as_float(r.d1[t]), acc[t]);
       }
       if constexpr (MODE != kA16) {
         if (a.acc_out) {
@@ -465,12 +502,18 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
             const int m = m0 + t;
             if (m < M && n < N) {
               int32_t* dst = a.acc_out + (static_cast<long long>(m) * N + n) * G + p.g;
-              dst[0] = static_cast<int32_t>(__uint_as_float(d0[t]));
-              if (p.ng == 2) dst[1] = static_cast<int32_t>(__uint_as_float(d1[t]));
+              dst[0] = static_cast<int32_t>(__uint_as_float(r.d0[t]));
+              if (p.ng == 2) dst[1] = static_cast<int32_t>(__uint_as_float(r.d1[t]));
             }
           }
         }
       }
+    };
+
+    auto drain = [&](const Pending& p) {
+      DrainRegs r;
+      const bool ok = drain_issue(p, r);
+      drain_finish(p, r, ok);
     };
 
     auto token_scale = [&](int m) -> float {
@@ -513,29 +556,51 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
         named_bar_sync(1, kWorkerWarps * 32);
         if (misc->last) {
           __threadfence();
-          float sum[HALF];
+          // Contributor c_first may have begun in an earlier tile (this tile is then its slot 1);
+          // every later contributor begins inside this tile (slot 0): c * U / P > tile * G for
+          // c > c_first, and it is at most the tile's last unit for c <= c_last.
+          const uint32_t first_beg = static_cast<uint32_t>(static_cast<uint64_t>(c_first) * U / P);
+          const uint32_t first_slot = first_beg / G == tile ? 0u : 1u;
+          // acc is already published above, so it is reused as the running sum of all
+          // contributors' partials, added in CTA order with kFixBatch contributors' loads in flight
 #pragma unroll
-          for (int t = 0; t < HALF; ++t) sum[t] = 0.0f;
-          for (uint32_t cc = c_first; cc <= c_last; ++cc) {
-            const uint32_t cc_beg = static_cast<uint32_t>(static_cast<uint64_t>(cc) * U / P);
-            const int sl = (tile == cc_beg / G) ? 0 : 1;
-            const float* src = a.partial + ((static_cast<size_t>(cc) * 2 + sl) * 128 + row) * NM + h * HALF;
+          for (int t = 0; t < HALF; ++t) acc[t] = 0.0f;
+          constexpr int NV = HALF / 4;  // float4 per contributor
+          constexpr int kFixBatch = NM == 16 ? 8 : 1;
+          const float* pbase = a.partial + static_cast<size_t>(row) * NM + h * HALF;
+          for (uint32_t c0 = c_first; c0 <= c_last; c0 += kFixBatch) {
+            float4 v[kFixBatch][NV];
 #pragma unroll
-            for (int t = 0; t < HALF; t += 4) {
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(src + t));
-              sum[t] += v.x;
-              sum[t + 1] += v.y;
-              sum[t + 2] += v.z;
-              sum[t + 3] += v.w;
+            for (int j = 0; j < kFixBatch; ++j) {
+              const uint32_t cc = c0 + j;
+              const uint32_t sl = cc == c_first ? first_slot : 0u;
+              const float4* src = reinterpret_cast<const float4*>(pbase + (static_cast<size_t>(cc) * 2 + sl) * 128 * NM);
+#pragma unroll
+              for (int t = 0; t < NV; ++t) v[j][t] = cc <= c_last ? __ldcg(src + t) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int j = 0; j < kFixBatch; ++j) {
+              if (c0 + j <= c_last) {
+#pragma unroll
+                for (int t = 0; t < NV; ++t) {
+                  acc[4 * t] += v[j][t].x;
+                  acc[4 * t + 1] += v[j][t].y;
+                  acc[4 * t + 2] += v[j][t].z;
+                  acc[4 * t + 3] += v[j][t].w;
+                }
+              }
             }
           }
-          if (!*abort_flag) store_y(p, sum);
+          if (!*abort_flag) store_y(p, acc);
           if (wt == 0) a.ticket[tile] = 0;
         }
       }
 #pragma unroll
       for (int t = 0; t < HALF; ++t) acc[t] = 0.0f;
     };
+
+    Pending prev{};
+    bool has_prev = false;
 
     StageIter it(u_beg, u_end, G, a.T_m);
     int s = 0;
@@ -545,10 +610,13 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
       if (s >= 2) ok = wait_bar(afree + pa, ((s >> 1) - 1) & 1, abort_flag) && ok;
       Pending cur{s, static_cast<int>(it.cur_ng), static_cast<int>(it.cur_g), it.cur_tile,
                   static_cast<int>(it.cur_n_tile), static_cast<int>(it.cur_m_tile), it.cur_last, 0.0f, 0.0f};
-      if (ok && !*abort_flag) {
+      const bool work = ok && !*abort_flag;
+      const bool convert = work && h < static_cast<int>(it.cur_ng);
+      uint8_t* st = ring + slot * SB;
+      const uint8_t* wrow = st + row * 128;  // this warp's 128 codes: one group of 32 rows
+      if (work) {
         cur.s0 = __half2float(sc[slot * 256 + row]);
         cur.s1 = __half2float(sc[slot * 256 + 128 + row]);
-        uint8_t* st = ring + slot * SB;
         if constexpr (MODE == kA4Fused) {
           // activation tile -> INT4 codes (as exact bf16) in place, rows m < M
           uint8_t* bst = st + kWBytes;
@@ -563,16 +631,15 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
           }
           fence_proxy_async_smem();
         }
-        if (h < static_cast<int>(it.cur_ng)) {
-          const uint8_t* wrow = st + row * 128;
+        if (convert) {
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((((4 * h + cc) ^ (row & 7))) << 4));
             uint32_t out[16];
-            codes_to_bf16x2(v.x, out);
-            codes_to_bf16x2(v.y, out + 4);
-            codes_to_bf16x2(v.z, out + 8);
-            codes_to_bf16x2(v.w, out + 12);
+            codes_to_bf16x2<OFFSET>(v.x, out);
+            codes_to_bf16x2<OFFSET>(v.y, out + 4);
+            codes_to_bf16x2<OFFSET>(v.z, out + 8);
+            codes_to_bf16x2<OFFSET>(v.w, out + 12);
             tmem_st16(tmem + lane_base + pa * 128 + h * 64 + cc * 16, out);
           }
           tmem_wait_st();
@@ -597,11 +664,13 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
       if (prev.last) epilogue(prev);
     }
   }
-
+  // Lane 0 of the producer and issuer warps ran its role alone; reconverge every warp before the
+  // CTA barrier (a partially arrived warp must not count as arrived), so TMEM is released only
+  // after every worker has finished reading it.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -5,6 +5,11 @@
 // the verify (W4A16) mode.  The quantiser is the plain symmetric one, per group of 128 input
 // channels: s = fp16(amax / 7), code = clamp(rint(w / s), -8, 7), codes 0 when s == 0.
 //
+// Packed layout: each 32-bit little-endian word holds 8 consecutive channels k = 8t..8t+7 as two's
+// complement nibbles, the even channels (8t+0, 2, 4, 6) in nibbles 0..3 and the odd ones
+// (8t+1, 3, 5, 7) in nibbles 4..7, so that a shift and a mask bring any (even, odd) channel pair to
+// the low bits of the two half-words (the pages fix no bit order; this one suits the converters).
+//
 // Launch shape: a half-warp per group (8 bf16 = one 16-byte load per lane), two groups per warp.
 // A row of W is K contiguous bf16 and K % 128 == 0, so group q covers the flat elements
 // [128q, 128q + 128) of W, the flat bytes [64q, 64q + 64) of Wp and the flat entry q of S.
@@ -47,7 +52,8 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(const uint16_t* __res
     for (int i = 0; i < 8; ++i) {
       float c = rintf(__fdiv_rn(__uint_as_float(w[i] << 16), sf));
       c = fminf(fmaxf(c, -8.0f), 7.0f);
-      packed |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xFu) << (4 * i);
+      // channel 8j + i goes to nibble (i >> 1) + 4 (i & 1): even channels in the low half-word
+      packed |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xFu) << (4 * ((i >> 1) + 4 * (i & 1)));
     }
   }
   if (valid) {

@@ -33,15 +33,26 @@ def bf16_bits(values):
 # ---------------------------------------------------------------- a1: weight quantiser / packer
 
 def check_pack_layout(o):
-    # byte j holds k = 2j in bits 0..3 and k = 2j+1 in bits 4..7, two's complement
+    # little-endian word t holds k = 8t+0,2,4,6 in nibbles 0..3 and k = 8t+1,3,5,7 in nibbles
+    # 4..7, two's complement: k0..k7 = 1,-2,7,-8,0,-1,3,4 give nibbles 1,7,0,3,E,8,F,4
     codes = np.array([[1, -2, 7, -8, 0, -1, 3, 4]], dtype=np.int8)
-    assert o.pack_codes(codes).tolist() == [[0xE1, 0x87, 0xF0, 0x43]]
+    assert o.pack_codes(codes).tolist() == [[0x71, 0x30, 0x8E, 0x4F]]
+    word = int.from_bytes(bytes(o.pack_codes(codes)[0]), "little")
+    assert [(word >> (4 * i)) & 0xF for i in range(8)] == [0x1, 0x7, 0x0, 0x3, 0xE, 0x8, 0xF, 0x4]
     # every byte value round-trips through unpack / pack
     allb = np.arange(256, dtype=np.uint8).reshape(1, 256)
     c = o.unpack_codes(allb)
     assert c.min() == -8 and c.max() == 7
-    assert c[0, 2 * 0x9F] == -1 and c[0, 2 * 0x9F + 1] == -7  # 0x9F: low nibble F (-1), high 9 (-7)
+    # byte 0x9F = 159 is byte 3 of word 39: nibble 6 (F = -1) is k = 312 + 5, nibble 7 (9 = -7) k = 312 + 7
+    assert c[0, 317] == -1 and c[0, 319] == -7
     assert np.array_equal(o.pack_codes(c), allb)
+    # one code at every position of a word lands in the nibble the layout names
+    for k in range(8):
+        one = np.zeros((1, 8), dtype=np.int8)
+        one[0, k] = 5
+        w = int.from_bytes(bytes(o.pack_codes(one)[0]), "little")
+        slot = (0, 4, 1, 5, 2, 6, 3, 7)[k]
+        assert w == 5 << (4 * slot)
 
 
 def check_weight_grid_roundtrip(o):
@@ -97,7 +108,8 @@ def check_pack_end_to_end(o):
     row[0, :4] = [7.0, -1.0, 2.0, -7.0]
     Wp, S = o.pack_weights(bf16_bits(row))
     assert Wp.shape == (1, 64) and S.shape == (1, 1)
-    assert Wp[0, 0] == 0xF7 and Wp[0, 1] == 0x92 and float(S[0, 0]) == 1.0
+    # codes 7, -1, 2, -7: word 0 nibbles (k0, k2, k4, k6, k1, k3, k5, k7) = 7, 2, 0, 0, F, 9, 0, 0
+    assert Wp[0, :4].tolist() == [0x27, 0x00, 0x9F, 0x00] and float(S[0, 0]) == 1.0
 
 
 # ---------------------------------------------------------------- a2: W4A16

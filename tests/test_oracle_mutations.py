@@ -15,7 +15,8 @@ MUTATIONS = [
     ("weight scale not fp16-rounded before coding", "s = S.astype(np.float32)[:, :, None]",
      "s = s32[:, :, None]"),
     ("weight rounding half up", "q = np.clip(np.rint(q), -8, 7)", "q = np.clip(np.floor(q + 0.5), -8, 7)"),
-    ("nibble order swapped", "return (lo | (hi << 4)).astype(np.uint8)", "return (hi | (lo << 4)).astype(np.uint8)"),
+    ("nibble order swapped", "byte = nib[:, :, 0::2] | (nib[:, :, 1::2] << 4)", "byte = nib[:, :, 1::2] | (nib[:, :, 0::2] << 4)"),
+    ("natural channel order in a word", "WORD_ORDER = (0, 2, 4, 6, 1, 3, 5, 7)", "WORD_ORDER = (0, 1, 2, 3, 4, 5, 6, 7)"),
     ("unpack without sign", "out = np.where(out >= 8, out - 16, out)", "out = out"),
     ("group scale tiled instead of repeated", "scale = np.repeat(S.astype(np.float64), GROUP, axis=1)",
      "scale = np.tile(S.astype(np.float64), (1, GROUP))"),

@@ -543,10 +543,16 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
       if (c_first == c_last) {
         if (!*abort_flag) store_y(p, acc);
       } else {
+        // only the float4 columns of this warp's token half that hold real tokens travel
+        constexpr int NV = HALF / 4;
+        const int m_here = min(NM, M - p.m_tile * a.NMrows);
+        const int nv = max(0, min(NV, (m_here - h * HALF + 3) / 4));
         const int my_slot = (tile == u_beg / G) ? 0 : 1;
         float* part = a.partial + ((static_cast<size_t>(c) * 2 + my_slot) * 128 + row) * NM + h * HALF;
 #pragma unroll
-        for (int t = 0; t < HALF; t += 4) *reinterpret_cast<float4*>(part + t) = make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]);
+        for (int t = 0; t < NV; ++t)
+          if (t < nv)
+            *reinterpret_cast<float4*>(part + 4 * t) = make_float4(acc[4 * t], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
         __threadfence();
         named_bar_sync(1, kWorkerWarps * 32);
         if (wt == 0) {
@@ -565,7 +571,6 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
           // contributors' partials, added in CTA order with kFixBatch contributors' loads in flight
 #pragma unroll
           for (int t = 0; t < HALF; ++t) acc[t] = 0.0f;
-          constexpr int NV = HALF / 4;  // float4 per contributor
           constexpr int kFixBatch = NM == 16 ? 8 : 1;
           const float* pbase = a.partial + static_cast<size_t>(row) * NM + h * HALF;
           for (uint32_t c0 = c_first; c0 <= c_last; c0 += kFixBatch) {
@@ -576,7 +581,8 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
               const uint32_t sl = cc == c_first ? first_slot : 0u;
               const float4* src = reinterpret_cast<const float4*>(pbase + (static_cast<size_t>(cc) * 2 + sl) * 128 * NM);
 #pragma unroll
-              for (int t = 0; t < NV; ++t) v[j][t] = cc <= c_last ? __ldcg(src + t) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+              for (int t = 0; t < NV; ++t)
+                v[j][t] = (cc <= c_last && t < nv) ? __ldcg(src + t) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
 #pragma unroll
             for (int j = 0; j < kFixBatch; ++j) {

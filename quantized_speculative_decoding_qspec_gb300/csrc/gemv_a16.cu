@@ -33,7 +33,15 @@ namespace {
 
 constexpr int kThreads = 512;  // 16 warps, one CTA per SM
 constexpr int kWarps = kThreads / 32;
-constexpr int kDepth = 4;      // groups of weights in flight per warp
+
+// 16 bytes of packed weights, read once: not kept in L1
+__device__ __forceinline__ uint4 ld_weights(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
 
 // pair i of a packed word (channels 2i, 2i + 1 of its 8) -> exact bf16x2 codes
 __device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
@@ -53,8 +61,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// MT = token slots staged in shared memory (4 or 8); tokens >= M contribute zeros.
-template <int MT>
+// MT = token slots staged in shared memory (4 or 8); tokens >= M contribute zeros.  D = weight
+// groups in flight per warp (a divisor of the groups per K slice, so that register slots line up
+// with tile boundaries).
+//
+// A warp's work is one stream of (row tile, group) items: the tiles r * stride + blockIdx.x * per_cta
+// + wtile for r = 0, 1, ..., and within each its K slice of groups.  Weights are fetched D items
+// ahead across tile boundaries, so the stream never drains; the first fetches are issued before
+// the kernel waits for its predecessor (no library kernel that may run ahead of this one writes
+// packed weights or scales).
+template <int MT, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_a16_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ Wp, const __half* __restrict__ S,
                     int M, int N, int K, int KS, uint16_t* __restrict__ y) {
@@ -62,9 +78,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = K / kGroup;
   // activations: chunk ((gi * 4 + j) * MT + m) * 4 + t holds x[m, 128 gi + 32 t + 8 j .. + 7]
   uint4* xs = reinterpret_cast<uint4*>(sm);
-  float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(G) * 16 * MT);  // [kWarps][32]
+  float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(G) * 16 * MT);  // [2][kWarps][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+
+  const int tiles = (N + 15) / 16;
+  const int per_cta = kWarps / KS;  // row tiles a CTA works on at once
+  const int wtile = warp / KS, ks = warp - wtile * KS;
+  const int gs = G / KS, g_beg = ks * gs;
+  const int stride = gridDim.x * per_cta;
+  const int tile0 = blockIdx.x * per_cta + wtile;
+  const int rounds = (tiles + stride - 1) / stride;  // the same for the KS warps of a tile slot
+  const size_t row_bytes = static_cast<size_t>(K) / 2;
+
+  // fetch cursor: the tile, its row pointers (at the slice's first group) and the group index
+  const uint8_t* f_wlo = Wp;
+  const uint8_t* f_whi = Wp;
+  const __half* f_slo = S;
+  const __half* f_shi = S;
+  bool f_vlo = false, f_vhi = false;
+  int f_tile = tile0, f_i = 0;
+  auto point = [&]() {
+    const int n_lo = f_tile * 16 + g, n_hi = n_lo + 8;
+    f_vlo = f_tile < tiles && n_lo < N;
+    f_vhi = f_tile < tiles && n_hi < N;
+    f_wlo = Wp + static_cast<size_t>(f_vlo ? n_lo : 0) * row_bytes + g_beg * 64 + t * 16;
+    f_whi = Wp + static_cast<size_t>(f_vhi ? n_hi : 0) * row_bytes + g_beg * 64 + t * 16;
+    f_slo = S + static_cast<size_t>(f_vlo ? n_lo : 0) * G + g_beg;
+    f_shi = S + static_cast<size_t>(f_vhi ? n_hi : 0) * G + g_beg;
+  };
+  uint4 wl[D], wh[D];
+  float sl[D], sh[D];
+  auto fetch = [&](int k) {  // next item of the stream into register slot k
+    wl[k] = f_vlo ? ld_weights(f_wlo + f_i * 64) : make_uint4(0, 0, 0, 0);
+    wh[k] = f_vhi ? ld_weights(f_whi + f_i * 64) : make_uint4(0, 0, 0, 0);
+    sl[k] = f_vlo ? __half2float(f_slo[f_i]) : 0.0f;
+    sh[k] = f_vhi ? __half2float(f_shi[f_i]) : 0.0f;
+    if (++f_i == gs) {
+      f_i = 0;
+      f_tile += stride;
+      point();
+    }
+  };
+  point();
+#pragma unroll
+  for (int k = 0; k < D; ++k) fetch(k);
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -79,71 +137,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  const int tiles = (N + 15) / 16;
-  const int per_cta = kWarps / KS;  // row tiles a CTA works on at once
-  const int wtile = warp / KS, ks = warp - wtile * KS;
-  const int gs = G / KS, g_beg = ks * gs;
-  const int stride = gridDim.x * per_cta;
-  const int rounds = (tiles + stride - 1) / stride;  // the same for every warp (barriers below)
-  const size_t row_bytes = static_cast<size_t>(K) / 2;
-
   for (int r = 0; r < rounds; ++r) {
-    const int tile = r * stride + blockIdx.x * per_cta + wtile;
-    const int n_lo = tile * 16 + g, n_hi = n_lo + 8;
-    const bool v_lo = tile < tiles && n_lo < N, v_hi = tile < tiles && n_hi < N;
-    const uint8_t* w_lo = Wp + static_cast<size_t>(v_lo ? n_lo : 0) * row_bytes + t * 16;
-    const uint8_t* w_hi = Wp + static_cast<size_t>(v_hi ? n_hi : 0) * row_bytes + t * 16;
-    const __half* s_lo = S + static_cast<size_t>(v_lo ? n_lo : 0) * G;
-    const __half* s_hi = S + static_cast<size_t>(v_hi ? n_hi : 0) * G;
-
-    uint4 wl[kDepth], wh[kDepth];
-    float sl[kDepth], sh[kDepth];
-    auto fetch = [&](int k, int i) {  // group g_beg + i into register slot k
-      const bool ok = i < gs;
-      const int gi = g_beg + i;
-      wl[k] = ok && v_lo ? ld_stream_v4(w_lo + gi * 64) : make_uint4(0, 0, 0, 0);
-      wh[k] = ok && v_hi ? ld_stream_v4(w_hi + gi * 64) : make_uint4(0, 0, 0, 0);
-      sl[k] = ok && v_lo ? __half2float(s_lo[gi]) : 0.0f;
-      sh[k] = ok && v_hi ? __half2float(s_hi[gi]) : 0.0f;
-    };
+    const int tile = r * stride + tile0;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // rows (tile * 16 + g, + 8) x tokens (2t, 2t + 1)
+    for (int i0 = 0; i0 < gs; i0 += D) {
 #pragma unroll
-    for (int k = 0; k < kDepth; ++k) fetch(k, k);
-
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // rows (n_lo, n_hi) x tokens (2t, 2t + 1)
-    for (int i0 = 0; i0 < gs; i0 += kDepth) {
+      for (int k = 0; k < D; ++k) {
+        const uint4* xg = xs + static_cast<size_t>(g_beg + i0 + k) * 16 * MT;
+        const uint32_t lo[4] = {wl[k].x, wl[k].y, wl[k].z, wl[k].w};
+        const uint32_t hi[4] = {wh[k].x, wh[k].y, wh[k].z, wh[k].w};
+        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int k = 0; k < kDepth; ++k) {
-        const int i = i0 + k;
-        if (i < gs) {
-          const uint4* xg = xs + static_cast<size_t>(g_beg + i) * 16 * MT;
-          const uint32_t lo[4] = {wl[k].x, wl[k].y, wl[k].z, wl[k].w};
-          const uint32_t hi[4] = {wh[k].x, wh[k].y, wh[k].z, wh[k].w};
-          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 xb = make_uint4(0, 0, 0, 0);
-            if (MT == 8 || g < MT) xb = xg[(j * MT + g) * 4 + t];
-            mma_16816(d, code_pair(lo[j], 0), code_pair(hi[j], 0), code_pair(lo[j], 1), code_pair(hi[j], 1), xb.x,
-                      xb.y);
-            mma_16816(d, code_pair(lo[j], 2), code_pair(hi[j], 2), code_pair(lo[j], 3), code_pair(hi[j], 3), xb.z,
-                      xb.w);
-          }
-          acc[0] = fmaf(sl[k], d[0], acc[0]);
-          acc[1] = fmaf(sl[k], d[1], acc[1]);
-          acc[2] = fmaf(sh[k], d[2], acc[2]);
-          acc[3] = fmaf(sh[k], d[3], acc[3]);
+        for (int j = 0; j < 4; ++j) {
+          uint4 xb = make_uint4(0, 0, 0, 0);
+          if (MT == 8 || g < MT) xb = xg[(j * MT + g) * 4 + t];
+          mma_16816(d, code_pair(lo[j], 0), code_pair(hi[j], 0), code_pair(lo[j], 1), code_pair(hi[j], 1), xb.x,
+                    xb.y);
+          mma_16816(d, code_pair(lo[j], 2), code_pair(hi[j], 2), code_pair(lo[j], 3), code_pair(hi[j], 3), xb.z,
+                    xb.w);
         }
-        fetch(k, i + kDepth);
+        acc[0] = fmaf(sl[k], d[0], acc[0]);
+        acc[1] = fmaf(sl[k], d[1], acc[1]);
+        acc[2] = fmaf(sh[k], d[2], acc[2]);
+        acc[3] = fmaf(sh[k], d[3], acc[3]);
+        fetch(k);
       }
     }
-
-    if (KS > 1) {  // K slices of a tile: summed in slice order by the slice-0 warp
-      red[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      __syncthreads();
+    if (KS > 1) {  // K slices summed in slice order by the slice-0 warp of the tile slot
+      float4* rb = red + (r & 1) * kWarps * 32;
+      rb[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + wtile), "r"(KS * 32) : "memory");
       if (ks == 0) {
-        float4 s4 = red[warp * 32 + lane];
+        float4 s4 = rb[warp * 32 + lane];
         for (int j = 1; j < KS; ++j) {
-          const float4 o = red[(warp + j) * 32 + lane];
+          const float4 o = rb[(warp + j) * 32 + lane];
           s4.x += o.x;
           s4.y += o.y;
           s4.z += o.z;
@@ -155,19 +182,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[3] = s4.w;
       }
     }
-    if (ks == 0) {
+    if (ks == 0 && tile < tiles) {
+      const int n_lo = tile * 16 + g, n_hi = n_lo + 8;
       const int m0 = 2 * t, m1 = 2 * t + 1;
-      if (v_lo && m0 < M) y[static_cast<size_t>(m0) * N + n_lo] = f32_to_bf16_bits(acc[0]);
-      if (v_lo && m1 < M) y[static_cast<size_t>(m1) * N + n_lo] = f32_to_bf16_bits(acc[1]);
-      if (v_hi && m0 < M) y[static_cast<size_t>(m0) * N + n_hi] = f32_to_bf16_bits(acc[2]);
-      if (v_hi && m1 < M) y[static_cast<size_t>(m1) * N + n_hi] = f32_to_bf16_bits(acc[3]);
+      if (n_lo < N && m0 < M) y[static_cast<size_t>(m0) * N + n_lo] = f32_to_bf16_bits(acc[0]);
+      if (n_lo < N && m1 < M) y[static_cast<size_t>(m1) * N + n_lo] = f32_to_bf16_bits(acc[1]);
+      if (n_hi < N && m0 < M) y[static_cast<size_t>(m0) * N + n_hi] = f32_to_bf16_bits(acc[2]);
+      if (n_hi < N && m1 < M) y[static_cast<size_t>(m1) * N + n_hi] = f32_to_bf16_bits(acc[3]);
     }
-    if (KS > 1) __syncthreads();  // red is reused by the next round
   }
 }
 
 size_t smem_bytes(int MT, int K) {
-  return static_cast<size_t>(K / kGroup) * 16 * MT * 16 + static_cast<size_t>(kWarps) * 32 * 16;
+  return static_cast<size_t>(K / kGroup) * 16 * MT * 16 + 2 * static_cast<size_t>(kWarps) * 32 * 16;
+}
+
+template <int MT, int D>
+qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+                      int best_ks, int best_grid, cudaStream_t stream) {
+  const size_t smem = smem_bytes(MT, K);
+  auto kern = gemv_a16_kernel<MT, D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return QSPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(best_grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, y) == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
 }
 
 template <int MT>
@@ -191,21 +238,10 @@ qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M
       best_grid = grid;
     }
   }
-  const size_t smem = smem_bytes(MT, K);
-  auto kern = gemv_a16_kernel<MT>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-    return QSPEC_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(best_grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, y) == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
+  const int gs = G / best_ks;
+  if (gs % 4 == 0) return launch_d<MT, 4>(x, Wp, S, M, N, K, y, best_ks, best_grid, stream);
+  if (gs % 2 == 0) return launch_d<MT, 2>(x, Wp, S, M, N, K, y, best_ks, best_grid, stream);
+  return launch_d<MT, 1>(x, Wp, S, M, N, K, y, best_ks, best_grid, stream);
 }
 
 }  // namespace

@@ -165,9 +165,12 @@ __global__ void __launch_bounds__(kThreads, 3) gemv_a4_kernel(const uint16_t* __
 
   uint4 wa[kBatch], wb[kBatch];
   float sa_[kBatch], sb_[kBatch];
+  // The first weights are requested before waiting for the predecessor kernel (no library kernel
+  // that may run ahead of this one writes packed weights or scales), so their latency overlaps its
+  // tail and the activation quantiser below.
+  load_item(0, 0, wa, sa_);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  load_item(0, 0, wa, sa_);  // the first weights are in flight while the activations are quantised
   quantise_tokens<M>(x, K, codes, csum, s_a, amax_bits, xq_out, xs_out);
 
   float yacc[M];

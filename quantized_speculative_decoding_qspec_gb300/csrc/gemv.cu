@@ -1,12 +1,14 @@
-// Verify-mode (W4A16) linear for decode-sized M (1..8 tokens): register-resident dequantised
-// weight fragments fed straight into warp-level tensor-core MMAs.
+// Both linears at decode sizes (M = 1..8 tokens): register-resident weight fragments fed straight
+// into warp-level tensor-core MMAs.
 //
 // QSpec article ("QSpec実行時の2つの量子化による推論の一致率を調べる"), section
 // "W4A4 と W4A16 量子化": W4A16 keeps the 16-bit activations and converts the 4-bit weights while
-// multiplying.  At decode sizes the product is a GEMV bound by the weight stream (0.5 B per weight);
-// the tcgen05 path would have to expand every weight to bf16 in TMEM (4x the streamed bytes, written
-// and read back on chip), which measured slower than the HBM stream itself, so here the expanded
-// weights never leave registers:
+// multiplying; W4A4 also quantises the activations to 4 bits (per token here: s_a = amax / 7 in
+// fp32, codes = clamp(rint(x / s_a), -8, 7)).  Section "QSpec の W4A4 モードと W4A16 モード": both
+// modes read the same packed weights.  At decode sizes the product is a GEMV bound by the weight
+// stream (0.5 B per weight); the tcgen05 path would have to expand every weight to bf16 in TMEM
+// (4x the streamed bytes, written and read back on chip), which measured slower than the HBM stream
+// itself, so here the expanded weights never leave registers:
 //
 //  * a warp owns 16 weight rows x a K slice.  Lane (g, t) = (lane / 4, lane % 4) loads 16 bytes of
 //    each of its two rows g and g + 8 per 128-channel group: packed words 4t..4t+3, i.e. channels
@@ -16,9 +18,12 @@
 //    fragment register of mma.m16n8k16: the MMA's 16 k-slots of lane t are mapped onto the
 //    channels lane t holds (a fixed permutation of K inside the group), and the activations are
 //    staged in shared memory in exactly that order, so one 16-byte shared load gives the B
-//    fragments of two MMAs;
+//    fragments of two MMAs.  W4A4 stages the activation codes, as bf16 (exact), in the same place:
+//    every product and every 128-channel sum is then a small integer, exact in the fp32 MMA
+//    accumulator, so the group sums are the exact integer sums of code * code;
 //  * per group the fp32 MMA result is scaled by s[n, g] and accumulated in fp32; K slices of a
-//    tile are summed through shared memory in a fixed order; y is rounded to bf16 once.
+//    tile are summed through shared memory in a fixed order; W4A4 multiplies by s_a at the end;
+//    y is rounded to bf16 once.
 //
 // Tokens are the MMA's N = 8 side (rows >= M are zero), weight rows its M = 16 side.
 #include <cuda_bf16.h>
@@ -52,6 +57,19 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// a / b rounded to nearest (IEEE), given rb = 1 / b rounded to nearest: Markstein's division
+// refinement -- q0 = a * rb is within one ulp of a / b, the FMA gives the remainder a - b q0
+// exactly, and one more FMA rounds q0 + remainder * rb correctly.  That needs the remainder to be
+// representable: with b >= 2^-100 it is whenever |a / b| >= 1/4, the only quotients whose rounding
+// can change a code (smaller ones give code 0 either way).  The quantiser keeps the IEEE division
+// for smaller b.  Checked exhaustively against the IEEE division for every bf16 amax (b = amax / 7)
+// and every bf16 |a| <= amax: identical codes, identical quotients wherever |a / b| >= 1/4.
+__device__ __forceinline__ float div_rn_markstein(float a, float b, float rb) {
+  const float q0 = a * rb;
+  const float r = fmaf(-b, q0, a);
+  return fmaf(r, rb, q0);
+}
+
 // d += A (16 x 16, row fragments a0..a3) * B (16 x 8, column fragments b0, b1), fp32 accumulate
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -61,6 +79,8 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// A4: W4A4 (quantise the tokens, optional int8 codes / fp32 scales out); ACC: also the int32 group
+// sums (a separate instantiation keeps their stores out of the hot loop when not asked for).
 // MT = token slots staged in shared memory (4 or 8); tokens >= M contribute zeros.  D = weight
 // groups in flight per warp (a divisor of the groups per K slice, so that register slots line up
 // with tile boundaries).
@@ -70,15 +90,18 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // ahead across tile boundaries, so the stream never drains; the first fetches are issued before
 // the kernel waits for its predecessor (no library kernel that may run ahead of this one writes
 // packed weights or scales).
-template <int MT, int D>
+template <bool A4, bool ACC, int MT, int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemv_a16_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ Wp, const __half* __restrict__ S,
-                    int M, int N, int K, int KS, uint16_t* __restrict__ y) {
+    gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ Wp, const __half* __restrict__ S,
+                int M, int N, int K, int KS, uint16_t* __restrict__ y, int8_t* __restrict__ xq_out,
+                float* __restrict__ xs_out, int32_t* __restrict__ acc_out) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int G = K / kGroup;
   // activations: chunk ((gi * 4 + j) * MT + m) * 4 + t holds x[m, 128 gi + 32 t + 8 j .. + 7]
   uint4* xs = reinterpret_cast<uint4*>(sm);
   float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(G) * 16 * MT);  // [2][kWarps][32]
+  __shared__ unsigned int red_max[A4 ? kWarps * MT : 1];
+  __shared__ float s_a[MT], s_r[MT];  // per-token scale and its reciprocal (rounded to nearest)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
@@ -127,13 +150,106 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  for (int c = threadIdx.x; c < G * 16 * MT; c += kThreads) {
-    const int ct = c & 3, cm = (c >> 2) % MT, rest = c / (4 * MT);
-    const int cj = rest & 3, gi = rest >> 2;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (cm < M)
-      v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(cm) * K + gi * 128 + ct * 32 + cj * 8));
-    xs[c] = v;
+  // Staging: chunk (gi, j, t) of token m <- x[m, 128 gi + 32 t + 8 j .. + 7].  Slots of tokens
+  // M..MT-1 are never written: they only feed MMA columns that are not stored.  A thread loads its
+  // kU chunks before using any, so one L2 round trip covers them (all of x, for the usual sizes,
+  // which W4A4 then keeps in registers between its two passes).
+  const int per_token = G * 16;
+  const int total = M * per_token;
+  constexpr int kU = 4;
+  auto locate = [&](int c, int& m, int& v) {
+    m = c / per_token;
+    v = c - m * per_token;  // (gi * 4 + j) * 4 + t
+  };
+  auto src_of = [&](int m, int v) {
+    const int t_ = v & 3, j_ = (v >> 2) & 3, gi = v >> 4;
+    return static_cast<size_t>(m) * K + gi * 128 + t_ * 32 + j_ * 8;
+  };
+  auto load_batch = [&](int c0, uint4 (&u)[kU]) {
+#pragma unroll
+    for (int e = 0; e < kU; ++e) {
+      const int c = c0 + e * kThreads;
+      int m = 0, v = 0;
+      if (c < total) locate(c, m, v);
+      u[e] = c < total ? __ldg(reinterpret_cast<const uint4*>(x + src_of(m, v))) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto store_batch = [&](int c0, const uint4 (&u)[kU]) {
+#pragma unroll
+    for (int e = 0; e < kU; ++e) {
+      const int c = c0 + e * kThreads;
+      if (c >= total) continue;
+      int m, v;
+      locate(c, m, v);
+      uint4 val = u[e];
+      if constexpr (A4) {  // codes = clamp(rint(x / s_a), -8, 7), kept as exact bf16
+        const float sa = s_a[m], rsa = s_r[m];
+        const bool fast = sa >= 0x1p-100f;  // see div_rn_markstein
+        uint32_t w[4] = {val.x, val.y, val.z, val.w};
+        uint32_t q8[2] = {0, 0};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float c0f = 0.0f, c1f = 0.0f;
+          if (sa != 0.0f) {
+            const float x0 = bf16_lo(w[i]), x1 = bf16_hi(w[i]);
+            const float q0 = fast ? div_rn_markstein(x0, sa, rsa) : __fdiv_rn(x0, sa);
+            const float q1 = fast ? div_rn_markstein(x1, sa, rsa) : __fdiv_rn(x1, sa);
+            c0f = fminf(fmaxf(rintf(q0), -8.0f), 7.0f);
+            c1f = fminf(fmaxf(rintf(q1), -8.0f), 7.0f);
+          }
+          w[i] = static_cast<uint32_t>(f32_to_bf16_bits(c0f)) | (static_cast<uint32_t>(f32_to_bf16_bits(c1f)) << 16);
+          q8[i >> 1] |= ((static_cast<uint32_t>(static_cast<int>(c0f)) & 0xFFu) |
+                         ((static_cast<uint32_t>(static_cast<int>(c1f)) & 0xFFu) << 8))
+                        << (16 * (i & 1));
+        }
+        val = make_uint4(w[0], w[1], w[2], w[3]);
+        if (xq_out && blockIdx.x == 0) *reinterpret_cast<uint2*>(xq_out + src_of(m, v)) = make_uint2(q8[0], q8[1]);
+      }
+      xs[((v >> 2) * MT + m) * 4 + (v & 3)] = val;
+    }
+  };
+  const bool single = total <= kU * kThreads;
+  uint4 u[kU];
+  if (single) load_batch(threadIdx.x, u);
+  if constexpr (A4) {
+    // per-token amax over all of K (bf16 bit patterns of |x| order like the values)
+    unsigned int mx[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) mx[m] = 0;
+    for (int c0 = threadIdx.x; c0 < total; c0 += kU * kThreads) {
+      if (!single) load_batch(c0, u);
+#pragma unroll
+      for (int e = 0; e < kU; ++e) {
+        const int c = c0 + e * kThreads;
+        if (c >= total) continue;
+        const unsigned int a =
+            max(max(max(u[e].x & 0x7FFFu, (u[e].x >> 16) & 0x7FFFu), max(u[e].y & 0x7FFFu, (u[e].y >> 16) & 0x7FFFu)),
+                max(max(u[e].z & 0x7FFFu, (u[e].z >> 16) & 0x7FFFu), max(u[e].w & 0x7FFFu, (u[e].w >> 16) & 0x7FFFu)));
+        const int m = c / per_token;
+#pragma unroll
+        for (int mm = 0; mm < MT; ++mm)
+          if (mm == m) mx[mm] = max(mx[mm], a);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xFFFFFFFFu, mx[m], off));
+      if (lane == 0) red_max[warp * MT + m] = mx[m];
+    }
+    __syncthreads();
+    if (threadIdx.x < M) {
+      unsigned int m_all = 0;
+      for (int w = 0; w < kWarps; ++w) m_all = max(m_all, red_max[w * MT + threadIdx.x]);
+      s_a[threadIdx.x] = __fdiv_rn(__uint_as_float(m_all << 16), 7.0f);
+      s_r[threadIdx.x] = __frcp_rn(s_a[threadIdx.x]);
+      if (xs_out && blockIdx.x == 0) xs_out[threadIdx.x] = s_a[threadIdx.x];
+    }
+    __syncthreads();
+  }
+  for (int c0 = threadIdx.x; c0 < total; c0 += kU * kThreads) {
+    if (!single) load_batch(c0, u);
+    store_batch(c0, u);
   }
   __syncthreads();
 
@@ -160,6 +276,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[1] = fmaf(sl[k], d[1], acc[1]);
         acc[2] = fmaf(sh[k], d[2], acc[2]);
         acc[3] = fmaf(sh[k], d[3], acc[3]);
+        if constexpr (A4 && ACC) {
+          if (tile < tiles) {  // exact integer group sums
+            const int n_lo = tile * 16 + g, n_hi = n_lo + 8, gi = g_beg + i0 + k;
+            const int m0 = 2 * t, m1 = 2 * t + 1;
+            if (n_lo < N && m0 < M) acc_out[(static_cast<size_t>(m0) * N + n_lo) * G + gi] = static_cast<int32_t>(d[0]);
+            if (n_lo < N && m1 < M) acc_out[(static_cast<size_t>(m1) * N + n_lo) * G + gi] = static_cast<int32_t>(d[1]);
+            if (n_hi < N && m0 < M) acc_out[(static_cast<size_t>(m0) * N + n_hi) * G + gi] = static_cast<int32_t>(d[2]);
+            if (n_hi < N && m1 < M) acc_out[(static_cast<size_t>(m1) * N + n_hi) * G + gi] = static_cast<int32_t>(d[3]);
+          }
+        }
         fetch(k);
       }
     }
@@ -185,6 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ks == 0 && tile < tiles) {
       const int n_lo = tile * 16 + g, n_hi = n_lo + 8;
       const int m0 = 2 * t, m1 = 2 * t + 1;
+      if constexpr (A4) {
+        const float sa0 = m0 < M ? s_a[m0] : 0.0f, sa1 = m1 < M ? s_a[m1] : 0.0f;
+        acc[0] *= sa0;
+        acc[1] *= sa1;
+        acc[2] *= sa0;
+        acc[3] *= sa1;
+      }
       if (n_lo < N && m0 < M) y[static_cast<size_t>(m0) * N + n_lo] = f32_to_bf16_bits(acc[0]);
       if (n_lo < N && m1 < M) y[static_cast<size_t>(m1) * N + n_lo] = f32_to_bf16_bits(acc[1]);
       if (n_hi < N && m0 < M) y[static_cast<size_t>(m0) * N + n_hi] = f32_to_bf16_bits(acc[2]);
@@ -197,11 +330,17 @@ size_t smem_bytes(int MT, int K) {
   return static_cast<size_t>(K / kGroup) * 16 * MT * 16 + 2 * static_cast<size_t>(kWarps) * 32 * 16;
 }
 
-template <int MT, int D>
+struct Outs {
+  int8_t* xq;
+  float* xs;
+  int32_t* acc;
+};
+
+template <bool A4, bool ACC, int MT, int D>
 qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
-                      int best_ks, int best_grid, cudaStream_t stream) {
+                      Outs o, int best_ks, int best_grid, cudaStream_t stream) {
   const size_t smem = smem_bytes(MT, K);
-  auto kern = gemv_a16_kernel<MT, D>;
+  auto kern = gemv_kernel<A4, ACC, MT, D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return QSPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -214,19 +353,21 @@ qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, y) == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, y, o.xq, o.xs, o.acc) == cudaSuccess
+             ? QSPEC_OK
+             : QSPEC_ERR_CUDA;
 }
 
-template <int MT>
+template <bool A4, int MT>
 qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
-                    cudaStream_t stream) {
+                    Outs o, cudaStream_t stream) {
   const int G = K / kGroup;
   const long long tiles = (static_cast<long long>(N) + 15) / 16;
   const int sms = num_sms();
   // K split: the fewest rounds of (groups per slice + fixed cost), ties to the wider grid
   int best_ks = 1, best_grid = 1;
   long long best_cost = -1;
-  for (int ks = 1; ks <= 16; ks *= 2) {
+  for (int ks = 1; ks <= kWarps; ks *= 2) {
     if (G % ks != 0) continue;
     const long long slots = kWarps / ks;
     const int grid = static_cast<int>(std::min<long long>(sms, (tiles + slots - 1) / slots));
@@ -239,22 +380,31 @@ qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M
     }
   }
   const int gs = G / best_ks;
-  if (gs % 4 == 0) return launch_d<MT, 4>(x, Wp, S, M, N, K, y, best_ks, best_grid, stream);
-  if (gs % 2 == 0) return launch_d<MT, 2>(x, Wp, S, M, N, K, y, best_ks, best_grid, stream);
-  return launch_d<MT, 1>(x, Wp, S, M, N, K, y, best_ks, best_grid, stream);
+  if constexpr (A4) {
+    if (o.acc) {  // the checking path: group sums out, no need for the deepest prefetch
+      if (gs % 2 == 0) return launch_d<true, true, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+      return launch_d<true, true, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+    }
+  }
+  if (gs % 4 == 0) return launch_d<A4, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+  if (gs % 2 == 0) return launch_d<A4, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+  return launch_d<A4, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
 }
 
 }  // namespace
 
-bool gemv_a16_supported(int M, int N, int K) {
+bool gemv_supported(int M, int N, int K) {
   if (M < 1 || M > 8 || N < 1 || K % kGroup != 0) return false;
   return smem_bytes(M <= 4 ? 4 : 8, K) <= 200 * 1024;
 }
 
-qspec_status gemv_a16(const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K, uint16_t* y,
-                      cudaStream_t stream) {
+qspec_status gemv(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
+                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream) {
   const __half* Sh = reinterpret_cast<const __half*>(S);
-  return M <= 4 ? launch<4>(x, Wp, Sh, M, N, K, y, stream) : launch<8>(x, Wp, Sh, M, N, K, y, stream);
+  const Outs o{xq_out, xs_out, acc_out};
+  if (a4)
+    return M <= 4 ? launch<true, 4>(x, Wp, Sh, M, N, K, y, o, stream) : launch<true, 8>(x, Wp, Sh, M, N, K, y, o, stream);
+  return M <= 4 ? launch<false, 4>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 8>(x, Wp, Sh, M, N, K, y, o, stream);
 }
 
 }  // namespace qspec

@@ -214,8 +214,8 @@ extern "C" qspec_status qspec_linear_w4a16(const uint16_t* x, const uint8_t* Wp,
   if (!ws) return QSPEC_ERR_WORKSPACE;
   if (!qspec::aligned16(ws)) return QSPEC_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (qspec::gemv_a16_supported(int(M), int(N), int(K)))
-    return qspec::gemv_a16(x, Wp, S, int(M), int(N), int(K), y, s);
+  if (qspec::gemv_supported(int(M), int(N), int(K)))
+    return qspec::gemv(false, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, s);
   if (qspec::linear_tc_supported(false, int(M), int(N), int(K)))
     return qspec::linear_tc(false, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, ws, ws_bytes, s);
   return qspec::linear_simt(false, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, s);
@@ -233,8 +233,8 @@ extern "C" qspec_status qspec_linear_w4a4(const uint16_t* x, const uint8_t* Wp, 
   if (!ws) return QSPEC_ERR_WORKSPACE;
   if (!qspec::aligned16(ws)) return QSPEC_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (qspec::gemv_a4_supported(int(M), int(N), int(K)))
-    return qspec::gemv_a4(x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, s);
+  if (qspec::gemv_supported(int(M), int(N), int(K)))
+    return qspec::gemv(true, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, s);
   if (qspec::linear_tc_supported(true, int(M), int(N), int(K)))
     return qspec::linear_tc(true, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, ws, ws_bytes, s);
   return qspec::linear_simt(true, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, s);

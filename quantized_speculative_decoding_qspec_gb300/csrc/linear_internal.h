@@ -20,15 +20,10 @@ qspec_status linear_tc(bool a4, const uint16_t* x, const uint8_t* Wp, const uint
                        int N, int K, uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out,
                        void* ws, size_t ws_bytes, cudaStream_t stream);
 
-// CUDA-core dp4a GEMV for W4A4 at decode sizes (M <= 4).
-bool gemv_a4_supported(int M, int N, int K);
-qspec_status gemv_a4(const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K, uint16_t* y,
-                     int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream);
-
-// Register-fragment MMA GEMV for W4A16 at decode sizes (M <= 8; the staged activations must fit).
-bool gemv_a16_supported(int M, int N, int K);
-qspec_status gemv_a16(const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K, uint16_t* y,
-                      cudaStream_t stream);
+// Register-fragment MMA GEMV for both modes at decode sizes (M <= 8; the staged activations must fit).
+bool gemv_supported(int M, int N, int K);
+qspec_status gemv(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
+                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream);
 
 // Reads (synchronously) and clears the error bits the linear kernels set on the current device.
 qspec_status read_and_clear_linear_error(cudaStream_t stream, unsigned int* bits);

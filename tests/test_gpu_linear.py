@@ -123,6 +123,31 @@ def test_w4a4_extreme_codes(q):
     assert rel_fro(bf16_host_f64(y), oracle.linear_w4a16(X, Wp_ref, S_ref)) <= W4A16_TOL
 
 
+@pytest.mark.parametrize("amax", [1.0, 7.0, 0.3, 1.0e-3, 123.5, 3.0e5, 3.0e38, 1.0e-29, 2.0e-30, 1.0e-37])
+def test_activation_quantiser_dense_bf16(q, amax):
+    # Each token holds its amax and then the 16383 largest bf16 magnitudes below it, signs
+    # alternating: every quotient x / s_a that can round differently lies in this range, and the
+    # codes and scales must equal the oracle's bit for bit.
+    K, M, N = 16384, 4, 16
+    top = int(oracle.f64_to_bf16_bits(np.array([amax]))[0])
+    X = np.zeros((M, K), dtype=np.uint16)
+    for m in range(M):
+        a_bits = top - m  # four neighbouring amax values
+        mags = np.maximum(np.arange(a_bits - 1, a_bits - K, -1), 0).astype(np.uint16)
+        signs = np.where(np.arange(K - 1) % 2 == 0, 0, 0x8000).astype(np.uint16)
+        X[m, 0] = a_bits
+        X[m, 1:] = mags | signs
+    W = syn.weights(N, K, 7)
+    Wp, S, Wp_ref, S_ref = check_pack(q, W)
+    xq = torch.empty(M, K, dtype=torch.int8, device=DEV)
+    xs = torch.empty(M, dtype=torch.float32, device=DEV)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    q.qspec_linear_w4a4(bf16_dev(X), Wp, S, y, q.new_linear_workspace(M, N, K), xq, xs)
+    qa, s_a = oracle.quantize_activations(X)
+    assert np.array_equal(xs.cpu().numpy().view(np.uint32), s_a.view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy(), qa)
+
+
 def test_zero_activation_token(q):
     N, K, M = 64, 256, 3
     W = syn.weights(N, K, 5)

@@ -76,6 +76,16 @@ def peaks():
         return 6800.0, "fallback"
 
 
+# CUDA sources each kernel family's launches are built from (a change to any of them invalidates the
+# recorded DRAM traffic)
+KERNEL_SOURCES = {
+    "linear_w4a4": ["gemv.cu", "linear.cu", "common.cuh"],
+    "linear_w4a16": ["gemv.cu", "linear.cu", "common.cuh"],
+    "verify_greedy": ["verify.cu", "common.cuh"],
+    "verify_sample": ["verify.cu", "common.cuh"],
+}
+
+
 def kernel_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -85,15 +95,16 @@ def kernel_traffic(kernel):
         ent = d[kernel]
     except Exception:
         return None
-    if ent.get("source_sha256") != source_hash():
+    if ent.get("source_sha256") != source_hash(KERNEL_SOURCES[kernel]):
         return None
     return ent.get("dram_bytes_per_launch")
 
 
-def source_hash():
+def source_hash(files):
+    """sha256 over the named files of the library's csrc directory (name + contents, in order)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_speculative_decoding_qspec_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in files:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()
@@ -411,6 +422,7 @@ def gpu_arm(args, rank, world):
     fam_bytes = {"w4a4": sb["w4a4"], "w4a16": sb["w4a16"],
                  "greedy": verify_bytes(1, GAMMA, VOCAB, False), "sample": verify_bytes(1, GAMMA, VOCAB, True)}
     fam_time = {f: family_time(f) for f in fam_bytes}
+    fam_launches = {"w4a4": GAMMA * len(LAYERS), "w4a16": len(LAYERS), "greedy": 1, "sample": 2}
     dominant = max(fam_time, key=fam_time.get)
     hbm_peak, peak_kind = peaks()
     achieved = fam_bytes[dominant] / fam_time[dominant] / 1e9
@@ -486,6 +498,7 @@ def gpu_arm(args, rank, world):
                      "peak": hbm_peak, "peak_source": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4),
                      "traffic": kernel_traffic(kernel_names[dominant]),
+                     "algorithmic_bytes_per_launch": fam_bytes[dominant] // fam_launches[dominant],
                      "algorithmic_bytes_per_step": fam_bytes[dominant],
                      "timing": f"CUDA events around the kernel family in {n_inst - n_kern} steps of the timed region"},
         "breakdown": {

@@ -640,6 +640,54 @@ def sweep_linear():
         q.qspec_check_status()
 
 
+def sweep_batched():
+    """Batched verify (16 sequences x gamma = 3): W4A16 at M = 64 and W4A4 at M = 16 on the
+    Llama-3-8B shapes, and greedy verify over [64, 128256] bf16 logits with per-sequence accept
+    lengths.  One JSON line per item."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as g
+    g.build()
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+    from quantized_speculative_decoding_qspec_gb300 import synthetic as syn
+    dev = torch.device("cuda", 0)
+    hbm, _ = peaks()
+    for li, (name, N, K) in enumerate(LAYERS):
+        W = torch.from_numpy(syn.weights(N, K, 2, layer=li).view(np.int16)).to(dev).view(torch.bfloat16)
+        Wp = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+        S = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+        q.qspec_pack_weights(W, Wp, S)
+        del W
+        for M, mode in ((64, "a16"), (16, "a4")):
+            x = torch.from_numpy(syn.activations(M, K, 2, step=M).view(np.int16)).to(dev).view(torch.bfloat16)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            ws = q.new_linear_workspace(M, N, K, device=dev)
+            fn = ((lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws)) if mode == "a16"
+                  else (lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws)))
+            t = _graph_time(fn)
+            b = linear_bytes(M, N, K)
+            print(json.dumps({"sweep": "batched_linear", "layer": name, "N": N, "K": K, "M": M, "mode": mode,
+                              "us": round(t * 1e6, 2), "GB_s": round(b / t / 1e9, 1),
+                              "hbm_frac": round(b / t / 1e9 / hbm, 3), "l2_resident": b < 100e6,
+                              "TOPS": round(2 * M * N * K / t / 1e12, 2)}), flush=True)
+        q.qspec_check_status()
+        del Wp, S
+    B, gamma = 16, GAMMA
+    inp = syn.verify_inputs(B, gamma, VOCAB, 0.5, workload_id=2, sampling=False)
+    gt = torch.from_numpy(np.ascontiguousarray(inp["tgt"]).view(np.int16)).to(dev).view(torch.bfloat16)
+    gd = torch.from_numpy(inp["d"]).to(dev)
+    gws = q.new_verify_workspace(B, gamma, VOCAB, device=dev)
+    gn = torch.empty(B, dtype=torch.int32, device=dev)
+    go = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+    t = _graph_time(lambda: q.qspec_verify_greedy(gt, gd, gn, go, gws), reps=10, iters=3)
+    q.qspec_check_status(gws)
+    b = verify_bytes(B, gamma, VOCAB, False)
+    print(json.dumps({"sweep": "batched_greedy_verify", "B": B, "gamma": gamma, "V": VOCAB,
+                      "us": round(t * 1e6, 2), "GB_s": round(b / t / 1e9, 1), "hbm_frac": round(b / t / 1e9 / hbm, 3),
+                      "l2_resident": b < 100e6, "accept_len": gn.cpu().tolist()}), flush=True)
+
+
 def sweep_sampling(quick=False):
     """Sampling-verify sweep: gamma x batch x vocab x draft noise.  Per cell: time, logits GB/s,
     positions/s, mean emitted tokens per sequence and call, and E[T] = (1 - a^(g+1)) / (1 - a)
@@ -662,6 +710,23 @@ def sweep_sampling(quick=False):
     for gamma in gammas:
         for B in batches:
             for V in vocabs:
+                # greedy verify on the same shapes (it does not depend on the draft noise)
+                ginp = syn.verify_inputs(B, gamma, V, 0.5, workload_id=4, sampling=False)
+                gt = bf(ginp["tgt"])
+                gd = torch.from_numpy(ginp["d"]).to(dev)
+                gws = q.new_verify_workspace(B, gamma, V, device=dev)
+                gn = torch.empty(B, dtype=torch.int32, device=dev)
+                go = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+                tg = _graph_time(lambda: q.qspec_verify_greedy(gt, gd, gn, go, gws), reps=10, iters=3)
+                q.qspec_check_status(gws)
+                bg = verify_bytes(B, gamma, V, False)
+                print(json.dumps({"sweep": "greedy_verify", "gamma": gamma, "B": B, "V": V,
+                                  "us": round(tg * 1e6, 2), "GB_s": round(bg / tg / 1e9, 1),
+                                  "hbm_frac": round(bg / tg / 1e9 / hbm, 3),
+                                  "l2_resident": bg < 100e6,
+                                  "positions_per_s": round(B * (gamma + 1) / tg, 1),
+                                  "tokens_per_call": round(float(gn.float().mean().item()) + 1, 3)}), flush=True)
+                del gt, gd, gws
                 for sigma in sigmas:
                     inp = syn.verify_inputs(B, gamma, V, sigma, workload_id=4, sampling=True)
                     tgt, drf = bf(inp["tgt"]), bf(inp["drf"])
@@ -680,7 +745,7 @@ def sweep_sampling(quick=False):
                     b = verify_bytes(B, gamma, V, True)
                     print(json.dumps({"sweep": "sampling_verify", "gamma": gamma, "B": B, "V": V, "sigma": sigma,
                                       "us": round(t * 1e6, 2), "GB_s": round(b / t / 1e9, 1),
-                                      "hbm_frac": round(b / t / 1e9 / hbm, 3),
+                                      "hbm_frac": round(b / t / 1e9 / hbm, 3), "l2_resident": b < 100e6,
                                       "positions_per_s": round(B * (gamma + 1) / t, 1),
                                       "tokens_per_call": round(float(n.float().mean().item()) + 1, 3),
                                       "mean_accept_prob": round(alpha, 4), "E_T_at_mean_alpha": round(et, 3)}),
@@ -689,7 +754,7 @@ def sweep_sampling(quick=False):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--sweep", choices=["linear", "sampling", "sampling-quick"], default=None,
+    ap.add_argument("--sweep", choices=["linear", "batched", "sampling", "sampling-quick"], default=None,
                     help="measurement sweeps instead of the step benchmark")
     ap.add_argument("--profile-case", default=None,
                     help="run only one kernel of the step, e.g. lm_head:a4:1 or verify:greedy (for ncu)")
@@ -713,6 +778,9 @@ def main():
         return
     if args.sweep == "linear":
         sweep_linear()
+        return
+    if args.sweep == "batched":
+        sweep_batched()
         return
     if args.sweep in ("sampling", "sampling-quick"):
         sweep_sampling(quick=args.sweep == "sampling-quick")

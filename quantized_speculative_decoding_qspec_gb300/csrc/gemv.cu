@@ -1,4 +1,4 @@
-// Both linears at decode sizes (M = 1..8 tokens): register-resident weight fragments fed straight
+// Both linears at decode sizes (M = 1..16 tokens): register-resident weight fragments fed straight
 // into warp-level tensor-core MMAs.
 //
 // QSpec article ("QSpec実行時の2つの量子化による推論の一致率を調べる"), section
@@ -10,7 +10,7 @@
 // (4x the streamed bytes, written and read back on chip), which measured slower than the HBM stream
 // itself, so here the expanded weights never leave registers:
 //
-//  * a warp owns 16 weight rows x a K slice.  Lane (g, t) = (lane / 4, lane % 4) loads 16 bytes of
+//  * a warp owns 16 weight rows x a K slice (x up to 16 tokens in two MMA column blocks of 8).  Lane (g, t) = (lane / 4, lane % 4) loads 16 bytes of
 //    each of its two rows g and g + 8 per 128-channel group: packed words 4t..4t+3, i.e. channels
 //    32t..32t+31 of the group;
 //  * one shift + LOP3 + bf16 subtract turns a nibble pair of a word into an exact bf16x2 code pair
@@ -81,7 +81,8 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 
 // A4: W4A4 (quantise the tokens, optional int8 codes / fp32 scales out); ACC: also the int32 group
 // sums (a separate instantiation keeps their stores out of the hot loop when not asked for).
-// MT = token slots staged in shared memory (4 or 8); tokens >= M contribute zeros.  D = weight
+// MT = token slots staged in shared memory (1, 2, 4, 8 or 16; tokens >= M contribute zeros); the
+// tokens form NB = ceil(MT / 8) MMA column blocks of 8 that share every weight fragment.  D = weight
 // groups in flight per warp (a divisor of the groups per K slice, so that register slots line up
 // with tile boundaries).
 //
@@ -99,7 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = K / kGroup;
   // activations: chunk ((gi * 4 + j) * MT + m) * 4 + t holds x[m, 128 gi + 32 t + 8 j .. + 7]
   uint4* xs = reinterpret_cast<uint4*>(sm);
-  float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(G) * 16 * MT);  // [2][kWarps][32]
+  constexpr int NB = (MT + 7) / 8;
+  float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(G) * 16 * MT);  // [2][kWarps][NB][32]
   __shared__ unsigned int red_max[A4 ? kWarps * MT : 1];
   __shared__ float s_a[MT], s_r[MT];  // per-token scale and its reciprocal (rounded to nearest)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -174,63 +176,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       u[e] = c < total ? __ldg(reinterpret_cast<const uint4*>(x + src_of(m, v))) : make_uint4(0, 0, 0, 0);
     }
   };
-  auto store_batch = [&](int c0, const uint4 (&u)[kU]) {
+  auto slot_of = [&](int m, int v) { return ((v >> 2) * MT + m) * 4 + (v & 3); };
+  // W4A4: codes = clamp(rint(x / s_a), -8, 7) of one chunk, as exact bf16 (and the int8 codes out)
+  auto quantise = [&](int m, int v, uint4 val) {
+    const float sa = s_a[m], rsa = s_r[m];
+    const bool fast = sa >= 0x1p-100f;  // see div_rn_markstein
+    uint32_t w[4] = {val.x, val.y, val.z, val.w};
+    uint32_t q8[2] = {0, 0};
 #pragma unroll
-    for (int e = 0; e < kU; ++e) {
-      const int c = c0 + e * kThreads;
-      if (c >= total) continue;
-      int m, v;
-      locate(c, m, v);
-      uint4 val = u[e];
-      if constexpr (A4) {  // codes = clamp(rint(x / s_a), -8, 7), kept as exact bf16
-        const float sa = s_a[m], rsa = s_r[m];
-        const bool fast = sa >= 0x1p-100f;  // see div_rn_markstein
-        uint32_t w[4] = {val.x, val.y, val.z, val.w};
-        uint32_t q8[2] = {0, 0};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float c0f = 0.0f, c1f = 0.0f;
-          if (sa != 0.0f) {
-            const float x0 = bf16_lo(w[i]), x1 = bf16_hi(w[i]);
-            const float q0 = fast ? div_rn_markstein(x0, sa, rsa) : __fdiv_rn(x0, sa);
-            const float q1 = fast ? div_rn_markstein(x1, sa, rsa) : __fdiv_rn(x1, sa);
-            c0f = fminf(fmaxf(rintf(q0), -8.0f), 7.0f);
-            c1f = fminf(fmaxf(rintf(q1), -8.0f), 7.0f);
-          }
-          w[i] = static_cast<uint32_t>(f32_to_bf16_bits(c0f)) | (static_cast<uint32_t>(f32_to_bf16_bits(c1f)) << 16);
-          q8[i >> 1] |= ((static_cast<uint32_t>(static_cast<int>(c0f)) & 0xFFu) |
-                         ((static_cast<uint32_t>(static_cast<int>(c1f)) & 0xFFu) << 8))
-                        << (16 * (i & 1));
-        }
-        val = make_uint4(w[0], w[1], w[2], w[3]);
-        if (xq_out && blockIdx.x == 0) *reinterpret_cast<uint2*>(xq_out + src_of(m, v)) = make_uint2(q8[0], q8[1]);
+    for (int i = 0; i < 4; ++i) {
+      float c0f = 0.0f, c1f = 0.0f;
+      if (sa != 0.0f) {
+        const float x0 = bf16_lo(w[i]), x1 = bf16_hi(w[i]);
+        const float q0 = fast ? div_rn_markstein(x0, sa, rsa) : __fdiv_rn(x0, sa);
+        const float q1 = fast ? div_rn_markstein(x1, sa, rsa) : __fdiv_rn(x1, sa);
+        c0f = fminf(fmaxf(rintf(q0), -8.0f), 7.0f);
+        c1f = fminf(fmaxf(rintf(q1), -8.0f), 7.0f);
       }
-      xs[((v >> 2) * MT + m) * 4 + (v & 3)] = val;
+      w[i] = static_cast<uint32_t>(f32_to_bf16_bits(c0f)) | (static_cast<uint32_t>(f32_to_bf16_bits(c1f)) << 16);
+      q8[i >> 1] |= ((static_cast<uint32_t>(static_cast<int>(c0f)) & 0xFFu) |
+                     ((static_cast<uint32_t>(static_cast<int>(c1f)) & 0xFFu) << 8))
+                    << (16 * (i & 1));
     }
+    if (xq_out && blockIdx.x == 0) *reinterpret_cast<uint2*>(xq_out + src_of(m, v)) = make_uint2(q8[0], q8[1]);
+    return make_uint4(w[0], w[1], w[2], w[3]);
   };
-  const bool single = total <= kU * kThreads;
-  uint4 u[kU];
-  if (single) load_batch(threadIdx.x, u);
-  if constexpr (A4) {
-    // per-token amax over all of K (bf16 bit patterns of |x| order like the values)
-    unsigned int mx[MT];
+  auto chunk_amax = [](uint4 val) {
+    return max(max(max(val.x & 0x7FFFu, (val.x >> 16) & 0x7FFFu), max(val.y & 0x7FFFu, (val.y >> 16) & 0x7FFFu)),
+               max(max(val.z & 0x7FFFu, (val.z >> 16) & 0x7FFFu), max(val.w & 0x7FFFu, (val.w >> 16) & 0x7FFFu)));
+  };
+  // per-token amax (bf16 bit patterns of |x| order like the values) -> s_a = amax / 7, 1 / s_a
+  unsigned int mx[A4 ? MT : 1];
+  auto amax_add = [&](int m, uint4 val) {
+    const unsigned int am = chunk_amax(val);
 #pragma unroll
-    for (int m = 0; m < MT; ++m) mx[m] = 0;
-    for (int c0 = threadIdx.x; c0 < total; c0 += kU * kThreads) {
-      if (!single) load_batch(c0, u);
-#pragma unroll
-      for (int e = 0; e < kU; ++e) {
-        const int c = c0 + e * kThreads;
-        if (c >= total) continue;
-        const unsigned int a =
-            max(max(max(u[e].x & 0x7FFFu, (u[e].x >> 16) & 0x7FFFu), max(u[e].y & 0x7FFFu, (u[e].y >> 16) & 0x7FFFu)),
-                max(max(u[e].z & 0x7FFFu, (u[e].z >> 16) & 0x7FFFu), max(u[e].w & 0x7FFFu, (u[e].w >> 16) & 0x7FFFu)));
-        const int m = c / per_token;
-#pragma unroll
-        for (int mm = 0; mm < MT; ++mm)
-          if (mm == m) mx[mm] = max(mx[mm], a);
-      }
-    }
+    for (int mm = 0; mm < MT; ++mm)
+      if (mm == m) mx[mm] = max(mx[mm], am);
+  };
+  auto finish_scales = [&]() {
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
 #pragma unroll
@@ -246,88 +229,160 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (xs_out && blockIdx.x == 0) xs_out[threadIdx.x] = s_a[threadIdx.x];
     }
     __syncthreads();
+  };
+  if constexpr (A4) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) mx[m] = 0;
   }
-  for (int c0 = threadIdx.x; c0 < total; c0 += kU * kThreads) {
-    if (!single) load_batch(c0, u);
-    store_batch(c0, u);
+  uint4 u[kU];
+  if (total <= kU * kThreads) {
+    // one batch: x stays in registers between the passes
+    load_batch(threadIdx.x, u);
+    if constexpr (A4) {
+#pragma unroll
+      for (int e = 0; e < kU; ++e) {
+        const int c = threadIdx.x + e * kThreads;
+        if (c < total) amax_add(c / per_token, u[e]);
+      }
+      finish_scales();
+    }
+#pragma unroll
+    for (int e = 0; e < kU; ++e) {
+      const int c = threadIdx.x + e * kThreads;
+      if (c >= total) continue;
+      int m, v;
+      locate(c, m, v);
+      xs[slot_of(m, v)] = A4 ? quantise(m, v, u[e]) : u[e];
+    }
+  } else {
+    // several batches: x goes to shared memory as it is, W4A4 then works there (no second trip
+    // to L2)
+    for (int c0 = threadIdx.x; c0 < total; c0 += kU * kThreads) {
+      load_batch(c0, u);
+#pragma unroll
+      for (int e = 0; e < kU; ++e) {
+        const int c = c0 + e * kThreads;
+        if (c >= total) continue;
+        int m, v;
+        locate(c, m, v);
+        xs[slot_of(m, v)] = u[e];
+        if constexpr (A4) amax_add(m, u[e]);
+      }
+    }
+    if constexpr (A4) {
+      finish_scales();
+      for (int c = threadIdx.x; c < total; c += kThreads) {
+        int m, v;
+        locate(c, m, v);
+        const int sl = slot_of(m, v);
+        xs[sl] = quantise(m, v, xs[sl]);
+      }
+    }
   }
   __syncthreads();
 
   for (int r = 0; r < rounds; ++r) {
     const int tile = r * stride + tile0;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // rows (tile * 16 + g, + 8) x tokens (2t, 2t + 1)
+    // rows (tile * 16 + g, + 8) x tokens (8 nb + 2t, 8 nb + 2t + 1) of column block nb
+    float acc[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
     for (int i0 = 0; i0 < gs; i0 += D) {
 #pragma unroll
       for (int k = 0; k < D; ++k) {
         const uint4* xg = xs + static_cast<size_t>(g_beg + i0 + k) * 16 * MT;
         const uint32_t lo[4] = {wl[k].x, wl[k].y, wl[k].z, wl[k].w};
         const uint32_t hi[4] = {wh[k].x, wh[k].y, wh[k].z, wh[k].w};
-        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float d[NB][4];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) d[nb][0] = d[nb][1] = d[nb][2] = d[nb][3] = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          uint4 xb = make_uint4(0, 0, 0, 0);
-          if (MT == 8 || g < MT) xb = xg[(j * MT + g) * 4 + t];
-          mma_16816(d, code_pair(lo[j], 0), code_pair(hi[j], 0), code_pair(lo[j], 1), code_pair(hi[j], 1), xb.x,
-                    xb.y);
-          mma_16816(d, code_pair(lo[j], 2), code_pair(hi[j], 2), code_pair(lo[j], 3), code_pair(hi[j], 3), xb.z,
-                    xb.w);
+          uint4 xb[NB];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            xb[nb] = make_uint4(0, 0, 0, 0);
+            if (MT % 8 == 0 || g < MT) xb[nb] = xg[(j * MT + nb * 8 + g) * 4 + t];
+          }
+          const uint32_t a0 = code_pair(lo[j], 0), a1 = code_pair(hi[j], 0), a2 = code_pair(lo[j], 1),
+                         a3 = code_pair(hi[j], 1);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_16816(d[nb], a0, a1, a2, a3, xb[nb].x, xb[nb].y);
+          const uint32_t c0 = code_pair(lo[j], 2), c1 = code_pair(hi[j], 2), c2 = code_pair(lo[j], 3),
+                         c3 = code_pair(hi[j], 3);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_16816(d[nb], c0, c1, c2, c3, xb[nb].z, xb[nb].w);
         }
-        acc[0] = fmaf(sl[k], d[0], acc[0]);
-        acc[1] = fmaf(sl[k], d[1], acc[1]);
-        acc[2] = fmaf(sh[k], d[2], acc[2]);
-        acc[3] = fmaf(sh[k], d[3], acc[3]);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          acc[nb][0] = fmaf(sl[k], d[nb][0], acc[nb][0]);
+          acc[nb][1] = fmaf(sl[k], d[nb][1], acc[nb][1]);
+          acc[nb][2] = fmaf(sh[k], d[nb][2], acc[nb][2]);
+          acc[nb][3] = fmaf(sh[k], d[nb][3], acc[nb][3]);
+        }
         if constexpr (A4 && ACC) {
           if (tile < tiles) {  // exact integer group sums
             const int n_lo = tile * 16 + g, n_hi = n_lo + 8, gi = g_beg + i0 + k;
-            const int m0 = 2 * t, m1 = 2 * t + 1;
-            if (n_lo < N && m0 < M) acc_out[(static_cast<size_t>(m0) * N + n_lo) * G + gi] = static_cast<int32_t>(d[0]);
-            if (n_lo < N && m1 < M) acc_out[(static_cast<size_t>(m1) * N + n_lo) * G + gi] = static_cast<int32_t>(d[1]);
-            if (n_hi < N && m0 < M) acc_out[(static_cast<size_t>(m0) * N + n_hi) * G + gi] = static_cast<int32_t>(d[2]);
-            if (n_hi < N && m1 < M) acc_out[(static_cast<size_t>(m1) * N + n_hi) * G + gi] = static_cast<int32_t>(d[3]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const int m0 = nb * 8 + 2 * t, m1 = m0 + 1;
+              if (n_lo < N && m0 < M) acc_out[(static_cast<size_t>(m0) * N + n_lo) * G + gi] = static_cast<int32_t>(d[nb][0]);
+              if (n_lo < N && m1 < M) acc_out[(static_cast<size_t>(m1) * N + n_lo) * G + gi] = static_cast<int32_t>(d[nb][1]);
+              if (n_hi < N && m0 < M) acc_out[(static_cast<size_t>(m0) * N + n_hi) * G + gi] = static_cast<int32_t>(d[nb][2]);
+              if (n_hi < N && m1 < M) acc_out[(static_cast<size_t>(m1) * N + n_hi) * G + gi] = static_cast<int32_t>(d[nb][3]);
+            }
           }
         }
         fetch(k);
       }
     }
     if (KS > 1) {  // K slices summed in slice order by the slice-0 warp of the tile slot
-      float4* rb = red + (r & 1) * kWarps * 32;
-      rb[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      float4* rb = red + (r & 1) * kWarps * NB * 32;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+        rb[(warp * NB + nb) * 32 + lane] = make_float4(acc[nb][0], acc[nb][1], acc[nb][2], acc[nb][3]);
       asm volatile("bar.sync %0, %1;" ::"r"(1 + wtile), "r"(KS * 32) : "memory");
       if (ks == 0) {
-        float4 s4 = rb[warp * 32 + lane];
-        for (int j = 1; j < KS; ++j) {
-          const float4 o = rb[(warp + j) * 32 + lane];
-          s4.x += o.x;
-          s4.y += o.y;
-          s4.z += o.z;
-          s4.w += o.w;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          float4 s4 = rb[(warp * NB + nb) * 32 + lane];
+          for (int j = 1; j < KS; ++j) {
+            const float4 o = rb[((warp + j) * NB + nb) * 32 + lane];
+            s4.x += o.x;
+            s4.y += o.y;
+            s4.z += o.z;
+            s4.w += o.w;
+          }
+          acc[nb][0] = s4.x;
+          acc[nb][1] = s4.y;
+          acc[nb][2] = s4.z;
+          acc[nb][3] = s4.w;
         }
-        acc[0] = s4.x;
-        acc[1] = s4.y;
-        acc[2] = s4.z;
-        acc[3] = s4.w;
       }
     }
     if (ks == 0 && tile < tiles) {
       const int n_lo = tile * 16 + g, n_hi = n_lo + 8;
-      const int m0 = 2 * t, m1 = 2 * t + 1;
-      if constexpr (A4) {
-        const float sa0 = m0 < M ? s_a[m0] : 0.0f, sa1 = m1 < M ? s_a[m1] : 0.0f;
-        acc[0] *= sa0;
-        acc[1] *= sa1;
-        acc[2] *= sa0;
-        acc[3] *= sa1;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int m0 = nb * 8 + 2 * t, m1 = m0 + 1;
+        if constexpr (A4) {
+          const float sa0 = m0 < M ? s_a[m0] : 0.0f, sa1 = m1 < M ? s_a[m1] : 0.0f;
+          acc[nb][0] *= sa0;
+          acc[nb][1] *= sa1;
+          acc[nb][2] *= sa0;
+          acc[nb][3] *= sa1;
+        }
+        if (n_lo < N && m0 < M) y[static_cast<size_t>(m0) * N + n_lo] = f32_to_bf16_bits(acc[nb][0]);
+        if (n_lo < N && m1 < M) y[static_cast<size_t>(m1) * N + n_lo] = f32_to_bf16_bits(acc[nb][1]);
+        if (n_hi < N && m0 < M) y[static_cast<size_t>(m0) * N + n_hi] = f32_to_bf16_bits(acc[nb][2]);
+        if (n_hi < N && m1 < M) y[static_cast<size_t>(m1) * N + n_hi] = f32_to_bf16_bits(acc[nb][3]);
       }
-      if (n_lo < N && m0 < M) y[static_cast<size_t>(m0) * N + n_lo] = f32_to_bf16_bits(acc[0]);
-      if (n_lo < N && m1 < M) y[static_cast<size_t>(m1) * N + n_lo] = f32_to_bf16_bits(acc[1]);
-      if (n_hi < N && m0 < M) y[static_cast<size_t>(m0) * N + n_hi] = f32_to_bf16_bits(acc[2]);
-      if (n_hi < N && m1 < M) y[static_cast<size_t>(m1) * N + n_hi] = f32_to_bf16_bits(acc[3]);
     }
   }
 }
 
 size_t smem_bytes(int MT, int K) {
-  return static_cast<size_t>(K / kGroup) * 16 * MT * 16 + 2 * static_cast<size_t>(kWarps) * 32 * 16;
+  return static_cast<size_t>(K / kGroup) * 16 * MT * 16 + 2 * static_cast<size_t>(kWarps) * ((MT + 7) / 8) * 32 * 16;
 }
 
 struct Outs {
@@ -386,25 +441,35 @@ qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M
       return launch_d<true, true, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
     }
   }
-  if (gs % 4 == 0) return launch_d<A4, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+  // (16 token slots keep two column blocks of accumulators: at most two groups in flight then)
+  if constexpr (MT < 16) {
+    if (gs % 4 == 0) return launch_d<A4, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+  }
   if (gs % 2 == 0) return launch_d<A4, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
   return launch_d<A4, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
 }
 
 }  // namespace
 
+// Token slots for M tokens: the smallest staged width that holds them.
+int token_slots(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+
 bool gemv_supported(int M, int N, int K) {
-  if (M < 1 || M > 8 || N < 1 || K % kGroup != 0) return false;
-  return smem_bytes(M <= 4 ? 4 : 8, K) <= 200 * 1024;
+  if (M < 1 || M > 16 || N < 1 || K % kGroup != 0) return false;
+  return smem_bytes(token_slots(M), K) <= 200 * 1024;
 }
 
 qspec_status gemv(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
                   uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream) {
   const __half* Sh = reinterpret_cast<const __half*>(S);
   const Outs o{xq_out, xs_out, acc_out};
-  if (a4)
-    return M <= 4 ? launch<true, 4>(x, Wp, Sh, M, N, K, y, o, stream) : launch<true, 8>(x, Wp, Sh, M, N, K, y, o, stream);
-  return M <= 4 ? launch<false, 4>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 8>(x, Wp, Sh, M, N, K, y, o, stream);
+  switch (token_slots(M)) {
+    case 1: return a4 ? launch<true, 1>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 1>(x, Wp, Sh, M, N, K, y, o, stream);
+    case 2: return a4 ? launch<true, 2>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 2>(x, Wp, Sh, M, N, K, y, o, stream);
+    case 4: return a4 ? launch<true, 4>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 4>(x, Wp, Sh, M, N, K, y, o, stream);
+    case 8: return a4 ? launch<true, 8>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 8>(x, Wp, Sh, M, N, K, y, o, stream);
+    default: return a4 ? launch<true, 16>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 16>(x, Wp, Sh, M, N, K, y, o, stream);
+  }
 }
 
 }  // namespace qspec

@@ -232,6 +232,16 @@ __device__ __forceinline__ MS ms_merge(MS a, MS b) {
   return {m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
 }
 
+// 2^x from the SFU (ex2.approx: relative error below 2^-22).  Used for the streamed row sums only:
+// the terms that matter have x near 0, and the fp32 summation of ~10^5 terms already carries a
+// larger relative error; the probabilities reported per token use the accurate expf.
+__device__ __forceinline__ float exp2_sfu(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
 __device__ __forceinline__ void ms_add8(MS& a, const float (&v)[8]) {
   float m8 = v[0];
 #pragma unroll
@@ -242,7 +252,7 @@ __device__ __forceinline__ void ms_add8(MS& a, const float (&v)[8]) {
   }
   if (a.m != -INFINITY) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) a.s += expf(v[e] - a.m);
+    for (int e = 0; e < 8; ++e) a.s += exp2_sfu((v[e] - a.m) * kLog2e);
   }
 }
 

@@ -102,6 +102,14 @@ def test_linear_largest_k(q):
     linear_case(q, 4, 128, 14336)
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 64, 28672), (2, 136, 28672), (16, 256, 14336), (8, 200, 14336),
+                                   (12, 520, 4096)])
+def test_linear_staging_widths(q, M, N, K):
+    # one- and two-token staging for long K, and the shapes whose activations do not fit the
+    # GEMV's shared memory (they take the tensor-core kernel)
+    linear_case(q, M, N, K)
+
+
 def test_w4a4_extreme_codes(q):
     # -8 codes in the weights (not produced by the packer but accepted), +-7 activations everywhere
     N, K, M = 16, 256, 2

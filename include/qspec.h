@@ -120,7 +120,7 @@ qspec_status qspec_linear_w4a4(const uint16_t* x, const uint8_t* Wp, const uint1
 size_t qspec_linear_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
- * qspec_verify_workspace_size -- bytes of device workspace that both verify calls need for the
+ * qspec_verify_workspace_size -- bytes of device workspace that the verify calls need for the
  * given shape.  The workspace must be zero-filled before its first use (e.g. one cudaMemset
  * after allocation); every call leaves it ready for the next call.  Returns 0 for invalid sizes.
  */
@@ -179,6 +179,37 @@ qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const uint16_t* dra
                                  int32_t* accept_len, int32_t* out_tok, float* accept_prob,
                                  float* p_tok, float* q_tok, void* ws, size_t ws_bytes,
                                  qspec_stream_t stream);
+
+/*
+ * qspec_verify_top1 -- top-1 statistics of the two modes at every draft position (step f2).
+ *
+ * Article "QSpec実行時の2つの量子化による推論の一致率を調べる", sections "実験：W4A4 と W4A16 の
+ * Top-1 一致率を調べる" and "結果": at each draft position the W4A4 (draft) and W4A16 (target) modes
+ * each have a most likely token and a probability for it (their own top-1; the two may differ).
+ * The article reports how often the two tokens agree, each mode's mean top-1 probability, and the
+ * agreement inside the region where both probabilities exceed 0.8 and where both are at most 0.8.
+ *     tgt_top1[b,i]   = argmax_j tgt_logits[b,i,j]     (i < gamma; lowest index among equal maxima)
+ *     draft_top1[b,i] = argmax_j draft_logits[b,i,j]
+ *     tgt_p1[b,i]     = 1 / sum_j exp(tgt_logits[b,i,j] - max_j tgt_logits[b,i,j])   (fp32 softmax)
+ *     draft_p1[b,i]   likewise for the draft row
+ *
+ *   tgt_logits   [B, gamma+1, V] bf16 (row gamma is not read);  draft_logits [B, gamma, V] bf16
+ *   tgt_top1, draft_top1 [B, gamma] int32 (outputs)
+ *   tgt_p1, draft_p1     [B, gamma] fp32 (outputs) or NULL
+ *   high                 threshold of the high-confidence region (the article uses 0.8); not NaN
+ *   tally                [8] fp64 or NULL: ACCUMULATED (added to, never cleared) over calls, so a
+ *                        decode loop can keep one running tally on the device:
+ *                        [0] positions, [1] agreeing positions, [2] positions with both p1 > high,
+ *                        [3] agreeing among [2], [4] positions with both p1 <= high, [5] agreeing
+ *                        among [4], [6] sum of tgt_p1, [7] sum of draft_p1.  Counts are exact; the
+ *                        sums are fp64 sums of the fp32 probabilities in an unspecified order.
+ *   ws, ws_bytes as for qspec_verify_greedy.  Same size limits.  Token ids are bit-exact;
+ *   probabilities carry the fp32 softmax's rounding (within 1e-5 absolute of the exact value).
+ */
+qspec_status qspec_verify_top1(const uint16_t* tgt_logits, const uint16_t* draft_logits, int32_t B,
+                               int32_t gamma, int32_t V, int32_t* tgt_top1, int32_t* draft_top1,
+                               float* tgt_p1, float* draft_p1, float high, double* tally, void* ws,
+                               size_t ws_bytes, qspec_stream_t stream);
 
 /*
  * qspec_verify_greedy_noalloc -- qspec_verify_greedy for callers that cannot allocate device memory.

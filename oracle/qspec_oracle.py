@@ -389,6 +389,53 @@ def verify_sample(tgt_bits, drf_bits, draft_tok, u_acc, u_res):
 
 
 # ----------------------------------------------------------------------------------------------
+# f2: top-1 statistics   [QSpec-article] sections "実験：W4A4 と W4A16 の Top-1 一致率を調べる", "結果"
+# ----------------------------------------------------------------------------------------------
+
+TOP1_TALLY = ("positions", "agree", "both_high", "agree_both_high", "both_low", "agree_both_low",
+              "sum_p1_target", "sum_p1_draft")
+
+
+def top1_stats(tgt_bits, drf_bits, high=0.8):
+    """Per draft position: each mode's most likely token and the probability that mode gives it.
+
+    tgt_bits: bf16 bits [B, gamma+1, V] (verify mode, only rows 0..gamma-1 are draft positions);
+    drf_bits: bf16 bits [B, gamma, V] (draft mode).  The article records, at every draft position,
+    the top-1 token of W4A4 and of W4A16 and each one's own top-1 probability (they may be different
+    tokens); it reports the agreement rate, the mean top-1 probability per mode, and the agreement
+    inside "both above the threshold" (p > high in both modes) and "both at or below it".
+    Returns (tgt_top1 int32 [B, gamma], draft_top1 int32 [B, gamma], tgt_p1 fp64, draft_p1 fp64,
+    tally fp64 [8] in the order of TOP1_TALLY).
+    """
+    Lt = bf16_to_f32(tgt_bits)
+    Ld = bf16_to_f32(drf_bits)
+    B, gamma, V = Ld.shape
+    t_tok = np.zeros((B, gamma), dtype=np.int32)
+    d_tok = np.zeros((B, gamma), dtype=np.int32)
+    t_p = np.zeros((B, gamma))
+    d_p = np.zeros((B, gamma))
+    tally = np.zeros(len(TOP1_TALLY))
+    for b in range(B):
+        for i in range(gamma):
+            t_tok[b, i] = first_argmax(Lt[b, i])
+            d_tok[b, i] = first_argmax(Ld[b, i])
+            t_p[b, i] = softmax(Lt[b, i])[t_tok[b, i]]
+            d_p[b, i] = softmax(Ld[b, i])[d_tok[b, i]]
+            agree = t_tok[b, i] == d_tok[b, i]
+            tally[0] += 1
+            tally[1] += agree
+            if t_p[b, i] > high and d_p[b, i] > high:
+                tally[2] += 1
+                tally[3] += agree
+            if t_p[b, i] <= high and d_p[b, i] <= high:
+                tally[4] += 1
+                tally[5] += agree
+            tally[6] += t_p[b, i]
+            tally[7] += d_p[b, i]
+    return t_tok, d_tok, t_p, d_p, tally
+
+
+# ----------------------------------------------------------------------------------------------
 # Expected tokens per target call    [SD-tutorial] "1回のtarget検証で何token進むか"
 # ----------------------------------------------------------------------------------------------
 

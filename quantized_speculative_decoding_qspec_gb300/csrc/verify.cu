@@ -51,14 +51,16 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Layout {
   Plan p1;            // pass-1 plan over B * (2 gamma + 1) rows (greedy uses B * (gamma + 1) rows)
   Plan pg;
+  Plan pt;            // top-1 statistics: B * 2 gamma rows
   int chunks2;
-  size_t err, cnt1, cnt2, seq_n, rowstat, part1, part2, total;
+  size_t err, cnt1, cnt2, seq_n, rowstat, part1, part2, part3, total;
 };
 
 Layout layout(int B, int gamma, int V) {
   Layout L;
   L.pg = plan_rows(int64_t(B) * (gamma + 1), V);
   L.p1 = plan_rows(int64_t(B) * (2 * gamma + 1), V);
+  L.pt = plan_rows(int64_t(B) * (2 * gamma), V);
   L.chunks2 = (V + kChunk2 - 1) / kChunk2;
   size_t off = 0;
   L.err = off;      off += 256;
@@ -70,6 +72,7 @@ Layout layout(int B, int gamma, int V) {
   const size_t part_s = sizeof(float2) * size_t(B) * (2 * gamma + 1) * L.p1.chunks;
   L.part1 = off;    off = align256(off + (part_g > part_s ? part_g : part_s));
   L.part2 = off;    off = align256(off + sizeof(float) * size_t(B) * L.chunks2);
+  L.part3 = off;    off = align256(off + sizeof(float4) * size_t(B) * (2 * gamma) * L.pt.chunks);
   L.total = off;
   return L;
 }
@@ -82,6 +85,7 @@ struct WS {
   float2* rowstat;
   float2* part1;
   float* part2;
+  float4* part3;
 };
 
 WS bind(void* base, const Layout& L) {
@@ -89,7 +93,7 @@ WS bind(void* base, const Layout& L) {
   return {reinterpret_cast<unsigned int*>(p + L.err), reinterpret_cast<unsigned int*>(p + L.cnt1),
           reinterpret_cast<unsigned int*>(p + L.cnt2), reinterpret_cast<int*>(p + L.seq_n),
           reinterpret_cast<float2*>(p + L.rowstat), reinterpret_cast<float2*>(p + L.part1),
-          reinterpret_cast<float*>(p + L.part2)};
+          reinterpret_cast<float*>(p + L.part2), reinterpret_cast<float4*>(p + L.part3)};
 }
 
 // ------------------------------------------------------------------ argmax (greedy)
@@ -617,6 +621,142 @@ __global__ void __launch_bounds__(kThreads) sample_pass2_kernel(
   }
 }
 
+// ------------------------------------------------------------------ top-1 statistics
+
+// Per draft position i < gamma of each sequence: the most likely token of the target (W4A16) row i
+// and of the draft (W4A4) row i, and the probability each row gives its own most likely token,
+// softmax max = 1 / sum_j exp(l_j - max).  One pass per (row, chunk): argmax and online (max, sum);
+// the last CTA of a sequence merges the chunks.  Rows [0, B gamma) are target rows, then draft rows.
+// One read of logits [beg, end): argmax (lowest index on ties) and the running (max, sum exp).
+template <bool kVec>
+__device__ __forceinline__ void scan_top1(const uint16_t* __restrict__ rp, int beg, int end, float& bv, int& bi,
+                                          MS& a) {
+  if (kVec) {
+    const int nv = (end - beg) >> 3;
+    const uint4* vp = reinterpret_cast<const uint4*>(rp + beg);
+    for (int v0 = threadIdx.x; v0 < nv; v0 += kUnroll * kThreads) {
+      uint4 u[kUnroll];
+#pragma unroll
+      for (int t = 0; t < kUnroll; ++t) {
+        const int v = v0 + t * kThreads;
+        u[t] = v < nv ? ld_stream_v4(vp + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int t = 0; t < kUnroll; ++t) {
+        const int v = v0 + t * kThreads;
+        if (v < nv) {
+          const int i0 = beg + 8 * v;
+          const uint32_t w[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) { f[2 * e] = bf16_lo(w[e]); f[2 * e + 1] = bf16_hi(w[e]); }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) argmax_take(bv, bi, f[e], i0 + e);
+          ms_add8(a, f);
+        }
+      }
+    }
+  } else {
+    for (int i = beg + threadIdx.x; i < end; i += kThreads) {
+      float f[8];
+      f[0] = bf16_lo(rp[i]);
+#pragma unroll
+      for (int e = 1; e < 8; ++e) f[e] = -INFINITY;
+      argmax_take(bv, bi, f[0], i);
+      ms_add8(a, f);
+    }
+  }
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) top1_kernel(const uint16_t* __restrict__ Lt,
+                                                        const uint16_t* __restrict__ Ld, int B, int gamma,
+                                                        int V, Plan plan, WS ws, int32_t* __restrict__ tgt_top1,
+                                                        int32_t* __restrict__ draft_top1,
+                                                        float* __restrict__ tgt_p1, float* __restrict__ draft_p1,
+                                                        float high, double* __restrict__ tally) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t row = blockIdx.x / plan.chunks;
+  const int c = blockIdx.x % plan.chunks;
+  const int64_t n_tgt = int64_t(B) * gamma;
+  const bool is_tgt = row < n_tgt;
+  const int64_t rr = is_tgt ? row : row - n_tgt;  // (b, i) = (rr / gamma, rr % gamma)
+  const int b = static_cast<int>(rr / gamma), i = static_cast<int>(rr % gamma);
+  const uint16_t* rp = is_tgt ? Lt + (int64_t(b) * (gamma + 1) + i) * V : Ld + rr * V;
+  const int beg = c * plan.chunk_len;
+  const int end = min(V, beg + plan.chunk_len);
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  MS a{-INFINITY, 0.0f};
+  scan_top1<kVec>(rp, beg, end, bv, bi, a);
+  block_argmax(bv, bi);
+  a = block_ms(a);
+
+  __shared__ bool s_last;
+  if (threadIdx.x == 0) {
+    ws.part3[row * plan.chunks + c] = make_float4(bv, __int_as_float(bi), a.m, a.s);
+    __threadfence();
+    const unsigned int prev = atomicAdd(ws.cnt1 + b, 1u);
+    s_last = prev == static_cast<unsigned int>(2 * gamma * plan.chunks - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  __shared__ int s_tok[2 * QSPEC_MAX_GAMMA];
+  __shared__ float s_p1[2 * QSPEC_MAX_GAMMA];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int k = warp; k < 2 * gamma; k += kThreads / 32) {
+    const int64_t r = k < gamma ? int64_t(b) * gamma + k : n_tgt + int64_t(b) * gamma + (k - gamma);
+    float v = -INFINITY;
+    int idx = INT_MAX;
+    MS t{-INFINITY, 0.0f};
+    for (int cc = lane; cc < plan.chunks; cc += 32) {
+      const float4 pp = __ldcg(ws.part3 + r * plan.chunks + cc);
+      argmax_take(v, idx, pp.x, __float_as_int(pp.y));
+      t = ms_merge(t, MS{pp.z, pp.w});
+    }
+    warp_argmax(v, idx);
+    t = warp_ms(t);
+    if (lane == 0) {
+      // the top-1 token's own term is exp(max - max) = 1
+      const float p1 = t.s > 0.0f ? __fdiv_rn(1.0f, t.s) : 0.0f;
+      s_tok[k] = idx;
+      s_p1[k] = p1;
+      const int64_t o = int64_t(b) * gamma + (k < gamma ? k : k - gamma);
+      if (k < gamma) {
+        tgt_top1[o] = idx;
+        if (tgt_p1) tgt_p1[o] = p1;
+      } else {
+        draft_top1[o] = idx;
+        if (draft_p1) draft_p1[o] = p1;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (tally) {
+      // positions, agree, both > high, agreeing among them, both <= high, agreeing among them,
+      // sum of target top-1 probabilities, sum of draft top-1 probabilities
+      double t[8] = {};
+      for (int k = 0; k < gamma; ++k) {
+        const bool agree = s_tok[k] == s_tok[gamma + k];
+        const float pt = s_p1[k], pd = s_p1[gamma + k];
+        t[0] += 1.0;
+        t[1] += agree;
+        if (pt > high && pd > high) { t[2] += 1.0; t[3] += agree; }
+        if (pt <= high && pd <= high) { t[4] += 1.0; t[5] += agree; }
+        t[6] += pt;
+        t[7] += pd;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) atomicAdd(tally + e, t[e]);
+    }
+    ws.cnt1[b] = 0;
+  }
+}
+
 qspec_status check_verify_args(const void* tgt, const int32_t* d, int B, int gamma, int V,
                                const int32_t* accept_len, const int32_t* out_tok, void* ws,
                                size_t ws_bytes) {
@@ -710,6 +850,32 @@ extern "C" qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const ui
     e = cudaLaunchKernelEx(&cfg, sample_pass2_kernel<false>, tgt_logits, draft_logits, u_resample, int(B),
                            int(gamma), int(V), L.chunks2, w, out_tok);
   return e == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
+}
+
+extern "C" qspec_status qspec_verify_top1(const uint16_t* tgt_logits, const uint16_t* draft_logits, int32_t B,
+                                          int32_t gamma, int32_t V, int32_t* tgt_top1, int32_t* draft_top1,
+                                          float* tgt_p1, float* draft_p1, float high, double* tally,
+                                          void* ws, size_t ws_bytes, qspec_stream_t stream) {
+  if (!tgt_logits || !draft_logits || !tgt_top1 || !draft_top1) return QSPEC_ERR_INVALID_ARG;
+  if (B <= 0 || gamma <= 0 || V <= 0) return QSPEC_ERR_INVALID_ARG;
+  if (gamma > QSPEC_MAX_GAMMA || V < 2 || V > QSPEC_MAX_V ||
+      int64_t(B) * (2 * gamma + 1) * int64_t(V) >= (int64_t(1) << 40))
+    return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(tgt_logits) || !aligned16(draft_logits) || !aligned16(tgt_top1) || !aligned16(draft_top1) ||
+      (tgt_p1 && !aligned16(tgt_p1)) || (draft_p1 && !aligned16(draft_p1)) || (tally && !aligned16(tally)))
+    return QSPEC_ERR_MISALIGNED;
+  if (!(high == high)) return QSPEC_ERR_INVALID_ARG;
+  if (!ws || !aligned16(ws)) return ws ? QSPEC_ERR_MISALIGNED : QSPEC_ERR_WORKSPACE;
+  const Layout L = layout(B, gamma, V);
+  if (ws_bytes < L.total) return QSPEC_ERR_WORKSPACE;
+  const WS w = bind(ws, L);
+  const int64_t blocks = int64_t(B) * (2 * gamma) * L.pt.chunks;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (V % 8 == 0)
+    return launch_pdl(top1_kernel<true>, dim3(unsigned(blocks)), dim3(kThreads), 0, s, tgt_logits, draft_logits,
+                      int(B), int(gamma), int(V), L.pt, w, tgt_top1, draft_top1, tgt_p1, draft_p1, high, tally);
+  return launch_pdl(top1_kernel<false>, dim3(unsigned(blocks)), dim3(kThreads), 0, s, tgt_logits, draft_logits,
+                    int(B), int(gamma), int(V), L.pt, w, tgt_top1, draft_top1, tgt_p1, draft_p1, high, tally);
 }
 
 // ------------------------------------------------------------------ allocation-free greedy verify

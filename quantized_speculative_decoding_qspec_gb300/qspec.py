@@ -37,6 +37,8 @@ SIGNATURES = {
     "qspec_verify_greedy": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qspec_verify_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                            ctypes.c_size_t, _P]),
+    "qspec_verify_top1": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                         ctypes.c_size_t, _P]),
     "qspec_verify_greedy_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
     "qspec_check_status": (ctypes.c_int, [_P, _P]),
     "qspec_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -185,6 +187,23 @@ def qspec_verify_sample(tgt_logits, draft_logits, draft_tok, u_accept, u_resampl
                                       _ptr(u_resample), B, G1 - 1, V, _ptr(accept_len), _ptr(out_tok),
                                       _ptr(accept_prob), _ptr(p_tok), _ptr(q_tok), _ptr(ws), ws.numel(),
                                       _stream(stream)))
+
+
+def qspec_verify_top1(tgt_logits, draft_logits, tgt_top1, draft_top1, ws, tgt_p1=None, draft_p1=None,
+                      high=0.8, tally=None, stream=None):
+    """Each mode's top-1 token and top-1 probability at every draft position; optional running tally
+    (fp64 [8], accumulated: positions, agree, both>high, agree there, both<=high, agree there, sums of p1)."""
+    _dt(tgt_logits, torch.bfloat16, "tgt_logits"); _dt(draft_logits, torch.bfloat16, "draft_logits")
+    _dt(tgt_top1, torch.int32, "tgt_top1"); _dt(draft_top1, torch.int32, "draft_top1")
+    _dt(tgt_p1, torch.float32, "tgt_p1"); _dt(draft_p1, torch.float32, "draft_p1")
+    _dt(tally, torch.float64, "tally"); _dt(ws, torch.uint8, "ws")
+    if tally is not None and tally.numel() < 8:
+        raise ValueError("tally needs 8 fp64 entries")
+    B, G1, V = tgt_logits.shape
+    _check("qspec_verify_top1",
+           load().qspec_verify_top1(_ptr(tgt_logits), _ptr(draft_logits), B, G1 - 1, V, _ptr(tgt_top1),
+                                    _ptr(draft_top1), _ptr(tgt_p1), _ptr(draft_p1), float(high), _ptr(tally),
+                                    _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def qspec_check_status(ws=None, stream=None):

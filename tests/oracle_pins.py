@@ -465,10 +465,57 @@ def check_sampling_from_logits(o):
     assert same["accept_len"][0] == 1 and same["accept_prob"][0, 0] == 1.0
 
 
+# ---------------------------------------------------------------- f2: top-1 statistics
+
+def check_top1_closed_forms(o):
+    # one spike of height a over V-1 zeros: p1 = e^a / (e^a + V - 1); equal logits: p1 = 1/V at index 0;
+    # a two-way tie [1, 1, 0]: the lower index, p1 = e / (2e + 1)
+    V = 5
+    tgt = np.zeros((1, 4, V), dtype=np.float32)
+    drf = np.zeros((1, 3, V), dtype=np.float32)
+    tgt[0, 0, 3] = 2.0
+    drf[0, 0, 1] = 2.0                    # the draft's own top-1 is another token
+    tgt[0, 2, [1, 4]] = 1.0
+    drf[0, 2, [2, 3]] = -1.0              # draft top-1 = index 0 among three zeros: p1 = 1/(3 + 2/e)
+    tgt[0, 3, :] = 9.0                    # row gamma is not a draft position
+    tt, dt, tp, dp, _ = o.top1_stats(bf16_bits(tgt), bf16_bits(drf))
+    e = np.e
+    assert tt.tolist() == [[3, 0, 1]] and dt.tolist() == [[1, 0, 0]]
+    assert abs(tp[0, 0] - e ** 2 / (e ** 2 + 4)) < 1e-12 and abs(dp[0, 0] - e ** 2 / (e ** 2 + 4)) < 1e-12
+    assert abs(tp[0, 1] - 0.2) < 1e-12 and abs(dp[0, 1] - 0.2) < 1e-12
+    assert abs(tp[0, 2] - e / (2 * e + 3)) < 1e-12
+    assert abs(dp[0, 2] - 1.0 / (3 + 2 / e)) < 1e-12
+
+
+def check_top1_tally(o):
+    # positions: (agree, both high), (disagree, both low), (agree, one high one low),
+    # (agree, both low), (disagree, both high)
+    def row(top, big, V=4):
+        r = np.zeros(V, dtype=np.float32)
+        r[top] = big
+        return r
+    hi, lo = 8.0, 0.5                     # p1 = e^8/(e^8+3) > 0.9;  p1 = e^.5/(e^.5+3) < 0.5
+    half = np.array([1.0, 1.0], dtype=np.float32)
+    tgt = np.stack([row(0, hi), row(1, lo), row(2, hi), row(3, lo), row(0, hi)])
+    drf = np.stack([row(0, hi), row(2, lo), row(2, lo), row(3, lo), row(1, hi)])
+    tgt = np.concatenate([tgt, np.zeros((1, 4), np.float32)])[None]
+    drf = drf[None]
+    _, _, tp, dp, tally = o.top1_stats(bf16_bits(tgt), bf16_bits(drf), high=0.9)
+    assert tally[:6].tolist() == [5, 3, 2, 1, 2, 1]
+    assert abs(tally[6] - tp.sum()) < 1e-12 and abs(tally[7] - dp.sum()) < 1e-12
+    assert abs(tally[6] - (3 * np.exp(8) / (np.exp(8) + 3) + 2 * np.exp(.5) / (np.exp(.5) + 3))) < 1e-12
+    # threshold strictness: two equal logits give exactly 1/2, which is "at or below 0.5"
+    t2 = np.stack([half, half])[None]
+    _, _, tp2, dp2, tally2 = o.top1_stats(bf16_bits(t2), bf16_bits(half[None, None]), high=0.5)
+    assert tp2[0, 0] == 0.5 and dp2[0, 0] == 0.5
+    assert tally2[:6].tolist() == [1, 1, 0, 0, 1, 1]
+
+
 ALL_FAST = [
     check_pack_layout, check_weight_grid_roundtrip, check_weight_hand_cases, check_pack_end_to_end,
     check_w4a16_onehot_and_grid, check_w4a16_error_bound, check_act_quant_hand_cases,
     check_w4a4_bruteforce, check_w4a4_extremes, check_w4a4_constant_activation, check_softmax,
     check_greedy_tutorial_example, check_greedy_bruteforce, check_greedy_ties,
     check_greedy_equivalence, check_sampling_worked_example, check_sampling_from_logits,
+    check_top1_closed_forms, check_top1_tally,
 ]

@@ -40,6 +40,12 @@ MUTATIONS = [
     ("acceptance ratio inverted", "min(1.0, p_tok[i] / q_tok[i])", "min(1.0, q_tok[i] / p_tok[i])"),
     ("resample uniform not indexed by n", "j = inverse_cdf(r, float(u_res[n]))", "j = inverse_cdf(r, float(u_res[0]))"),
     ("inverse cdf non-strict", "hit = np.nonzero(c > u * R)[0]", "hit = np.nonzero(c >= u * R)[0]"),
+    ("top-1 probability of the draft taken at the target's token", "d_p[b, i] = softmax(Ld[b, i])[d_tok[b, i]]",
+     "d_p[b, i] = softmax(Ld[b, i])[t_tok[b, i]]"),
+    ("high-confidence test not strict", "if t_p[b, i] > high and d_p[b, i] > high:",
+     "if t_p[b, i] >= high and d_p[b, i] >= high:"),
+    ("low region counts either mode at or below", "if t_p[b, i] <= high and d_p[b, i] <= high:",
+     "if t_p[b, i] <= high or d_p[b, i] <= high:"),
     ("E[T] exponent off by one", "return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)",
      "return (1.0 - alpha ** gamma) / (1.0 - alpha)"),
 ]

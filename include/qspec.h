@@ -237,11 +237,43 @@ qspec_status qspec_verify_greedy_noalloc(const uint16_t* tgt_logits, const int32
                                          int32_t* out_tok, int32_t* tgt_argmax, qspec_stream_t stream);
 
 /*
+ * qspec_gather_rows -- dst[m, :] = src[idx[m], :] for m < n (step f1: embedding lookup of the tokens
+ * a decode step feeds the model, and reordering of logits rows between [gamma, B] and [B, gamma]).
+ *
+ * Tutorial "Speculative Decodingとは？LLM生成を速くする方法", section "draft modelとtarget modelの
+ * 処理フロー": each draft step feeds the token just chosen back into the model.
+ *   src  [n_src, row_bytes] device;  idx [n] int32 device;  dst [n, row_bytes] device (no overlap
+ *   with src).  row_bytes a multiple of 4; src, dst and idx 4-byte aligned, and src and dst 16-byte
+ *   aligned when row_bytes is a multiple of 16 and at least 1024 (one CTA per row, 16-byte copies;
+ *   shorter rows such as token ids take one thread per row); n <= 2^31 - 1.
+ *   An id outside [0, n_src) writes a zero row and makes the next qspec_check_status return
+ *   QSPEC_ERR_INVALID_ARG.
+ */
+qspec_status qspec_gather_rows(const void* src, int64_t n_src, int64_t row_bytes, const int32_t* idx,
+                               int64_t n, void* dst, qspec_stream_t stream);
+
+/*
+ * qspec_select_tokens -- the next token of each of R logits rows (step f1: how a draft step, or a
+ * plain target-only decode step, picks its token).
+ *
+ * Same section: the draft proposes its most likely token when decoding greedily and a draw from its
+ * distribution q when sampling (temperature 1, fp32 softmax, inverse CDF in index order as in the
+ * sampling verify):
+ *     u == NULL:  tok[r] = argmax_j logits[r, j]    (lowest index among equal maxima; bit-exact)
+ *     otherwise:  tok[r] = smallest j with sum_{i<=j} exp(l_i - m) > u[r] * sum_i exp(l_i - m)
+ *                 (m = max_j l_j; if rounding leaves no such j, the last j with a nonzero term)
+ *   logits [R, V] bf16 (16-byte aligned);  u [R] fp32 in [0,1) or NULL;  tok [R] int32 (output);
+ *   u and tok 4-byte aligned.  One CTA per row.  2 <= V <= 2^24.  A row of only -inf gives token 0.
+ */
+qspec_status qspec_select_tokens(const uint16_t* logits, int32_t R, int32_t V, const float* u, int32_t* tok,
+                                 qspec_stream_t stream);
+
+/*
  * qspec_check_status -- synchronises `stream`, then reports (and clears) the error words that the
  * kernels set on the device: the verify workspace's word when `ws` is not NULL, and the library's
- * own word for the linear kernels of the current device.  QSPEC_ERR_TIMEOUT if a kernel gave up a
- * bounded wait, QSPEC_ERR_INVALID_ARG if a draft token id was out of range, QSPEC_ERR_CUDA if the
- * stream reported an error, QSPEC_OK otherwise.
+ * own words for the linear and decode-loop kernels of the current device.  QSPEC_ERR_TIMEOUT if a
+ * kernel gave up a bounded wait, QSPEC_ERR_INVALID_ARG if a draft token id or a gather id was out of
+ * range, QSPEC_ERR_CUDA if the stream reported an error, QSPEC_OK otherwise.
  */
 qspec_status qspec_check_status(void* ws, qspec_stream_t stream);
 

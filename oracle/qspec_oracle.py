@@ -389,6 +389,74 @@ def verify_sample(tgt_bits, drf_bits, draft_tok, u_acc, u_res):
 
 
 # ----------------------------------------------------------------------------------------------
+# f1: the decode loop     [SD-tutorial] "draft modelとtarget modelの処理フロー"
+# ----------------------------------------------------------------------------------------------
+
+
+def select_token(logits_bits, u=None) -> int:
+    """A model's next token from its bf16 logits row: the most likely token when decoding greedily
+    (u is None), else the inverse-CDF draw from softmax(logits) with uniform u."""
+    l = bf16_to_f32(logits_bits).astype(np.float64)
+    if u is None:
+        return first_argmax(l)
+    return inverse_cdf(softmax(l), float(u))
+
+
+def toy_forward(E_bits, layers, tok, draft_mode):
+    """Logits of a stack of linears on the shared packed weights, for one input token per row.
+
+    x = E[tok] (bf16 embedding rows); then for each (Wp, S) in order, x = bf16(linear(x)) with the
+    draft-mode (W4A4) or verify-mode (W4A16) linear; the last layer's output are the bf16 logits.
+    Returns bf16 bits [len(tok), N_last].
+    """
+    x = np.asarray(E_bits)[np.asarray(tok, dtype=np.int64)]
+    for Wp, S in layers:
+        y = linear_w4a4(x, Wp, S)["y"] if draft_mode else linear_w4a16(x, Wp, S)
+        x = f64_to_bf16_bits(y)
+    return x
+
+
+def speculative_decode(target, draft, prefix, n_iter, gamma, u_draft=None, u_acc=None, u_res=None):
+    """The classic draft-then-verify loop for one sequence, n_iter iterations.
+
+    target(seq) / draft(seq) return the bf16 logits row of the token that follows seq.  Each
+    iteration: the draft model extends its own copy of the sequence one token at a time, gamma times
+    (select_token with u_draft[it][i], greedy when u_draft is None); the target scores the gamma
+    draft positions and the one after them; verify_greedy (u_acc is None) or verify_sample decides
+    how many drafts stand and which token follows them; those n + 1 tokens are appended.
+    Returns (generated tokens, accept lengths n per iteration).
+    """
+    seq = [int(t) for t in prefix]
+    start = len(seq)
+    ns = []
+    for it in range(n_iter):
+        d, dl = [], []
+        for i in range(gamma):
+            l = draft(seq + d)
+            dl.append(l)
+            d.append(select_token(l, None if u_draft is None else u_draft[it][i]))
+        tl = np.stack([target(seq + d[:i]) for i in range(gamma + 1)])[None]
+        dt = np.array([d], dtype=np.int32)
+        if u_acc is None:
+            n, out, _ = verify_greedy(tl, dt)
+            n, out = int(n[0]), out[0]
+        else:
+            r = verify_sample(tl, np.stack(dl)[None], dt, np.asarray(u_acc[it])[None], np.asarray(u_res[it])[None])
+            n, out = int(r["accept_len"][0]), r["out_tok"][0]
+        seq += [int(t) for t in out[:n + 1]]
+        ns.append(n)
+    return seq[start:], ns
+
+
+def target_only_decode(target, prefix, n_new, u=None):
+    """Plain decoding with the target alone: one target call per token (greedy when u is None)."""
+    seq = [int(t) for t in prefix]
+    for k in range(n_new):
+        seq.append(select_token(target(seq), None if u is None else u[k]))
+    return seq[len(prefix):]
+
+
+# ----------------------------------------------------------------------------------------------
 # f2: top-1 statistics   [QSpec-article] sections "実験：W4A4 と W4A16 の Top-1 一致率を調べる", "結果"
 # ----------------------------------------------------------------------------------------------
 

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqspec.so")
 
-UNITS = ["pack.cu", "linear.cu", "linear_tc.cu", "gemv.cu", "verify.cu", "api.cu"]
+UNITS = ["pack.cu", "linear.cu", "linear_tc.cu", "gemv.cu", "verify.cu", "decode.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

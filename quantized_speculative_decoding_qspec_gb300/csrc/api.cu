@@ -4,6 +4,7 @@
 
 namespace qspec {
 unsigned int* verify_error_word(void* ws);
+qspec_status read_and_clear_decode_error(cudaStream_t s, unsigned int* bits);
 }
 
 extern "C" const char* qspec_status_string(qspec_status status) {
@@ -24,7 +25,9 @@ extern "C" qspec_status qspec_check_status(void* ws, qspec_stream_t stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return QSPEC_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return QSPEC_ERR_CUDA;
   unsigned int lin = 0, ver = 0;
+  unsigned int dec = 0;
   if (qspec::read_and_clear_linear_error(s, &lin) != QSPEC_OK) return QSPEC_ERR_CUDA;
+  if (qspec::read_and_clear_decode_error(s, &dec) != QSPEC_OK) return QSPEC_ERR_CUDA;
   if (ws) {
     unsigned int* w = qspec::verify_error_word(ws);
     if (cudaMemcpyAsync(&ver, w, sizeof(ver), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
@@ -35,6 +38,6 @@ extern "C" qspec_status qspec_check_status(void* ws, qspec_stream_t stream) {
       return QSPEC_ERR_CUDA;
   }
   if (lin & 1u) return QSPEC_ERR_TIMEOUT;
-  if (ver & 2u) return QSPEC_ERR_INVALID_ARG;
+  if ((ver & 2u) || (dec & 4u)) return QSPEC_ERR_INVALID_ARG;
   return QSPEC_OK;
 }

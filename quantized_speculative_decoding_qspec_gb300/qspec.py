@@ -40,6 +40,8 @@ SIGNATURES = {
     "qspec_verify_top1": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_float, _P, _P,
                                          ctypes.c_size_t, _P]),
     "qspec_verify_greedy_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "qspec_gather_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _P, _P]),
+    "qspec_select_tokens": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
     "qspec_check_status": (ctypes.c_int, [_P, _P]),
     "qspec_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -204,6 +206,26 @@ def qspec_verify_top1(tgt_logits, draft_logits, tgt_top1, draft_top1, ws, tgt_p1
            load().qspec_verify_top1(_ptr(tgt_logits), _ptr(draft_logits), B, G1 - 1, V, _ptr(tgt_top1),
                                     _ptr(draft_top1), _ptr(tgt_p1), _ptr(draft_p1), float(high), _ptr(tally),
                                     _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def qspec_gather_rows(src, idx, dst, stream=None):
+    """dst[m] = src[idx[m]] over the leading dimension (rows of src.numel() / src.shape[0] elements)."""
+    _dt(idx, torch.int32, "idx")
+    if src.dtype != dst.dtype:
+        raise TypeError("src and dst must have the same dtype")
+    n_src, n = src.shape[0], idx.numel()
+    row_bytes = src[0].numel() * src.element_size()
+    if dst.shape[0] != n or dst[0].numel() * dst.element_size() != row_bytes:
+        raise ValueError("dst must be [len(idx), row of src]")
+    _check("qspec_gather_rows", load().qspec_gather_rows(_ptr(src), n_src, row_bytes, _ptr(idx), n, _ptr(dst),
+                                                         _stream(stream)))
+
+
+def qspec_select_tokens(logits, tok, u=None, stream=None):
+    """Next token per row of bf16 logits [R, V]: argmax when u is None, else an inverse-CDF draw with u [R]."""
+    _dt(logits, torch.bfloat16, "logits"); _dt(tok, torch.int32, "tok"); _dt(u, torch.float32, "u")
+    R, V = logits.shape
+    _check("qspec_select_tokens", load().qspec_select_tokens(_ptr(logits), R, V, _ptr(u), _ptr(tok), _stream(stream)))
 
 
 def qspec_check_status(ws=None, stream=None):

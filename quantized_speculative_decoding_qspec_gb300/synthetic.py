@@ -16,7 +16,8 @@ Distributions (the workloads of the QSpec top-1 agreement article, "QSpecå®Ÿè¡Œæ
   token) scaled by 20;
 * target logits: N(0, 1) plus a U(4, 12) spike on one uniformly chosen token per row;
 * draft logits: target logits plus N(0, sigma) on every element;
-* uniforms: ``integers(0, 2**24) * 2**-24``, exact fp32 values in [0, 1).
+* uniforms: ``integers(0, 2**24) * 2**-24``, exact fp32 values in [0, 1);
+* the decode loop's toy model: an N(0, 1) token embedding table and N(0, 0.02) weights per linear.
 """
 from __future__ import annotations
 
@@ -33,6 +34,8 @@ STREAM_DRAFT_NOISE = 7
 STREAM_DRAFT_SAMPLE = 8
 STREAM_U_ACCEPT = 9
 STREAM_U_RESAMPLE = 10
+STREAM_EMBEDDINGS = 11
+STREAM_U_DRAFT = 12
 
 
 def rng(workload_id: int, stream_id: int, sub: int = 0) -> np.random.Generator:
@@ -74,6 +77,15 @@ def weights(N: int, K: int, workload_id: int = 0, layer: int = 0, std: float = 0
     w = g.standard_normal((N, K), dtype=np.float32)
     w *= np.float32(std)
     return f32_to_bf16_bits(w)
+
+
+def embeddings(V: int, D: int, workload_id: int = 0, std: float = 1.0) -> np.ndarray:
+    """bf16 bits of a [V, D] token embedding table, N(0, std)."""
+    g = rng(workload_id, STREAM_EMBEDDINGS)
+    e = g.standard_normal((V, D), dtype=np.float32)
+    if std != 1.0:
+        e *= np.float32(std)
+    return f32_to_bf16_bits(e)
 
 
 def outlier_channels(K: int, workload_id: int = 0, frac: float = 0.01) -> np.ndarray:

@@ -465,6 +465,90 @@ def check_sampling_from_logits(o):
     assert same["accept_len"][0] == 1 and same["accept_prob"][0, 0] == 1.0
 
 
+# ---------------------------------------------------------------- f1: decode loop
+
+def _bits(l):
+    return ((np.asarray(l, np.float32).view(np.uint32) + np.uint32(0x8000)) >> np.uint32(16)).astype(np.uint16)
+
+
+def check_select_token(o):
+    # greedy: lowest index among equal maxima; sampling: inverse CDF of softmax, strict '>'
+    assert o.select_token(bf16_bits([1.0, 3.0, 3.0, -2.0])) == 1
+    l = np.log(np.array([0.25, 0.5, 0.25]))     # bf16 rounding keeps the two 0.25 equal
+    b = _bits(l)
+    p = o.softmax(o.bf16_to_f32(b).astype(np.float64))
+    assert abs(p[0] - p[2]) == 0.0
+    for u, want in ((0.0, 0), (p[0] - 1e-9, 0), (p[0] + 1e-9, 1), (p[0] + p[1] + 1e-9, 2), (1 - 2 ** -24, 2)):
+        assert o.select_token(b, u) == want, (u, want)
+    assert o.select_token(bf16_bits([-np.inf, 5.0, -np.inf]), 0.999) == 1
+
+
+def check_toy_forward_onehot(o):
+    # one-hot weight rows quantise to code 7 with s = fp16(1/7): each layer maps x_v to x_v * 7 s
+    # (verify mode), rounded to bf16; in draft mode x_v becomes s_a * qa_v * 7 s.
+    D, V = 128, 128
+    rng = np.random.default_rng(5)
+    E = bf16_bits(o.bf16_to_f32(_bits(rng.standard_normal((6, D)))))
+    W = np.zeros((V, D), dtype=np.float32)
+    perm = rng.permutation(D)
+    W[np.arange(V), perm] = 1.0
+    Wp, S = o.pack_weights(bf16_bits(W))
+    s = float(np.float16(1.0 / 7.0))
+    tok = [3, 0, 5]
+    x = o.bf16_to_f32(E[tok]).astype(np.float64)
+    want = o.f64_to_bf16_bits(x[:, perm] * 7 * s)
+    assert np.array_equal(o.toy_forward(E, [(Wp, S)], tok, False), want)
+    qa, s_a = o.quantize_activations(E[tok])
+    want4 = o.f64_to_bf16_bits(s_a.astype(np.float64)[:, None] * qa[:, perm].astype(np.float64) * 7 * s)
+    assert np.array_equal(o.toy_forward(E, [(Wp, S)], tok, True), want4)
+    # two layers apply in order: the second permutation acts on the first layer's output
+    perm2 = rng.permutation(D)
+    W2 = np.zeros((V, D), dtype=np.float32)
+    W2[np.arange(V), perm2] = 1.0
+    Wp2, S2 = o.pack_weights(bf16_bits(W2))
+    y1 = o.bf16_to_f32(want).astype(np.float64)
+    want2 = o.f64_to_bf16_bits(y1[:, perm2] * 7 * s)
+    assert np.array_equal(o.toy_forward(E, [(Wp, S), (Wp2, S2)], tok, False), want2)
+
+
+def check_decode_loop_greedy(o):
+    # greedy speculative decoding emits exactly what target-only greedy decoding emits; a draft equal
+    # to the target has every draft accepted (gamma + 1 tokens per iteration)
+    V, gamma, n_iter = 40, 3, 12
+    def target(seq):
+        return _bits(_toy_logits(seq, V, 0))
+    def draft(seq):
+        return _bits(_toy_logits(seq, V, 0) + 0.8 * _toy_logits(seq, V, 1))
+    gen, ns = o.speculative_decode(target, draft, [7], n_iter, gamma)
+    assert len(gen) == sum(ns) + n_iter
+    assert gen == o.target_only_decode(target, [7], len(gen))
+    assert 0 < sum(ns) < gamma * n_iter
+    gen2, ns2 = o.speculative_decode(target, target, [7], 4, gamma)
+    assert ns2 == [gamma] * 4 and gen2 == o.target_only_decode(target, [7], 4 * (gamma + 1))
+
+
+def check_decode_loop_sampling_marginal(o, trials=3000):
+    # speculative sampling leaves the target's distribution of the next token unchanged: the first
+    # generated token is distributed as softmax(target(prefix)), whatever the draft
+    V, gamma = 3, 2
+    lt = np.array([0.0, 1.0, -0.5], dtype=np.float32)
+    ld = np.array([1.0, -1.0, 0.5], dtype=np.float32)
+    def target(seq):
+        return _bits(lt + 0.3 * (len(seq) % 2))
+    def draft(seq):
+        return _bits(ld)
+    p = o.softmax(o.bf16_to_f32(target([0])).astype(np.float64))
+    rng = np.random.default_rng(11)
+    counts = np.zeros(V)
+    for t in range(trials):
+        u = rng.random((1, 3 * gamma + 1))
+        gen, _ = o.speculative_decode(target, draft, [0], 1, gamma, u_draft=[u[0, :gamma]],
+                                      u_acc=[u[0, gamma:2 * gamma]], u_res=[u[0, 2 * gamma:]])
+        counts[gen[0]] += 1
+    se = np.sqrt(p * (1 - p) / trials)
+    assert np.all(np.abs(counts / trials - p) < 5 * se), (counts / trials, p)
+
+
 # ---------------------------------------------------------------- f2: top-1 statistics
 
 def check_top1_closed_forms(o):
@@ -517,5 +601,6 @@ ALL_FAST = [
     check_w4a4_bruteforce, check_w4a4_extremes, check_w4a4_constant_activation, check_softmax,
     check_greedy_tutorial_example, check_greedy_bruteforce, check_greedy_ties,
     check_greedy_equivalence, check_sampling_worked_example, check_sampling_from_logits,
-    check_top1_closed_forms, check_top1_tally,
+    check_top1_closed_forms, check_top1_tally, check_select_token, check_toy_forward_onehot,
+    check_decode_loop_greedy, check_decode_loop_sampling_marginal,
 ]

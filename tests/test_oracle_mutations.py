@@ -46,6 +46,13 @@ MUTATIONS = [
      "if t_p[b, i] >= high and d_p[b, i] >= high:"),
     ("low region counts either mode at or below", "if t_p[b, i] <= high and d_p[b, i] <= high:",
      "if t_p[b, i] <= high or d_p[b, i] <= high:"),
+    ("decode loop drops the token after the accepted drafts", "seq += [int(t) for t in out[:n + 1]]",
+     "seq += [int(t) for t in out[:n]]"),
+    ("target scores each position one token late", "tl = np.stack([target(seq + d[:i]) for i in range(gamma + 1)])[None]",
+     "tl = np.stack([target(seq + d[:i + 1]) for i in range(gamma + 1)])[None]"),
+    ("draft does not see its own tokens", "l = draft(seq + d)", "l = draft(seq)"),
+    ("toy model runs verify mode when drafting", 'y = linear_w4a4(x, Wp, S)["y"] if draft_mode else linear_w4a16(x, Wp, S)',
+     "y = linear_w4a16(x, Wp, S)"),
     ("E[T] exponent off by one", "return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)",
      "return (1.0 - alpha ** gamma) / (1.0 - alpha)"),
 ]

@@ -752,8 +752,50 @@ def sweep_sampling(quick=False):
                           flush=True)
 
 
+def decode_report(args):
+    """The decode loop on a one-block toy model with Llama-3-8B widths (D 4096, F 14336, V 128256):
+    gamma W4A4 draft passes, one W4A16 pass over gamma + 1 positions, verify, and top-1 statistics of
+    both modes; then target-only decoding for the speedup comparison.  One JSON line."""
+    import torch
+    import numpy as np
+    from quantized_speculative_decoding_qspec_gb300 import decode
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+    D, F, V = 4096, 14336, 128256
+    t0 = time.perf_counter()
+    model = decode.ToyModel(D, F, V, workload_id=21, device="cuda")
+    t_init = time.perf_counter() - t0
+    out = {"metric": "speculative decode loop on a toy model (tutorial measures)", "config": {
+        "workload": f"toy decoder: embedding [{V},{D}] bf16, packed linears [{F},{D}], [{D},{F}], [{V},{D}]; "
+                    f"B={args.decode_batch}, gamma={args.decode_gamma}, "
+                    f"{'sampling' if args.decode_sampling else 'greedy'}",
+        "weight_bytes_packed": model.weight_bytes(), "iterations": args.decode_iters}}
+    sd = decode.SpecDecoder(model, args.decode_batch, args.decode_gamma, sampling=args.decode_sampling)
+    first = np.arange(args.decode_batch, dtype=np.int32) * 1013 + 17
+    sd.run(first, 4, workload_id=22)                       # warm-up (graph capture)
+    spec = sd.run(first, args.decode_iters, workload_id=22)
+    n_tok = int(np.mean([len(g) for g in spec["generated"]]))
+    sd.run_target_only(first, 4, workload_id=22)
+    base = sd.run_target_only(first, n_tok, workload_id=22)
+    summ = decode.summarize(spec, base, args.decode_gamma)
+    if not args.decode_sampling:
+        m = min(len(g) for g in spec["generated"])
+        same_m = sd.run_target_only(first, m, workload_id=22, padded=True)
+        summ["output_equivalence_greedy"] = all(spec["generated"][b][:m] == same_m["generated"][b]
+                                                for b in range(args.decode_batch))
+    out.update({k: (round(v, 4) if isinstance(v, float) else v) for k, v in summ.items()})
+    out["init_s"] = round(t_init, 1)
+    q.qspec_check_status()
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--decode", action="store_true",
+                    help="run the speculative decode loop on a toy model and print its measures")
+    ap.add_argument("--decode-batch", type=int, default=1)
+    ap.add_argument("--decode-gamma", type=int, default=3)
+    ap.add_argument("--decode-iters", type=int, default=64)
+    ap.add_argument("--decode-sampling", action="store_true")
     ap.add_argument("--sweep", choices=["linear", "batched", "sampling", "sampling-quick"], default=None,
                     help="measurement sweeps instead of the step benchmark")
     ap.add_argument("--profile-case", default=None,
@@ -775,6 +817,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.profile_case:
         profile_case(args.profile_case, args.reps)
+        return
+    if args.decode:
+        decode_report(args)
         return
     if args.sweep == "linear":
         sweep_linear()

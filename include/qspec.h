@@ -84,8 +84,11 @@ qspec_status qspec_pack_weights(const uint16_t* W, int64_t N, int64_t K, uint8_t
  *   x  [M, K] bf16, Wp [N, K/2] uint8, S [N, K/128] fp16 (from qspec_pack_weights)
  *   y  [M, N] bf16 (output)
  *   ws, ws_bytes  device workspace, >= qspec_linear_workspace_size(M, N, K), zero-filled before its
- *                 first use (calls leave it ready for the next call); it holds the partial sums of
- *                 output tiles whose K range is split between SMs, and the W4A4 activation codes
+ *                 first use; it holds the per-tile tickets and partial sums of output tiles whose K
+ *                 range is split between SMs, and the W4A4 activation codes.  A call leaves the
+ *                 workspace ready for the next call OF THE SAME (M, N, K); its layout depends on the
+ *                 shape, so calls of different shapes (for instance the layers of a model) need
+ *                 workspaces of their own, or a zero-fill in between
  *   1 <= M <= 4096, N % 8 == 0, K % 128 == 0.
  * The fp32 summation order depends on the device's SM count, so results are reproducible on one
  * device but may differ in the last bits between devices.

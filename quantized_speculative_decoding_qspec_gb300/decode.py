@@ -58,10 +58,10 @@ class ToyModel:
     def _buffers(self, M: int):
         b = self._bufs.get(M)
         if b is None:
-            ws = max(q.qspec_linear_workspace_size(M, N, K) for N, K in self.shapes)
+            # one workspace per layer: a linear workspace stays ready only for calls of its own shape
             b = {"x": torch.empty(M, self.D, dtype=torch.bfloat16, device=self.device),
                  "h": [torch.empty(M, N, dtype=torch.bfloat16, device=self.device) for N, _ in self.shapes[:-1]],
-                 "ws": torch.zeros(ws, dtype=torch.uint8, device=self.device)}
+                 "ws": [q.new_linear_workspace(M, N, K, device=self.device) for N, K in self.shapes]}
             self._bufs[M] = b
         return b
 
@@ -74,7 +74,7 @@ class ToyModel:
         lin = q.qspec_linear_w4a4 if draft_mode else q.qspec_linear_w4a16
         for i, (Wp, S) in enumerate(self.layers):
             y = logits if i == len(self.layers) - 1 else b["h"][i]
-            lin(x, Wp, S, y, b["ws"])
+            lin(x, Wp, S, y, b["ws"][i])
             x = y
         return logits
 
@@ -113,12 +113,13 @@ class SpecDecoder:
         self.tp1 = torch.zeros(B, gamma, **f32)
         self.dp1 = torch.zeros(B, gamma, **f32)
         self.tally = torch.zeros(8, dtype=torch.float64, device=dev)
-        # target-only decoding (the baseline the speedup is measured against) at the same M as the
-        # verify pass, so that its logits are computed by the same kernel configuration
-        self.tt = torch.zeros(B * G1, **i32)
-        self.ttl = torch.empty(B * G1, V, dtype=torch.bfloat16, device=dev)
-        self.tsel = torch.zeros(B * G1, **i32)
-        self.u_t = torch.zeros(B * G1, **f32)
+        # target-only decoding, the baseline: at M = B (one token per sequence and step, for timing)
+        # and padded to the verify pass's M = B (gamma + 1), whose logits come from the same kernel
+        # configuration as the verify pass (for the output-equivalence check)
+        self.tgt = {}
+        for padded, M in ((False, B), (True, B * G1)):
+            self.tgt[padded] = {"tok": torch.zeros(M, **i32), "logits": torch.empty(M, V, dtype=torch.bfloat16, device=dev),
+                                "sel": torch.zeros(M, **i32), "u": torch.zeros(M, **f32)}
         # host staging (pinned)
         self.h_n = torch.zeros(B, dtype=torch.int32).pin_memory()
         self.h_out = torch.zeros(B, G1, dtype=torch.int32).pin_memory()
@@ -148,22 +149,26 @@ class SpecDecoder:
             q.qspec_verify_top1(self.tl, self.dlv, self.t1, self.d1, self.ws, tgt_p1=self.tp1, draft_p1=self.dp1,
                                 high=self.high, tally=self.tally)
 
-    def _target_phase(self):
-        self.model.forward(self.tt, self.ttl, draft_mode=False)
-        q.qspec_select_tokens(self.ttl, self.tsel, u=self.u_t if self.sampling else None)
+    def _target_phase(self, padded):
+        t = self.tgt[padded]
+        self.model.forward(t["tok"], t["logits"], draft_mode=False)
+        q.qspec_select_tokens(t["logits"], t["sel"], u=t["u"] if self.sampling else None)
+
+    def _phases(self):
+        return (self._draft_phase, self._verify_phase, lambda: self._target_phase(False),
+                lambda: self._target_phase(True))
 
     def _capture(self):
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):  # warm up (workspaces, lazy module loading) before capture
-            self._draft_phase()
-            self._verify_phase()
-            self._target_phase()
+            for fn in self._phases():
+                fn()
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         self.tally.zero_()
         graphs = []
-        for fn in (self._draft_phase, self._verify_phase, self._target_phase):
+        for fn in self._phases():
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 fn()
@@ -176,7 +181,7 @@ class SpecDecoder:
                 self._capture()
             self.graphs[k].replay()
         else:
-            (self._draft_phase, self._verify_phase, self._target_phase)[k]()
+            self._phases()[k]()
 
     # ---- host loop
     def run(self, first_tokens, n_iter: int, workload_id: int = 0, record: bool = False):
@@ -187,7 +192,7 @@ class SpecDecoder:
         if self.use_graphs and self.graphs is None:
             self._capture()
         self.tally.zero_()
-        last = np.asarray(first_tokens, dtype=np.int32).reshape(B)
+        last = np.array(first_tokens, dtype=np.int32).reshape(B)  # a copy: updated in place below
         gen = [[] for _ in range(B)]
         ns = np.zeros((n_iter, B), dtype=np.int32)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -237,12 +242,16 @@ class SpecDecoder:
             res["tally"] = self.tally.cpu().numpy()
         return res
 
-    def run_target_only(self, first_tokens, n_tokens: int, workload_id: int = 0):
-        """Plain decoding with the W4A16 model alone, one target pass per token (the baseline)."""
-        B, G1 = self.B, self.gamma + 1
+    def run_target_only(self, first_tokens, n_tokens: int, workload_id: int = 0, padded: bool = False):
+        """Plain decoding with the W4A16 model alone, one target pass per token (the baseline).
+        padded: run each step at the verify pass's M (sequence b's token in rows b(gamma+1) ..
+        b(gamma+1)+gamma), so that its logits are bit-identical to the verify pass's."""
+        B = self.B
+        G1 = self.gamma + 1 if padded else 1
+        t = self.tgt[padded]
         if self.use_graphs and self.graphs is None:
             self._capture()
-        last = np.asarray(first_tokens, dtype=np.int32).reshape(B)
+        last = np.array(first_tokens, dtype=np.int32).reshape(B)  # a copy: updated in place below
         gen = [[] for _ in range(B)]
         h_tt = torch.zeros(B * G1, dtype=torch.int32).pin_memory()
         h_sel = torch.zeros(B * G1, dtype=torch.int32).pin_memory()
@@ -252,16 +261,16 @@ class SpecDecoder:
         stream = torch.cuda.current_stream()
         t0 = time.perf_counter()
         for k in range(n_tokens):
-            h_tt.numpy()[:] = np.repeat(last, G1)        # sequence b's token in rows b(G1)..b(G1)+gamma
-            self.tt.copy_(h_tt, non_blocking=True)
+            h_tt.numpy()[:] = np.repeat(last, G1)
+            t["tok"].copy_(h_tt, non_blocking=True)
             if self.sampling:
                 u = syn.uniforms((B,), workload_id, syn.STREAM_U_DRAFT, 10_000_000 + k)
                 h_u.numpy()[:] = np.repeat(u, G1)
-                self.u_t.copy_(h_u, non_blocking=True)
+                t["u"].copy_(h_u, non_blocking=True)
             ev[0].record(stream)
-            self._run(2)
+            self._run(3 if padded else 2)
             ev[1].record(stream)
-            h_sel.copy_(self.tsel, non_blocking=True)
+            h_sel.copy_(t["sel"], non_blocking=True)
             stream.synchronize()
             t_target.append(ev[0].elapsed_time(ev[1]))
             sel = h_sel.numpy()

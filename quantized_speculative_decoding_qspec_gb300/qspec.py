@@ -118,7 +118,8 @@ def qspec_linear_workspace_size(M, N, K):
 
 
 def new_linear_workspace(M, N, K, device="cuda"):
-    """A zero-filled linear workspace (zero once; calls keep it ready)."""
+    """A zero-filled linear workspace (zero once; calls of this (M, N, K) keep it ready, other shapes
+    need their own)."""
     n = qspec_linear_workspace_size(M, N, K)
     if n == 0:
         raise ValueError("invalid linear shape")

@@ -172,16 +172,31 @@ def check_iterations(res, gamma, sampling, workload_id):
         assert gen[b] == want
 
 
-@pytest.mark.parametrize("B,gamma,use_graphs", [(1, 3, True), (3, 2, True), (2, 4, False)])
-def test_decode_loop_greedy(q, dec, B, gamma, use_graphs):
-    model = small_model(dec)
+def check_target_logits(model, rec, tol=1e-2):
+    """The verify pass's logits against the oracle's toy model on the same input tokens (three chained
+    W4A16 layers, each output rounded to bf16: relative Frobenius error within 1e-2)."""
+    tokens = np.concatenate([rec["tokens_in"][:, None], rec["d"]], axis=1).reshape(-1)
+    E = bf16_host_bits(model.E)
+    ref = oracle.bf16_to_f32(oracle.toy_forward(E, host_layers(model), tokens, False)).astype(np.float64)
+    got = oracle.bf16_to_f32(bf16_host_bits(rec["tl"])).astype(np.float64).reshape(ref.shape)
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= tol
+
+
+# (5, 3): the verify pass runs at M = 20, on the tensor-core linear; V = 16384 gives the last layer
+# more output tiles than the first two, so layers sharing one workspace would corrupt its tickets
+@pytest.mark.parametrize("B,gamma,use_graphs,V", [(1, 3, True, 1000), (3, 2, True, 1000), (2, 4, False, 1000),
+                                                  (5, 3, True, 16384)])
+def test_decode_loop_greedy(q, dec, B, gamma, use_graphs, V):
+    model = small_model(dec, V=V)
     sd = dec.SpecDecoder(model, B, gamma, use_graphs=use_graphs)
     first = np.arange(B, dtype=np.int32) * 37 + 1
     res = sd.run(first, n_iter=6, record=True)
     check_iterations(res, gamma, False, 0)
+    check_target_logits(model, res["records"][0])
+    check_target_logits(model, res["records"][-1])
     # output equivalence: greedy speculative decoding emits exactly what the target alone emits
     n_tok = min(len(g) for g in res["generated"])
-    base = sd.run_target_only(first, n_tok)
+    base = sd.run_target_only(first, n_tok, padded=True)
     for b in range(B):
         assert res["generated"][b][:n_tok] == base["generated"][b]
     # top-1 tally: positions counted once per draft position, agreement as the oracle counts it

@@ -755,6 +755,28 @@ struct WsLayout {
   size_t ticket, partial, codes, s_a, total;
 };
 
+// Stream-K grid: P CTAs share U = tiles x groups units.  A CTA costs about its units plus, for
+// the last contributor of a split tile, one read of every other contributor's partial tile
+// (NM >= 32: one contributor's loads in flight at a time, about 1.5 units each; NM = 16: eight
+// in flight).  Few tiles over many CTAs make many contributors per tile, so the grid is the P that
+// minimises ceil(U / P) + (contributors per tile) x fixup cost, ties to the wider grid.
+int pick_ctas(int NM, long long U, int G, int sms) {
+  const double fix = NM == 16 ? 0.25 : 1.5;
+  int best = 1;
+  double best_cost = 0.0;
+  const int p_max = static_cast<int>(std::min<long long>(U, sms));
+  for (int P = 1; P <= p_max; ++P) {
+    const long long per = (U + P - 1) / P;
+    const long long contrib = (static_cast<long long>(G) * P + U - 1) / U + 1;
+    const double cost = static_cast<double>(per) + (P > 1 ? fix * static_cast<double>(contrib) : 0.0);
+    if (P == 1 || cost <= best_cost) {
+      best = P;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 WsLayout ws_layout(bool a4, int M, int N, int K, int P) {
   const int NM = pick_nm(a4, M);
   const long long T = (static_cast<long long>(N) + 127) / 128 * ((M + NM - 1) / NM);
@@ -809,7 +831,7 @@ qspec_status linear_tc(bool a4, const uint16_t* x, const uint8_t* Wp, const uint
   const long long T = (static_cast<long long>(N) + 127) / 128 * T_m;
   const int G = K / kGroup;
   const long long U = T * G;
-  const int P = static_cast<int>(std::min<long long>(U, num_sms()));
+  const int P = pick_ctas(NM, U, G, num_sms());
   const WsLayout L = ws_layout(a4, M, N, K, num_sms());
   if (!ws || ws_bytes < L.total) return QSPEC_ERR_WORKSPACE;
   char* wsb = static_cast<char*>(ws);

@@ -628,9 +628,10 @@ def sweep_linear():
             x = torch.from_numpy(syn.activations(M, K, 3, step=M).view(np.int16)).to(dev).view(torch.bfloat16)
             y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
             ws = q.new_linear_workspace(M, N, K, device=dev)
-            for mode in ("a16", "a4"):
-                fn = ((lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws)) if mode == "a16"
-                      else (lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws)))
+            for mode in ("a16", "a4", "a8") if M in (1, 4, 16, 64) else ("a16", "a4"):
+                fn = {"a16": lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws),
+                      "a4": lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws),
+                      "a8": lambda: q.qspec_linear_w4a8(x, Wp, S, y, ws)}[mode]
                 t = _graph_time(fn)
                 b = linear_bytes(M, N, K)
                 print(json.dumps({"sweep": "llama70b_linear", "layer": name, "N": N, "K": K, "M": M, "mode": mode,

@@ -117,7 +117,22 @@ qspec_status qspec_linear_w4a4(const uint16_t* x, const uint8_t* Wp, const uint1
                                int32_t* acc_out, void* ws, size_t ws_bytes, qspec_stream_t stream);
 
 /*
- * qspec_linear_workspace_size -- bytes of device workspace both linear calls need for an [M, K] x
+ * qspec_linear_w4a8 -- the W4A8 configuration (step f3): qspec_linear_w4a4 with 8-bit activations.
+ *
+ * The speculative-decoding-with-quantisation summary (aibr.jp), section "中核となる技術的要素",
+ * names W4A8 beside W4A16 as a weight/activation configuration; it gives no quantiser, so this one
+ * is the W4A4 quantiser at 8 bits, on the same packed 4-bit weights:
+ *     s_a[m]    = amax_k |x[m,k]| / 127                     (fp32 IEEE division, kept in fp32)
+ *     qa[m,k]   = clamp( rint( x[m,k] / s_a[m] ), -128, 127 ) (fp32 IEEE division, ties even)
+ *     acc, y    as for qspec_linear_w4a4 (|acc| <= 131072: exact)
+ *   Arguments, outputs and limits as qspec_linear_w4a4.
+ */
+qspec_status qspec_linear_w4a8(const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int64_t M,
+                               int64_t N, int64_t K, uint16_t* y, int8_t* xq_out, float* xs_out,
+                               int32_t* acc_out, void* ws, size_t ws_bytes, qspec_stream_t stream);
+
+/*
+ * qspec_linear_workspace_size -- bytes of device workspace the linear calls need for an [M, K] x
  * [N, K] product on the CURRENT device (the size depends on its SM count).  0 for invalid sizes.
  */
 size_t qspec_linear_workspace_size(int64_t M, int64_t N, int64_t K);

@@ -14,6 +14,8 @@ Sources (web pages; cited by title and section):
   "W4A4 と W4A16 量子化" (W4A16: 4-bit weights converted while multiplying 16-bit activations;
   W4A4: weights and activations both 4-bit) and "QSpec の W4A4 モードと W4A16 モード" (one shared
   4-bit weight set serves both modes).
+* [SD+Q summary]  the summary of a study of speculative decoding with quantisation (aibr.jp),
+  section "中核となる技術的要素" (names W4A16 and W4A8 configurations).
 * [SD-tutorial]  "Speculative Decodingとは？LLM生成を速くする方法" (kasblo.com), sections
   "greedy decodingでは一致するprefixを採用する" (greedy rule), "samplingでもtargetの確率分布を保つ"
   (eq. a(x) = min(1, p(x)/q(x)) and the residual eq. p'(x)), "3 tokenの数値例" (worked example) and
@@ -176,20 +178,21 @@ def linear_w4a16(x_bits, Wp, S, rows=None) -> np.ndarray:
 # ----------------------------------------------------------------------------------------------
 
 
-def quantize_activations(x_bits):
-    """Per-token symmetric INT4 activation quantisation.
+def quantize_activations(x_bits, bits=4):
+    """Per-token symmetric activation quantisation to `bits`-bit codes (4: W4A4, 8: W4A8).
 
-    Returns (qa int8 [M, K], s_a float32 [M]):
-        amax = max_k |x[m, k]|;  s_a = amax / 7 (fp32 IEEE division, kept in fp32);
-        qa = clamp(rint(x / s_a), -8, 7) (fp32 IEEE division, ties to even); s_a == 0 -> 0.
+    Returns (qa int8 [M, K], s_a float32 [M]), with qmax = 2**(bits-1) - 1 (7 or 127):
+        amax = max_k |x[m, k]|;  s_a = amax / qmax (fp32 IEEE division, kept in fp32);
+        qa = clamp(rint(x / s_a), -qmax - 1, qmax) (fp32 IEEE division, ties to even); s_a == 0 -> 0.
     """
+    qmax = 2 ** (bits - 1) - 1
     x = bf16_to_f32(x_bits)
     amax = np.max(np.abs(x), axis=1)
-    s_a = (amax / np.float32(7.0)).astype(np.float32)
+    s_a = (amax / np.float32(qmax)).astype(np.float32)
     qa = np.zeros(x.shape, dtype=np.int8)
     for m in range(x.shape[0]):
         if s_a[m] != 0:
-            qa[m] = np.clip(np.rint(x[m] / s_a[m]), -8, 7).astype(np.int8)
+            qa[m] = np.clip(np.rint(x[m] / s_a[m]), -qmax - 1, qmax).astype(np.int8)
     return qa, s_a
 
 
@@ -212,13 +215,13 @@ def w4a4_group_sums(qa, Wp, rows=None) -> np.ndarray:
     return acc.astype(np.int32)
 
 
-def linear_w4a4(x_bits, Wp, S, rows=None):
-    """Draft-mode linear.
+def linear_w4a4(x_bits, Wp, S, rows=None, bits=4):
+    """Draft-mode linear (bits=8: the W4A8 configuration on the same weights).
 
     Returns dict(qa, s_a, acc int32 [M, N, G], y fp64 [M, N]) with
         y[m, n] = s_a[m] * sum_g s[n, g] * acc[m, n, g]   (fp64).
     """
-    qa, s_a = quantize_activations(x_bits)
+    qa, s_a = quantize_activations(x_bits, bits)
     acc = w4a4_group_sums(qa, Wp, rows)
     S = np.asarray(S, dtype=np.float16)
     if rows is not None:
@@ -226,6 +229,17 @@ def linear_w4a4(x_bits, Wp, S, rows=None):
     Sg = S.astype(np.float64)                                        # [N, G]
     y = s_a.astype(np.float64)[:, None] * np.einsum("mng,ng->mn", acc.astype(np.float64), Sg)
     return {"qa": qa, "s_a": s_a, "acc": acc, "y": y}
+
+
+# ----------------------------------------------------------------------------------------------
+# f3: W4A8       [SD+Q summary] "中核となる技術的要素" names W4A8 beside W4A16; the quantiser is the
+#                W4A4 one at 8 bits (the summary gives none)
+# ----------------------------------------------------------------------------------------------
+
+
+def linear_w4a8(x_bits, Wp, S, rows=None):
+    """W4A8 linear: per-token 8-bit activation codes (s_a = amax / 127), 4-bit shared weights."""
+    return linear_w4a4(x_bits, Wp, S, rows, bits=8)
 
 
 # ----------------------------------------------------------------------------------------------

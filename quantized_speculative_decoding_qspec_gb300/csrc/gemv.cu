@@ -79,7 +79,10 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// A4: W4A4 (quantise the tokens, optional int8 codes / fp32 scales out); ACC: also the int32 group
+// QB: activation bits of the quantised modes -- 4 (W4A4) or 8 (W4A8: the same per-token quantiser
+// with divisor 127 and codes in [-128, 127], a configuration the speculative-decoding-with-
+// quantisation summary on aibr.jp names in its section "中核となる技術的要素"), 0 for W4A16.  The
+// quantised modes quantise the tokens (optional int8 codes / fp32 scales out); ACC: also the int32 group
 // sums (a separate instantiation keeps their stores out of the hot loop when not asked for).
 // MT = token slots staged in shared memory (1, 2, 4, 8 or 16; tokens >= M contribute zeros); the
 // tokens form NB = ceil(MT / 8) MMA column blocks of 8 that share every weight fragment.  D = weight
@@ -91,11 +94,13 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // ahead across tile boundaries, so the stream never drains; the first fetches are issued before
 // the kernel waits for its predecessor (no library kernel that may run ahead of this one writes
 // packed weights or scales).
-template <bool A4, bool ACC, int MT, int D>
+template <int QB, bool ACC, int MT, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ Wp, const __half* __restrict__ S,
                 int M, int N, int K, int KS, uint16_t* __restrict__ y, int8_t* __restrict__ xq_out,
                 float* __restrict__ xs_out, int32_t* __restrict__ acc_out) {
+  constexpr bool A4 = QB != 0;                       // activations quantised (W4A4 or W4A8)
+  constexpr float kQmax = QB == 8 ? 127.0f : 7.0f;   // codes in [-kQmax - 1, kQmax]
   extern __shared__ __align__(16) uint8_t sm[];
   const int G = K / kGroup;
   // activations: chunk ((gi * 4 + j) * MT + m) * 4 + t holds x[m, 128 gi + 32 t + 8 j .. + 7]
@@ -177,10 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   auto slot_of = [&](int m, int v) { return ((v >> 2) * MT + m) * 4 + (v & 3); };
-  // W4A4: codes = clamp(rint(x / s_a), -8, 7) of one chunk, as exact bf16 (and the int8 codes out)
+  // W4A4 / W4A8: codes = clamp(rint(x / s_a), -qmax - 1, qmax) of one chunk, as exact bf16 (and the
+  // int8 codes out)
   auto quantise = [&](int m, int v, uint4 val) {
     const float sa = s_a[m], rsa = s_r[m];
-    const bool fast = sa >= 0x1p-100f;  // see div_rn_markstein
+    // see div_rn_markstein (checked for the 4-bit divisor; W4A8 keeps the IEEE division)
+    const bool fast = QB == 4 && sa >= 0x1p-100f;
     uint32_t w[4] = {val.x, val.y, val.z, val.w};
     uint32_t q8[2] = {0, 0};
 #pragma unroll
@@ -190,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float x0 = bf16_lo(w[i]), x1 = bf16_hi(w[i]);
         const float q0 = fast ? div_rn_markstein(x0, sa, rsa) : __fdiv_rn(x0, sa);
         const float q1 = fast ? div_rn_markstein(x1, sa, rsa) : __fdiv_rn(x1, sa);
-        c0f = fminf(fmaxf(rintf(q0), -8.0f), 7.0f);
-        c1f = fminf(fmaxf(rintf(q1), -8.0f), 7.0f);
+        c0f = fminf(fmaxf(rintf(q0), -kQmax - 1.0f), kQmax);
+        c1f = fminf(fmaxf(rintf(q1), -kQmax - 1.0f), kQmax);
       }
       w[i] = static_cast<uint32_t>(f32_to_bf16_bits(c0f)) | (static_cast<uint32_t>(f32_to_bf16_bits(c1f)) << 16);
       q8[i >> 1] |= ((static_cast<uint32_t>(static_cast<int>(c0f)) & 0xFFu) |
@@ -224,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x < M) {
       unsigned int m_all = 0;
       for (int w = 0; w < kWarps; ++w) m_all = max(m_all, red_max[w * MT + threadIdx.x]);
-      s_a[threadIdx.x] = __fdiv_rn(__uint_as_float(m_all << 16), 7.0f);
+      s_a[threadIdx.x] = __fdiv_rn(__uint_as_float(m_all << 16), kQmax);
       s_r[threadIdx.x] = __frcp_rn(s_a[threadIdx.x]);
       if (xs_out && blockIdx.x == 0) xs_out[threadIdx.x] = s_a[threadIdx.x];
     }
@@ -391,11 +398,11 @@ struct Outs {
   int32_t* acc;
 };
 
-template <bool A4, bool ACC, int MT, int D>
+template <int QB, bool ACC, int MT, int D>
 qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
                       Outs o, int best_ks, int best_grid, cudaStream_t stream) {
   const size_t smem = smem_bytes(MT, K);
-  auto kern = gemv_kernel<A4, ACC, MT, D>;
+  auto kern = gemv_kernel<QB, ACC, MT, D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return QSPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -413,7 +420,7 @@ qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int
              : QSPEC_ERR_CUDA;
 }
 
-template <bool A4, int MT>
+template <int QB, int MT>
 qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
                     Outs o, cudaStream_t stream) {
   const int G = K / kGroup;
@@ -435,18 +442,18 @@ qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M
     }
   }
   const int gs = G / best_ks;
-  if constexpr (A4) {
+  if constexpr (QB != 0) {
     if (o.acc) {  // the checking path: group sums out, no need for the deepest prefetch
-      if (gs % 2 == 0) return launch_d<true, true, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
-      return launch_d<true, true, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+      if (gs % 2 == 0) return launch_d<QB, true, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+      return launch_d<QB, true, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
     }
   }
   // (16 token slots keep two column blocks of accumulators: at most two groups in flight then)
   if constexpr (MT < 16) {
-    if (gs % 4 == 0) return launch_d<A4, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+    if (gs % 4 == 0) return launch_d<QB, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
   }
-  if (gs % 2 == 0) return launch_d<A4, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
-  return launch_d<A4, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+  if (gs % 2 == 0) return launch_d<QB, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+  return launch_d<QB, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
 }
 
 }  // namespace
@@ -459,16 +466,24 @@ bool gemv_supported(int M, int N, int K) {
   return smem_bytes(token_slots(M), K) <= 200 * 1024;
 }
 
-qspec_status gemv(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
+template <int MT>
+qspec_status launch_mode(int abits, const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K,
+                         uint16_t* y, Outs o, cudaStream_t stream) {
+  if (abits == 4) return launch<4, MT>(x, Wp, S, M, N, K, y, o, stream);
+  if (abits == 8) return launch<8, MT>(x, Wp, S, M, N, K, y, o, stream);
+  return launch<0, MT>(x, Wp, S, M, N, K, y, o, stream);
+}
+
+qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
                   uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream) {
   const __half* Sh = reinterpret_cast<const __half*>(S);
   const Outs o{xq_out, xs_out, acc_out};
   switch (token_slots(M)) {
-    case 1: return a4 ? launch<true, 1>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 1>(x, Wp, Sh, M, N, K, y, o, stream);
-    case 2: return a4 ? launch<true, 2>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 2>(x, Wp, Sh, M, N, K, y, o, stream);
-    case 4: return a4 ? launch<true, 4>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 4>(x, Wp, Sh, M, N, K, y, o, stream);
-    case 8: return a4 ? launch<true, 8>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 8>(x, Wp, Sh, M, N, K, y, o, stream);
-    default: return a4 ? launch<true, 16>(x, Wp, Sh, M, N, K, y, o, stream) : launch<false, 16>(x, Wp, Sh, M, N, K, y, o, stream);
+    case 1: return launch_mode<1>(abits, x, Wp, Sh, M, N, K, y, o, stream);
+    case 2: return launch_mode<2>(abits, x, Wp, Sh, M, N, K, y, o, stream);
+    case 4: return launch_mode<4>(abits, x, Wp, Sh, M, N, K, y, o, stream);
+    case 8: return launch_mode<8>(abits, x, Wp, Sh, M, N, K, y, o, stream);
+    default: return launch_mode<16>(abits, x, Wp, Sh, M, N, K, y, o, stream);
   }
 }
 

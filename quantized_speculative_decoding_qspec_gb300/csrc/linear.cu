@@ -47,16 +47,17 @@ __device__ __forceinline__ void load_x32(const uint16_t* p, float (&x)[32]) {
   }
 }
 
-// Per-token activation quantiser of step a3: s_a = amax / 7 (fp32), code = clamp(rint(x / s_a)).
-__device__ __forceinline__ float quant_act(float x, float s_a) {
+// Per-token activation quantiser of step a3: s_a = amax / qmax (fp32), code = clamp(rint(x / s_a),
+// -qmax - 1, qmax); qmax = 7 (W4A4) or 127 (W4A8).
+__device__ __forceinline__ float quant_act(float x, float s_a, float qmax) {
   if (s_a == 0.0f) return 0.0f;
-  return fminf(fmaxf(rintf(__fdiv_rn(x, s_a)), -8.0f), 7.0f);
+  return fminf(fmaxf(rintf(__fdiv_rn(x, s_a)), -qmax - 1.0f), qmax);
 }
 
 // grid: (N / 8, ceil(M / 8)); block: 8 warps; warp w computes row n = 8 * blockIdx.x + w for the
 // block's 8 tokens.  Lane l walks K in 32-weight chunks c = l, l + 32, ...; the 4 lanes sharing a
 // 128-channel group in one pass are 4j..4j+3 (K % 128 == 0 keeps a group inside one pass).
-template <bool kA4>
+template <int QB>
 __global__ void __launch_bounds__(256) linear_simt_kernel(const uint16_t* __restrict__ x,
                                                           const uint8_t* __restrict__ Wp,
                                                           const __half* __restrict__ S, int M,
@@ -72,6 +73,8 @@ __global__ void __launch_bounds__(256) linear_simt_kernel(const uint16_t* __rest
   const int mt = min(kMT, M - m0);
   const int G = K / kGroup;
 
+  constexpr bool kA4 = QB != 0;  // activations quantised (W4A4 or W4A8)
+  constexpr float kQmax = QB == 8 ? 127.0f : 7.0f;
   float s_a[kMT];
   if constexpr (kA4) {
     // Per-token amax over all of K (step a3), block-wide.
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(256) linear_simt_kernel(const uint16_t* __rest
     if (threadIdx.x < kMT) {
       float a = 0.0f;
       for (int w = 0; w < kWarps; ++w) a = fmaxf(a, s_red[w][threadIdx.x]);
-      s_amax[threadIdx.x] = __fdiv_rn(a, 7.0f);
+      s_amax[threadIdx.x] = __fdiv_rn(a, kQmax);
     }
     __syncthreads();
 #pragma unroll
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(256) linear_simt_kernel(const uint16_t* __rest
           const uint16_t* xr = x + static_cast<int64_t>(m0 + m) * K;
           for (int k = threadIdx.x; k < K; k += blockDim.x)
             xq_out[static_cast<int64_t>(m0 + m) * K + k] =
-                static_cast<int8_t>(quant_act(bf16_lo(xr[k]), s_a[m]));
+                static_cast<int8_t>(quant_act(bf16_lo(xr[k]), s_a[m], kQmax));
         }
       }
     }
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(256) linear_simt_kernel(const uint16_t* __rest
         if constexpr (kA4) {
           int part = 0;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) part += static_cast<int>(quant_act(xv[i], s_a[m])) * static_cast<int>(code[i]);
+          for (int i = 0; i < 32; ++i) part += static_cast<int>(quant_act(xv[i], s_a[m], kQmax)) * static_cast<int>(code[i]);
           // exact group sum over the 4 lanes sharing group g
           part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
           part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
@@ -169,15 +172,17 @@ __global__ void __launch_bounds__(256) linear_simt_kernel(const uint16_t* __rest
 
 }  // namespace
 
-qspec_status linear_simt(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M,
+qspec_status linear_simt(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M,
                          int N, int K, uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out,
                          cudaStream_t stream) {
   dim3 grid(N / kWarps, (M + kMT - 1) / kMT);
   const __half* Sh = reinterpret_cast<const __half*>(S);
-  if (a4)
-    linear_simt_kernel<true><<<grid, 256, 0, stream>>>(x, Wp, Sh, M, N, K, y, xq_out, xs_out, acc_out);
+  if (abits == 4)
+    linear_simt_kernel<4><<<grid, 256, 0, stream>>>(x, Wp, Sh, M, N, K, y, xq_out, xs_out, acc_out);
+  else if (abits == 8)
+    linear_simt_kernel<8><<<grid, 256, 0, stream>>>(x, Wp, Sh, M, N, K, y, xq_out, xs_out, acc_out);
   else
-    linear_simt_kernel<false><<<grid, 256, 0, stream>>>(x, Wp, Sh, M, N, K, y, nullptr, nullptr, nullptr);
+    linear_simt_kernel<0><<<grid, 256, 0, stream>>>(x, Wp, Sh, M, N, K, y, nullptr, nullptr, nullptr);
   return launch_status();
 }
 
@@ -201,9 +206,12 @@ extern "C" size_t qspec_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0 || M > QSPEC_MAX_M || N % 8 != 0 || K % qspec::kGroup != 0 ||
       N > (int64_t(1) << 30) || K > (int64_t(1) << 30))
     return 0;
-  const size_t a = qspec::linear_tc_workspace_size(false, int(M), int(N), int(K));
-  const size_t b = qspec::linear_tc_workspace_size(true, int(M), int(N), int(K));
-  return a > b ? a : b;
+  size_t n = 0;
+  for (int abits : {16, 4, 8}) {
+    const size_t b = qspec::linear_tc_workspace_size(abits, int(M), int(N), int(K));
+    if (b > n) n = b;
+  }
+  return n;
 }
 
 extern "C" qspec_status qspec_linear_w4a16(const uint16_t* x, const uint8_t* Wp, const uint16_t* S,
@@ -215,16 +223,17 @@ extern "C" qspec_status qspec_linear_w4a16(const uint16_t* x, const uint8_t* Wp,
   if (!qspec::aligned16(ws)) return QSPEC_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (qspec::gemv_supported(int(M), int(N), int(K)))
-    return qspec::gemv(false, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, s);
-  if (qspec::linear_tc_supported(false, int(M), int(N), int(K)))
-    return qspec::linear_tc(false, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, ws, ws_bytes, s);
-  return qspec::linear_simt(false, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, s);
+    return qspec::gemv(16, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, s);
+  if (qspec::linear_tc_supported(16, int(M), int(N), int(K)))
+    return qspec::linear_tc(16, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, ws, ws_bytes, s);
+  return qspec::linear_simt(16, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, s);
 }
 
-extern "C" qspec_status qspec_linear_w4a4(const uint16_t* x, const uint8_t* Wp, const uint16_t* S,
-                                          int64_t M, int64_t N, int64_t K, uint16_t* y,
-                                          int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws,
-                                          size_t ws_bytes, qspec_stream_t stream) {
+namespace {
+// The quantised-activation linears (steps a3 + a4, and the W4A8 variant): abits = 4 or 8.
+qspec_status linear_quantised(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int64_t M,
+                              int64_t N, int64_t K, uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out,
+                              void* ws, size_t ws_bytes, qspec_stream_t stream) {
   const qspec_status st = check_linear_args(x, Wp, S, M, N, K, y);
   if (st != QSPEC_OK) return st;
   if ((xq_out && !qspec::aligned16(xq_out)) || (xs_out && !qspec::aligned16(xs_out)) ||
@@ -234,8 +243,23 @@ extern "C" qspec_status qspec_linear_w4a4(const uint16_t* x, const uint8_t* Wp, 
   if (!qspec::aligned16(ws)) return QSPEC_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (qspec::gemv_supported(int(M), int(N), int(K)))
-    return qspec::gemv(true, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, s);
-  if (qspec::linear_tc_supported(true, int(M), int(N), int(K)))
-    return qspec::linear_tc(true, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, ws, ws_bytes, s);
-  return qspec::linear_simt(true, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, s);
+    return qspec::gemv(abits, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, s);
+  if (qspec::linear_tc_supported(abits, int(M), int(N), int(K)))
+    return qspec::linear_tc(abits, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, ws, ws_bytes, s);
+  return qspec::linear_simt(abits, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, s);
+}
+}  // namespace
+
+extern "C" qspec_status qspec_linear_w4a4(const uint16_t* x, const uint8_t* Wp, const uint16_t* S,
+                                          int64_t M, int64_t N, int64_t K, uint16_t* y,
+                                          int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws,
+                                          size_t ws_bytes, qspec_stream_t stream) {
+  return linear_quantised(4, x, Wp, S, M, N, K, y, xq_out, xs_out, acc_out, ws, ws_bytes, stream);
+}
+
+extern "C" qspec_status qspec_linear_w4a8(const uint16_t* x, const uint8_t* Wp, const uint16_t* S,
+                                          int64_t M, int64_t N, int64_t K, uint16_t* y,
+                                          int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws,
+                                          size_t ws_bytes, qspec_stream_t stream) {
+  return linear_quantised(8, x, Wp, S, M, N, K, y, xq_out, xs_out, acc_out, ws, ws_bytes, stream);
 }

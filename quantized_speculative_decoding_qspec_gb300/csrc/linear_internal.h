@@ -8,21 +8,23 @@
 
 namespace qspec {
 
+// abits: activation width of the mode -- 16 (W4A16), 4 (W4A4) or 8 (W4A8).
+
 // CUDA-core kernels: every shape the entry points accept.
-qspec_status linear_simt(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M,
+qspec_status linear_simt(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M,
                          int N, int K, uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out,
                          cudaStream_t stream);
 
 // Tensor-core (tcgen05) kernels: the shapes for which linear_tc_supported() is true.
-bool linear_tc_supported(bool a4, int M, int N, int K);
-size_t linear_tc_workspace_size(bool a4, int M, int N, int K);
-qspec_status linear_tc(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M,
+bool linear_tc_supported(int abits, int M, int N, int K);
+size_t linear_tc_workspace_size(int abits, int M, int N, int K);
+qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M,
                        int N, int K, uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out,
                        void* ws, size_t ws_bytes, cudaStream_t stream);
 
-// Register-fragment MMA GEMV for both modes at decode sizes (M <= 8; the staged activations must fit).
+// Register-fragment MMA GEMV for every mode at decode sizes (M <= 16; the staged activations must fit).
 bool gemv_supported(int M, int N, int K);
-qspec_status gemv(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
+qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
                   uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream);
 
 // Reads (synchronously) and clears the error bits the linear kernels set on the current device.

@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
 
 // Per-token quantiser for M > 4 (step a3): codes as exact bf16 for the GEMM, plus the optional
 // int8 codes and fp32 scales.  One CTA per token.
-__global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, int K,
+__global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, int K, float qmax,
                                                         uint16_t* __restrict__ codes, float* __restrict__ s_a,
                                                         int8_t* __restrict__ xq_out, float* __restrict__ xs_out) {
   grid_launch_dependents();
@@ -704,13 +704,13 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restri
   for (int off = 16; off >= 1; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
   if ((threadIdx.x & 31) == 0) atomicMax(&s_mx, mx);
   __syncthreads();
-  const float sa = __fdiv_rn(__uint_as_float(s_mx << 16), 7.0f);
+  const float sa = __fdiv_rn(__uint_as_float(s_mx << 16), qmax);
   if (threadIdx.x == 0) {
     s_a[m] = sa;
     if (xs_out) xs_out[m] = sa;
   }
   for (int k = threadIdx.x; k < K; k += 256) {
-    const float cq = sa == 0.0f ? 0.0f : fminf(fmaxf(rintf(__fdiv_rn(bf16_lo(xr[k]), sa)), -8.0f), 7.0f);
+    const float cq = sa == 0.0f ? 0.0f : fminf(fmaxf(rintf(__fdiv_rn(bf16_lo(xr[k]), sa)), -qmax - 1.0f), qmax);
     codes[static_cast<long long>(m) * K + k] = f32_to_bf16_bits(cq);
     if (xq_out) xq_out[static_cast<long long>(m) * K + k] = static_cast<int8_t>(cq);
   }
@@ -744,8 +744,13 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int pick_nm(bool a4, int M) {
-  if (a4 && M <= kFusedMaxM) return 16;
+// The fused kernel quantises W4A4 tokens itself (M <= 4); other quantised cases (W4A4 at larger M,
+// every W4A8) quantise in act_quant_kernel first and multiply codes.
+bool fused_mode(int abits, int M) { return abits == 4 && M <= kFusedMaxM; }
+bool codes_mode_of(int abits, int M) { return abits != 16 && !fused_mode(abits, M); }
+
+int pick_nm(int abits, int M) {
+  if (fused_mode(abits, M)) return 16;
   return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 48 ? 48 : 64));
 }
 
@@ -777,15 +782,16 @@ int pick_ctas(int NM, long long U, int G, int sms) {
   return best;
 }
 
-WsLayout ws_layout(bool a4, int M, int N, int K, int P) {
-  const int NM = pick_nm(a4, M);
+WsLayout ws_layout(int abits, int M, int N, int K, int P) {
+  const int NM = pick_nm(abits, M);
   const long long T = (static_cast<long long>(N) + 127) / 128 * ((M + NM - 1) / NM);
   WsLayout L;
   size_t off = 0;
   L.ticket = off;  off = al256(off + sizeof(unsigned int) * T);
   L.partial = off; off = al256(off + sizeof(float) * size_t(P) * 2 * 128 * NM);
-  L.codes = off;   off = al256(off + ((a4 && M > kFusedMaxM) ? sizeof(uint16_t) * size_t(M) * K : 0));
-  L.s_a = off;     off = al256(off + ((a4 && M > kFusedMaxM) ? sizeof(float) * size_t(M) : 0));
+  const bool codes = codes_mode_of(abits, M);
+  L.codes = off;   off = al256(off + (codes ? sizeof(uint16_t) * size_t(M) * K : 0));
+  L.s_a = off;     off = al256(off + (codes ? sizeof(float) * size_t(M) : 0));
   L.total = off;
   return L;
 }
@@ -812,31 +818,31 @@ qspec_status launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcA
 
 }  // namespace
 
-bool linear_tc_supported(bool a4, int M, int N, int K) {
+bool linear_tc_supported(int abits, int M, int N, int K) {
   if (M < 1 || M > QSPEC_MAX_M || N < 8 || K < kGroup) return false;
-  const int NM = pick_nm(a4, M);
+  const int NM = pick_nm(abits, M);
   const long long U = (static_cast<long long>(N) + 127) / 128 * ((M + NM - 1) / NM) * (K / kGroup);
   return U < (1LL << 31) && encode_fn() != nullptr;  // the device side counts units in 32 bits
 }
 
-size_t linear_tc_workspace_size(bool a4, int M, int N, int K) {
-  return ws_layout(a4, M, N, K, num_sms()).total;
+size_t linear_tc_workspace_size(int abits, int M, int N, int K) {
+  return ws_layout(abits, M, N, K, num_sms()).total;
 }
 
-qspec_status linear_tc(bool a4, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
+qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
                        uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, size_t ws_bytes,
                        cudaStream_t stream) {
-  const int NM = pick_nm(a4, M);
+  const int NM = pick_nm(abits, M);
   const int T_m = (M + NM - 1) / NM;
   const long long T = (static_cast<long long>(N) + 127) / 128 * T_m;
   const int G = K / kGroup;
   const long long U = T * G;
   const int P = pick_ctas(NM, U, G, num_sms());
-  const WsLayout L = ws_layout(a4, M, N, K, num_sms());
+  const WsLayout L = ws_layout(abits, M, N, K, num_sms());
   if (!ws || ws_bytes < L.total) return QSPEC_ERR_WORKSPACE;
   char* wsb = static_cast<char*>(ws);
 
-  const bool codes_mode = a4 && M > kFusedMaxM;
+  const bool codes_mode = codes_mode_of(abits, M);
   uint16_t* codes = reinterpret_cast<uint16_t*>(wsb + L.codes);
   float* s_a = reinterpret_cast<float*>(wsb + L.s_a);
 
@@ -859,7 +865,8 @@ qspec_status linear_tc(bool a4, const uint16_t* x, const uint8_t* Wp, const uint
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, act_quant_kernel, x, K, codes, s_a, xq_out, xs_out) != cudaSuccess)
+    const float qmax = abits == 8 ? 127.0f : 7.0f;
+    if (cudaLaunchKernelEx(&cfg, act_quant_kernel, x, K, qmax, codes, s_a, xq_out, xs_out) != cudaSuccess)
       return QSPEC_ERR_CUDA;
   }
 
@@ -881,7 +888,7 @@ qspec_status linear_tc(bool a4, const uint16_t* x, const uint8_t* Wp, const uint
   args.xq_out = xq_out;
   args.xs_out = xs_out;
 
-  if (!a4) {
+  if (abits == 16) {
     switch (NM) {
       case 16: return launch_tc<16, kA16>(tmW, tmX, args, P, stream);
       case 32: return launch_tc<32, kA16>(tmW, tmX, args, P, stream);

@@ -33,6 +33,7 @@ SIGNATURES = {
     "qspec_linear_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "qspec_linear_w4a16": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _P, ctypes.c_size_t, _P]),
     "qspec_linear_w4a4": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "qspec_linear_w4a8": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qspec_verify_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32]),
     "qspec_verify_greedy": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qspec_verify_sample": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
@@ -146,6 +147,18 @@ def qspec_linear_w4a4(x, Wp, S, y, ws, xq_out=None, xs_out=None, acc_out=None, s
     N = Wp.shape[0]
     _check("qspec_linear_w4a4",
            load().qspec_linear_w4a4(_ptr(x), _ptr(Wp), _ptr(S), M, N, K, _ptr(y), _ptr(xq_out), _ptr(xs_out),
+                                    _ptr(acc_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def qspec_linear_w4a8(x, Wp, S, y, ws, xq_out=None, xs_out=None, acc_out=None, stream=None):
+    """The W4A8 configuration: qspec_linear_w4a4 with per-token INT8 activation codes."""
+    _dt(x, torch.bfloat16, "x"); _dt(Wp, torch.uint8, "Wp"); _dt(S, torch.float16, "S"); _dt(y, torch.bfloat16, "y")
+    _dt(xq_out, torch.int8, "xq_out"); _dt(xs_out, torch.float32, "xs_out"); _dt(acc_out, torch.int32, "acc_out")
+    _dt(ws, torch.uint8, "ws")
+    M, K = x.shape
+    N = Wp.shape[0]
+    _check("qspec_linear_w4a8",
+           load().qspec_linear_w4a8(_ptr(x), _ptr(Wp), _ptr(S), M, N, K, _ptr(y), _ptr(xq_out), _ptr(xs_out),
                                     _ptr(acc_out), _ptr(ws), ws.numel(), _stream(stream)))
 
 

@@ -242,6 +242,58 @@ def check_w4a4_constant_activation(o):
     assert np.allclose(r["y"][0], 3.5 * W.astype(np.float64).sum(axis=1), rtol=1e-6, atol=1e-9)
 
 
+# ---------------------------------------------------------------- f3: W4A8
+
+def check_w4a8_quantiser(o):
+    # amax 127 gives s_a = 1: codes are the rounded values (ties to even), +-127 at +-amax
+    x = np.zeros((3, 128), dtype=np.float32)
+    x[0, :8] = [127.0, 2.5, 3.5, -2.5, -127.0, 0.5, 1.5, 100.0]
+    x[1, :2] = [1.0, 0.5]            # s_a = 1/127 in fp32; 0.5 / s_a = 63.5 (fp32) -> 64 (even)
+    qa, s_a = o.quantize_activations(bf16_bits(x), bits=8)
+    assert s_a[0] == 1.0 and qa[0, :8].tolist() == [127, 2, 4, -2, -127, 0, 2, 100]
+    assert s_a[1] == np.float32(1.0) / np.float32(127.0)
+    q = np.float32(0.5) / s_a[1]
+    assert q == np.float32(63.5) and qa[1, 0] == 127 and qa[1, 1] == 64
+    assert s_a[2] == 0.0 and not qa[2].any()
+    # the 4-bit quantiser is the same rule with divisor 7
+    qa4, s4 = o.quantize_activations(bf16_bits(x), bits=4)
+    assert s4[0] == np.float32(127.0) / np.float32(7.0) and qa4[0, 0] == 7
+
+
+def check_w4a8_linear(o):
+    rng = np.random.default_rng(9)
+    M, N, K = 3, 6, 256
+    x = rng.integers(-40, 41, size=(M, K)).astype(np.float32) / 4
+    W = rng.integers(-7, 8, size=(N, K)).astype(np.float32) / 64
+    W[:, 0] = 7 / 64
+    W[:, 128] = -7 / 64
+    Wp, S = o.pack_weights(bf16_bits(W))
+    r = o.linear_w4a8(bf16_bits(x), Wp, S)
+    qa, s_a = r["qa"], r["s_a"]
+    assert int(np.abs(qa).max()) == 127
+    wc = np.rint(W * 64).astype(np.int64)
+    for m in range(M):
+        for n in range(N):
+            for g in range(2):
+                sl = slice(128 * g, 128 * g + 128)
+                assert r["acc"][m, n, g] == int(np.dot(qa[m, sl].astype(np.int64), wc[n, sl]))
+    xa = qa.astype(np.float64) * s_a.astype(np.float64)[:, None]
+    assert np.allclose(r["y"], xa @ o.dequantize_weights(Wp, S).T, rtol=1e-12, atol=0)
+    # 8-bit activations track the 16-bit product far more closely than 4-bit ones
+    xs = rng.standard_normal((4, 1024)).astype(np.float32)
+    xs[:, ::97] *= 20
+    W2 = (rng.standard_normal((64, 1024)) * 0.02).astype(np.float32)
+    Wp2, S2 = o.pack_weights(o.f64_to_bf16_bits(W2))
+    xb = o.f64_to_bf16_bits(xs)
+    ref = o.linear_w4a16(xb, Wp2, S2)
+    e8 = np.linalg.norm(o.linear_w4a8(xb, Wp2, S2)["y"] - ref) / np.linalg.norm(ref)
+    e4 = np.linalg.norm(o.linear_w4a4(xb, Wp2, S2)["y"] - ref) / np.linalg.norm(ref)
+    assert e8 < 0.25 * e4, (e8, e4)
+    # largest group sum: 128 products of (-128)(-8)
+    big = o.w4a4_group_sums(np.full((1, 128), -128, np.int8), o.pack_codes(np.full((1, 128), -8, np.int8)))
+    assert big[0, 0, 0] == 131072
+
+
 # ---------------------------------------------------------------- a5: softmax
 
 def check_softmax(o):
@@ -602,5 +654,6 @@ ALL_FAST = [
     check_greedy_tutorial_example, check_greedy_bruteforce, check_greedy_ties,
     check_greedy_equivalence, check_sampling_worked_example, check_sampling_from_logits,
     check_top1_closed_forms, check_top1_tally, check_select_token, check_toy_forward_onehot,
+    check_w4a8_quantiser, check_w4a8_linear,
     check_decode_loop_greedy, check_decode_loop_sampling_marginal,
 ]

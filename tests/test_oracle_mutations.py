@@ -21,10 +21,13 @@ MUTATIONS = [
     ("group scale tiled instead of repeated", "scale = np.repeat(S.astype(np.float64), GROUP, axis=1)",
      "scale = np.tile(S.astype(np.float64), (1, GROUP))"),
     ("w4a16 transposed operand", "return x @ Wd.T", "return (Wd @ x.T)"),
-    ("activation divisor 8", "s_a = (amax / np.float32(7.0)).astype(np.float32)",
-     "s_a = (amax / np.float32(8.0)).astype(np.float32)"),
-    ("activation scale rounded to fp16", "s_a = (amax / np.float32(7.0)).astype(np.float32)",
-     "s_a = (amax / np.float32(7.0)).astype(np.float16).astype(np.float32)"),
+    ("activation divisor a power of two", "qmax = 2 ** (bits - 1) - 1", "qmax = 2 ** (bits - 1)"),
+    ("activation scale rounded to fp16", "s_a = (amax / np.float32(qmax)).astype(np.float32)",
+     "s_a = (amax / np.float32(qmax)).astype(np.float16).astype(np.float32)"),
+    ("activation codes clamped asymmetrically", "np.clip(np.rint(x[m] / s_a[m]), -qmax - 1, qmax)",
+     "np.clip(np.rint(x[m] / s_a[m]), -qmax, qmax - 1)"),
+    ("W4A8 quantises to 4 bits", "return linear_w4a4(x_bits, Wp, S, rows, bits=8)",
+     "return linear_w4a4(x_bits, Wp, S, rows, bits=4)"),
     ("w4a4 drops the token scale", "y = s_a.astype(np.float64)[:, None] * np.einsum",
      "y = 1.0 * np.einsum"),
     ("w4a4 groups strided", 'acc = np.einsum("mgk,ngk->mng", qa.reshape(M, G, GROUP), codes.reshape(N, G, GROUP))',

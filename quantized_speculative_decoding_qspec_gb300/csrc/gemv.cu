@@ -38,6 +38,7 @@ namespace {
 
 constexpr int kThreads = 512;  // 16 warps, one CTA per SM
 constexpr int kWarps = kThreads / 32;
+constexpr int kStageU = 4;  // 16-byte activation chunks a thread loads per staging batch
 
 // 16 bytes of packed weights, read once: not kept in L1
 __device__ __forceinline__ uint4 ld_weights(const void* p) {
@@ -98,8 +99,9 @@ template <int QB, bool ACC, int MT, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ Wp, const __half* __restrict__ S,
                 int M, int N, int K, int KS, uint16_t* __restrict__ y, int8_t* __restrict__ xq_out,
-                float* __restrict__ xs_out, int32_t* __restrict__ acc_out) {
+                float* __restrict__ xs_out, int32_t* __restrict__ acc_out, const float* __restrict__ s_a_in) {
   constexpr bool A4 = QB != 0;                       // activations quantised (W4A4 or W4A8)
+  constexpr bool QUANT = QB == 4 || QB == 8;         // ... here (QB == 1: x holds codes, s_a_in scales)
   constexpr float kQmax = QB == 8 ? 127.0f : 7.0f;   // codes in [-kQmax - 1, kQmax]
   extern __shared__ __align__(16) uint8_t sm[];
   const int G = K / kGroup;
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint4* xs = reinterpret_cast<uint4*>(sm);
   constexpr int NB = (MT + 7) / 8;
   float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(G) * 16 * MT);  // [2][kWarps][NB][32]
-  __shared__ unsigned int red_max[A4 ? kWarps * MT : 1];
+  __shared__ unsigned int red_max[QUANT ? kWarps * MT : 1];
   __shared__ float s_a[MT], s_r[MT];  // per-token scale and its reciprocal (rounded to nearest)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // which W4A4 then keeps in registers between its two passes).
   const int per_token = G * 16;
   const int total = M * per_token;
-  constexpr int kU = 4;
+  constexpr int kU = kStageU;
   auto locate = [&](int c, int& m, int& v) {
     m = c / per_token;
     v = c - m * per_token;  // (gi * 4 + j) * 4 + t
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                max(max(val.z & 0x7FFFu, (val.z >> 16) & 0x7FFFu), max(val.w & 0x7FFFu, (val.w >> 16) & 0x7FFFu)));
   };
   // per-token amax (bf16 bit patterns of |x| order like the values) -> s_a = amax / 7, 1 / s_a
-  unsigned int mx[A4 ? MT : 1];
+  unsigned int mx[QUANT ? MT : 1];
   auto amax_add = [&](int m, uint4 val) {
     const unsigned int am = chunk_amax(val);
 #pragma unroll
@@ -237,15 +239,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
   };
-  if constexpr (A4) {
+  if constexpr (QUANT) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) mx[m] = 0;
+  }
+  if constexpr (QB == 1) {
+    if (threadIdx.x < M) s_a[threadIdx.x] = s_a_in[threadIdx.x];
   }
   uint4 u[kU];
   if (total <= kU * kThreads) {
     // one batch: x stays in registers between the passes
     load_batch(threadIdx.x, u);
-    if constexpr (A4) {
+    if constexpr (QUANT) {
 #pragma unroll
       for (int e = 0; e < kU; ++e) {
         const int c = threadIdx.x + e * kThreads;
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c >= total) continue;
       int m, v;
       locate(c, m, v);
-      xs[slot_of(m, v)] = A4 ? quantise(m, v, u[e]) : u[e];
+      xs[slot_of(m, v)] = QUANT ? quantise(m, v, u[e]) : u[e];
     }
   } else {
     // several batches: x goes to shared memory as it is, W4A4 then works there (no second trip
@@ -273,10 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int m, v;
         locate(c, m, v);
         xs[slot_of(m, v)] = u[e];
-        if constexpr (A4) amax_add(m, u[e]);
+        if constexpr (QUANT) amax_add(m, u[e]);
       }
     }
-    if constexpr (A4) {
+    if constexpr (QUANT) {
       finish_scales();
       for (int c = threadIdx.x; c < total; c += kThreads) {
         int m, v;
@@ -396,6 +401,7 @@ struct Outs {
   int8_t* xq;
   float* xs;
   int32_t* acc;
+  const float* s_in;  // codes mode: the per-token scales of the staged codes
 };
 
 template <int QB, bool ACC, int MT, int D>
@@ -415,7 +421,7 @@ qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, y, o.xq, o.xs, o.acc) == cudaSuccess
+  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, y, o.xq, o.xs, o.acc, o.s_in) == cudaSuccess
              ? QSPEC_OK
              : QSPEC_ERR_CUDA;
 }
@@ -467,23 +473,36 @@ bool gemv_supported(int M, int N, int K) {
 }
 
 template <int MT>
-qspec_status launch_mode(int abits, const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K,
+qspec_status launch_mode(int qb, const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K,
                          uint16_t* y, Outs o, cudaStream_t stream) {
-  if (abits == 4) return launch<4, MT>(x, Wp, S, M, N, K, y, o, stream);
-  if (abits == 8) return launch<8, MT>(x, Wp, S, M, N, K, y, o, stream);
+  if (qb == 4) return launch<4, MT>(x, Wp, S, M, N, K, y, o, stream);
+  if (qb == 8) return launch<8, MT>(x, Wp, S, M, N, K, y, o, stream);
+  if (qb == 1) return launch<1, MT>(x, Wp, S, M, N, K, y, o, stream);
   return launch<0, MT>(x, Wp, S, M, N, K, y, o, stream);
 }
 
 qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
-                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream) {
+                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, cudaStream_t stream) {
   const __half* Sh = reinterpret_cast<const __half*>(S);
-  const Outs o{xq_out, xs_out, acc_out};
+  Outs o{xq_out, xs_out, acc_out, nullptr};
+  int qb = abits == 16 ? 0 : abits;
+  // Tokens that take several staging batches would be quantised by every CTA from shared memory;
+  // there the quantiser runs once, in its own kernel, and the GEMV stages the codes.
+  uint16_t* codes = nullptr;
+  float* s_a = nullptr;
+  if (qb != 0 && static_cast<long long>(M) * K > 8LL * kStageU * kThreads && ws_codes(abits, M, N, K, ws, &codes, &s_a)) {
+    const qspec_status st = quantise_tokens(abits, x, M, K, codes, s_a, xq_out, xs_out, stream);
+    if (st != QSPEC_OK) return st;
+    x = codes;
+    o = Outs{nullptr, nullptr, acc_out, s_a};
+    qb = 1;
+  }
   switch (token_slots(M)) {
-    case 1: return launch_mode<1>(abits, x, Wp, Sh, M, N, K, y, o, stream);
-    case 2: return launch_mode<2>(abits, x, Wp, Sh, M, N, K, y, o, stream);
-    case 4: return launch_mode<4>(abits, x, Wp, Sh, M, N, K, y, o, stream);
-    case 8: return launch_mode<8>(abits, x, Wp, Sh, M, N, K, y, o, stream);
-    default: return launch_mode<16>(abits, x, Wp, Sh, M, N, K, y, o, stream);
+    case 1: return launch_mode<1>(qb, x, Wp, Sh, M, N, K, y, o, stream);
+    case 2: return launch_mode<2>(qb, x, Wp, Sh, M, N, K, y, o, stream);
+    case 4: return launch_mode<4>(qb, x, Wp, Sh, M, N, K, y, o, stream);
+    case 8: return launch_mode<8>(qb, x, Wp, Sh, M, N, K, y, o, stream);
+    default: return launch_mode<16>(qb, x, Wp, Sh, M, N, K, y, o, stream);
   }
 }
 

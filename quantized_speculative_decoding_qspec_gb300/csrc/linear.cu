@@ -223,7 +223,7 @@ extern "C" qspec_status qspec_linear_w4a16(const uint16_t* x, const uint8_t* Wp,
   if (!qspec::aligned16(ws)) return QSPEC_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (qspec::gemv_supported(int(M), int(N), int(K)))
-    return qspec::gemv(16, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, s);
+    return qspec::gemv(16, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, ws, s);
   if (qspec::linear_tc_supported(16, int(M), int(N), int(K)))
     return qspec::linear_tc(16, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, ws, ws_bytes, s);
   return qspec::linear_simt(16, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, s);
@@ -243,7 +243,7 @@ qspec_status linear_quantised(int abits, const uint16_t* x, const uint8_t* Wp, c
   if (!qspec::aligned16(ws)) return QSPEC_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (qspec::gemv_supported(int(M), int(N), int(K)))
-    return qspec::gemv(abits, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, s);
+    return qspec::gemv(abits, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, ws, s);
   if (qspec::linear_tc_supported(abits, int(M), int(N), int(K)))
     return qspec::linear_tc(abits, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, ws, ws_bytes, s);
   return qspec::linear_simt(abits, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, s);

@@ -22,10 +22,17 @@ qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const ui
                        int N, int K, uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out,
                        void* ws, size_t ws_bytes, cudaStream_t stream);
 
+// The per-token quantiser as its own kernel (one CTA per token): bf16 codes [M, K] and fp32 scales
+// [M], plus the optional int8 codes and scales out.  ws_codes gives the workspace's code and scale
+// buffers for a quantised mode (false for W4A16).
+qspec_status quantise_tokens(int abits, const uint16_t* x, int M, int K, uint16_t* codes, float* s_a,
+                             int8_t* xq_out, float* xs_out, cudaStream_t stream);
+bool ws_codes(int abits, int M, int N, int K, void* ws, uint16_t** codes, float** s_a);
+
 // Register-fragment MMA GEMV for every mode at decode sizes (M <= 16; the staged activations must fit).
 bool gemv_supported(int M, int N, int K);
 qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
-                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, cudaStream_t stream);
+                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, cudaStream_t stream);
 
 // Reads (synchronously) and clears the error bits the linear kernels set on the current device.
 qspec_status read_and_clear_linear_error(cudaStream_t stream, unsigned int* bits);

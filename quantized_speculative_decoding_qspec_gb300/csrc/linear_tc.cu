@@ -789,7 +789,9 @@ WsLayout ws_layout(int abits, int M, int N, int K, int P) {
   size_t off = 0;
   L.ticket = off;  off = al256(off + sizeof(unsigned int) * T);
   L.partial = off; off = al256(off + sizeof(float) * size_t(P) * 2 * 128 * NM);
-  const bool codes = codes_mode_of(abits, M);
+  // quantised codes and scales: used by the codes mode here, and by the GEMV when it quantises
+  // the tokens in a separate kernel
+  const bool codes = abits != 16;
   L.codes = off;   off = al256(off + (codes ? sizeof(uint16_t) * size_t(M) * K : 0));
   L.s_a = off;     off = al256(off + (codes ? sizeof(float) * size_t(M) : 0));
   L.total = off;
@@ -856,18 +858,8 @@ qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const ui
     return QSPEC_ERR_CUDA;
 
   if (codes_mode) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(M);
-    cfg.blockDim = dim3(256);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const float qmax = abits == 8 ? 127.0f : 7.0f;
-    if (cudaLaunchKernelEx(&cfg, act_quant_kernel, x, K, qmax, codes, s_a, xq_out, xs_out) != cudaSuccess)
-      return QSPEC_ERR_CUDA;
+    const qspec_status st = quantise_tokens(abits, x, M, K, codes, s_a, xq_out, xs_out, stream);
+    if (st != QSPEC_OK) return st;
   }
 
   TcArgs args;
@@ -903,6 +895,31 @@ qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const ui
     case 48: return launch_tc<48, kA4Codes>(tmW, tmX, args, P, stream);
     default: return launch_tc<64, kA4Codes>(tmW, tmX, args, P, stream);
   }
+}
+
+bool ws_codes(int abits, int M, int N, int K, void* ws, uint16_t** codes, float** s_a) {
+  if (abits == 16 || !ws) return false;
+  const WsLayout L = ws_layout(abits, M, N, K, num_sms());
+  *codes = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + L.codes);
+  *s_a = reinterpret_cast<float*>(static_cast<char*>(ws) + L.s_a);
+  return true;
+}
+
+qspec_status quantise_tokens(int abits, const uint16_t* x, int M, int K, uint16_t* codes, float* s_a,
+                             int8_t* xq_out, float* xs_out, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(M);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float qmax = abits == 8 ? 127.0f : 7.0f;
+  return cudaLaunchKernelEx(&cfg, act_quant_kernel, x, K, qmax, codes, s_a, xq_out, xs_out) == cudaSuccess
+             ? QSPEC_OK
+             : QSPEC_ERR_CUDA;
 }
 
 qspec_status read_and_clear_linear_error(cudaStream_t stream, unsigned int* bits) {

@@ -486,11 +486,13 @@ qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_
   const __half* Sh = reinterpret_cast<const __half*>(S);
   Outs o{xq_out, xs_out, acc_out, nullptr};
   int qb = abits == 16 ? 0 : abits;
-  // Tokens that take several staging batches would be quantised by every CTA from shared memory;
-  // there the quantiser runs once, in its own kernel, and the GEMV stages the codes.
+  // Eight or more tokens that take several staging batches would be quantised by every CTA from
+  // shared memory; there the quantiser runs once, in its own kernel (one CTA per token), and the
+  // GEMV stages the codes.  With fewer tokens that kernel has too few CTAs to pay off (measured).
   uint16_t* codes = nullptr;
   float* s_a = nullptr;
-  if (qb != 0 && static_cast<long long>(M) * K > 8LL * kStageU * kThreads && ws_codes(abits, M, N, K, ws, &codes, &s_a)) {
+  if (qb != 0 && M >= 8 && static_cast<long long>(M) * K > 8LL * kStageU * kThreads &&
+      ws_codes(abits, M, N, K, ws, &codes, &s_a)) {
     const qspec_status st = quantise_tokens(abits, x, M, K, codes, s_a, xq_out, xs_out, stream);
     if (st != QSPEC_OK) return st;
     x = codes;

@@ -98,17 +98,23 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 template <int QB, bool ACC, int MT, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ Wp, const __half* __restrict__ S,
-                int M, int N, int K, int KS, uint16_t* __restrict__ y, int8_t* __restrict__ xq_out,
-                float* __restrict__ xs_out, int32_t* __restrict__ acc_out, const float* __restrict__ s_a_in) {
+                int M, int N, int K, int KS, int KC, uint16_t* __restrict__ y, int8_t* __restrict__ xq_out,
+                float* __restrict__ xs_out, int32_t* __restrict__ acc_out, const float* __restrict__ s_a_in,
+                float* __restrict__ part, unsigned int* __restrict__ tick) {
   constexpr bool A4 = QB != 0;                       // activations quantised (W4A4 or W4A8)
   constexpr bool QUANT = QB == 4 || QB == 8;         // ... here (QB == 1: x holds codes, s_a_in scales)
   constexpr float kQmax = QB == 8 ? 127.0f : 7.0f;   // codes in [-kQmax - 1, kQmax]
   extern __shared__ __align__(16) uint8_t sm[];
   const int G = K / kGroup;
-  // activations: chunk ((gi * 4 + j) * MT + m) * 4 + t holds x[m, 128 gi + 32 t + 8 j .. + 7]
+  // K chunks: CTA c works on groups [gb, gb + Gc) of chunk kc = c % KC (KC = 1 unless the staged
+  // activations of all K would not fit shared memory); the KC partial tiles are summed by the
+  // chunk that finishes last
+  const int kc = blockIdx.x % KC, cb = blockIdx.x / KC;
+  const int Gc = G / KC, gb = kc * Gc;
+  // activations: chunk ((gi * 4 + j) * MT + m) * 4 + t holds x[m, 128 (gb + gi) + 32 t + 8 j .. + 7]
   uint4* xs = reinterpret_cast<uint4*>(sm);
   constexpr int NB = (MT + 7) / 8;
-  float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(G) * 16 * MT);  // [2][kWarps][NB][32]
+  float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(Gc) * 16 * MT);  // [2][kWarps][NB][32]
   __shared__ unsigned int red_max[QUANT ? kWarps * MT : 1];
   __shared__ float s_a[MT], s_r[MT];  // per-token scale and its reciprocal (rounded to nearest)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -117,9 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles = (N + 15) / 16;
   const int per_cta = kWarps / KS;  // row tiles a CTA works on at once
   const int wtile = warp / KS, ks = warp - wtile * KS;
-  const int gs = G / KS, g_beg = ks * gs;
-  const int stride = gridDim.x * per_cta;
-  const int tile0 = blockIdx.x * per_cta + wtile;
+  const int gs = Gc / KS, g_beg = ks * gs;  // this warp's groups within the chunk
+  const int stride = (gridDim.x / KC) * per_cta;
+  const int tile0 = cb * per_cta + wtile;
   const int rounds = (tiles + stride - 1) / stride;  // the same for the KS warps of a tile slot
   const size_t row_bytes = static_cast<size_t>(K) / 2;
 
@@ -134,10 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_lo = f_tile * 16 + g, n_hi = n_lo + 8;
     f_vlo = f_tile < tiles && n_lo < N;
     f_vhi = f_tile < tiles && n_hi < N;
-    f_wlo = Wp + static_cast<size_t>(f_vlo ? n_lo : 0) * row_bytes + g_beg * 64 + t * 16;
-    f_whi = Wp + static_cast<size_t>(f_vhi ? n_hi : 0) * row_bytes + g_beg * 64 + t * 16;
-    f_slo = S + static_cast<size_t>(f_vlo ? n_lo : 0) * G + g_beg;
-    f_shi = S + static_cast<size_t>(f_vhi ? n_hi : 0) * G + g_beg;
+    f_wlo = Wp + static_cast<size_t>(f_vlo ? n_lo : 0) * row_bytes + (gb + g_beg) * 64 + t * 16;
+    f_whi = Wp + static_cast<size_t>(f_vhi ? n_hi : 0) * row_bytes + (gb + g_beg) * 64 + t * 16;
+    f_slo = S + static_cast<size_t>(f_vlo ? n_lo : 0) * G + gb + g_beg;
+    f_shi = S + static_cast<size_t>(f_vhi ? n_hi : 0) * G + gb + g_beg;
   };
   uint4 wl[D], wh[D];
   float sl[D], sh[D];
@@ -163,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // M..MT-1 are never written: they only feed MMA columns that are not stored.  A thread loads its
   // kU chunks before using any, so one L2 round trip covers them (all of x, for the usual sizes,
   // which W4A4 then keeps in registers between its two passes).
-  const int per_token = G * 16;
+  const int per_token = Gc * 16;
   const int total = M * per_token;
   constexpr int kU = kStageU;
   auto locate = [&](int c, int& m, int& v) {
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto src_of = [&](int m, int v) {
     const int t_ = v & 3, j_ = (v >> 2) & 3, gi = v >> 4;
-    return static_cast<size_t>(m) * K + gi * 128 + t_ * 32 + j_ * 8;
+    return static_cast<size_t>(m) * K + (gb + gi) * 128 + t_ * 32 + j_ * 8;
   };
   auto load_batch = [&](int c0, uint4 (&u)[kU]) {
 #pragma unroll
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      ((static_cast<uint32_t>(static_cast<int>(c1f)) & 0xFFu) << 8))
                     << (16 * (i & 1));
     }
-    if (xq_out && blockIdx.x == 0) *reinterpret_cast<uint2*>(xq_out + src_of(m, v)) = make_uint2(q8[0], q8[1]);
+    if (xq_out && cb == 0) *reinterpret_cast<uint2*>(xq_out + src_of(m, v)) = make_uint2(q8[0], q8[1]);
     return make_uint4(w[0], w[1], w[2], w[3]);
   };
   auto chunk_amax = [](uint4 val) {
@@ -243,6 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int m = 0; m < MT; ++m) mx[m] = 0;
   }
+  // a chunked CTA stages part of K but needs the amax over all of it: one extra read of x
+  auto amax_full = [&]() {
+    const int n16 = K / 8;
+    for (int c = threadIdx.x; c < M * n16; c += kThreads) {
+      const int m = c / n16;
+      amax_add(m, __ldg(reinterpret_cast<const uint4*>(x) + c));
+    }
+  };
   if constexpr (QB == 1) {
     if (threadIdx.x < M) s_a[threadIdx.x] = s_a_in[threadIdx.x];
   }
@@ -251,10 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one batch: x stays in registers between the passes
     load_batch(threadIdx.x, u);
     if constexpr (QUANT) {
+      if (KC == 1) {
 #pragma unroll
-      for (int e = 0; e < kU; ++e) {
-        const int c = threadIdx.x + e * kThreads;
-        if (c < total) amax_add(c / per_token, u[e]);
+        for (int e = 0; e < kU; ++e) {
+          const int c = threadIdx.x + e * kThreads;
+          if (c < total) amax_add(c / per_token, u[e]);
+        }
+      } else {
+        amax_full();
       }
       finish_scales();
     }
@@ -278,10 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int m, v;
         locate(c, m, v);
         xs[slot_of(m, v)] = u[e];
-        if constexpr (QUANT) amax_add(m, u[e]);
+        if constexpr (QUANT) {
+          if (KC == 1) amax_add(m, u[e]);
+        }
       }
     }
     if constexpr (QUANT) {
+      if (KC > 1) amax_full();
       finish_scales();
       for (int c = threadIdx.x; c < total; c += kThreads) {
         int m, v;
@@ -334,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (A4 && ACC) {
           if (tile < tiles) {  // exact integer group sums
-            const int n_lo = tile * 16 + g, n_hi = n_lo + 8, gi = g_beg + i0 + k;
+            const int n_lo = tile * 16 + g, n_hi = n_lo + 8, gi = gb + g_beg + i0 + k;
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
               const int m0 = nb * 8 + 2 * t, m1 = m0 + 1;
@@ -372,7 +393,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (ks == 0 && tile < tiles) {
+    bool store = ks == 0 && tile < tiles;
+    if (store && KC > 1) {
+      // publish this chunk's partial tile; the chunk that arrives last sums all KC in chunk order
+      float4* pp = reinterpret_cast<float4*>(part);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+        pp[((static_cast<size_t>(kc) * tiles + tile) * NB + nb) * 32 + lane] =
+            make_float4(acc[nb][0], acc[nb][1], acc[nb][2], acc[nb][3]);
+      __threadfence();
+      unsigned int prev = 0;
+      if (lane == 0) prev = atomicAdd(tick + tile, 1u);
+      prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+      store = prev == static_cast<unsigned int>(KC - 1);
+      if (store) {
+        __threadfence();
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int kk = 0; kk < KC; ++kk) {
+            const float4 o = __ldcg(pp + ((static_cast<size_t>(kk) * tiles + tile) * NB + nb) * 32 + lane);
+            s4.x += o.x;
+            s4.y += o.y;
+            s4.z += o.z;
+            s4.w += o.w;
+          }
+          acc[nb][0] = s4.x;
+          acc[nb][1] = s4.y;
+          acc[nb][2] = s4.z;
+          acc[nb][3] = s4.w;
+        }
+        if (lane == 0) tick[tile] = 0;
+      }
+    }
+    if (store) {
       const int n_lo = tile * 16 + g, n_hi = n_lo + 8;
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
@@ -393,21 +447,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-size_t smem_bytes(int MT, int K) {
-  return static_cast<size_t>(K / kGroup) * 16 * MT * 16 + 2 * static_cast<size_t>(kWarps) * ((MT + 7) / 8) * 32 * 16;
+// dynamic shared memory for MT token slots over Gc staged groups
+size_t smem_bytes(int MT, int Gc) {
+  return static_cast<size_t>(Gc) * 16 * MT * 16 + 2 * static_cast<size_t>(kWarps) * ((MT + 7) / 8) * 32 * 16;
+}
+constexpr size_t kSmemCap = 200 * 1024;
+
+// K chunks across CTAs: the fewest (a divisor of the group count) whose staged activations fit
+// shared memory; 0 if none does.
+int pick_kc(int MT, int G) {
+  for (int kc = 1; kc <= G; ++kc)
+    if (G % kc == 0 && smem_bytes(MT, G / kc) <= kSmemCap) return kc;
+  return 0;
+}
+
+inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace bytes of the chunk partials and tile tickets (0 when K is not chunked).
+size_t chunk_ws_bytes(int MT, int N, int G, int KC) {
+  if (KC <= 1) return 0;
+  const size_t tiles = (static_cast<size_t>(N) + 15) / 16;
+  return al256(static_cast<size_t>(KC) * tiles * ((MT + 7) / 8) * 32 * 16) + al256(tiles * sizeof(unsigned int));
 }
 
 struct Outs {
   int8_t* xq;
   float* xs;
   int32_t* acc;
-  const float* s_in;  // codes mode: the per-token scales of the staged codes
+  const float* s_in;     // codes mode: the per-token scales of the staged codes
+  float* part;           // K chunks: [KC][tiles][NB][32] float4 partial tiles
+  unsigned int* tick;    // K chunks: [tiles] arrival counters (zero between calls)
 };
 
 template <int QB, bool ACC, int MT, int D>
 qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
-                      Outs o, int best_ks, int best_grid, cudaStream_t stream) {
-  const size_t smem = smem_bytes(MT, K);
+                      Outs o, int best_ks, int KC, int best_grid, cudaStream_t stream) {
+  const size_t smem = smem_bytes(MT, K / kGroup / KC);
   auto kern = gemv_kernel<QB, ACC, MT, D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return QSPEC_ERR_CUDA;
@@ -421,45 +496,57 @@ qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, y, o.xq, o.xs, o.acc, o.s_in) == cudaSuccess
+  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, KC, y, o.xq, o.xs, o.acc, o.s_in, o.part,
+                            o.tick) == cudaSuccess
              ? QSPEC_OK
              : QSPEC_ERR_CUDA;
 }
 
 template <int QB, int MT>
 qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
-                    Outs o, cudaStream_t stream) {
-  const int G = K / kGroup;
+                    Outs o, int KC, cudaStream_t stream) {
+  const int Gc = K / kGroup / KC;
   const long long tiles = (static_cast<long long>(N) + 15) / 16;
-  const int sms = num_sms();
-  // K split: the fewest rounds of (groups per slice + fixed cost), ties to the wider grid
+  const int chunk_grids = std::max(1, num_sms() / KC);  // CTAs per K chunk
+  // K split among a CTA's warps: the fewest rounds of (groups per slice + fixed cost), ties to
+  // the wider grid
   int best_ks = 1, best_grid = 1;
   long long best_cost = -1;
   for (int ks = 1; ks <= kWarps; ks *= 2) {
-    if (G % ks != 0) continue;
+    if (Gc % ks != 0) continue;
     const long long slots = kWarps / ks;
-    const int grid = static_cast<int>(std::min<long long>(sms, (tiles + slots - 1) / slots));
+    const int grid = static_cast<int>(std::min<long long>(chunk_grids, (tiles + slots - 1) / slots));
     const long long rounds = (tiles + grid * slots - 1) / (grid * slots);
-    const long long cost = rounds * (G / ks + 2);
+    const long long cost = rounds * (Gc / ks + 2);
     if (best_cost < 0 || cost < best_cost || (cost == best_cost && grid > best_grid)) {
       best_cost = cost;
       best_ks = ks;
       best_grid = grid;
     }
   }
-  const int gs = G / best_ks;
+  best_grid *= KC;
+  const int gs = Gc / best_ks;
   if constexpr (QB != 0) {
     if (o.acc) {  // the checking path: group sums out, no need for the deepest prefetch
-      if (gs % 2 == 0) return launch_d<QB, true, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
-      return launch_d<QB, true, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+      if (gs % 2 == 0) return launch_d<QB, true, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+      return launch_d<QB, true, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
     }
   }
   // (16 token slots keep two column blocks of accumulators: at most two groups in flight then)
   if constexpr (MT < 16) {
-    if (gs % 4 == 0) return launch_d<QB, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+    if (gs % 4 == 0) return launch_d<QB, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
   }
-  if (gs % 2 == 0) return launch_d<QB, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
-  return launch_d<QB, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, best_grid, stream);
+  if (gs % 2 == 0) return launch_d<QB, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+  return launch_d<QB, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+}
+
+template <int MT>
+qspec_status launch_mode(int qb, const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K,
+                         uint16_t* y, Outs o, int KC, cudaStream_t stream) {
+  if (qb == 4) return launch<4, MT>(x, Wp, S, M, N, K, y, o, KC, stream);
+  if (qb == 8) return launch<8, MT>(x, Wp, S, M, N, K, y, o, KC, stream);
+  if (qb == 1) return launch<1, MT>(x, Wp, S, M, N, K, y, o, KC, stream);
+  return launch<0, MT>(x, Wp, S, M, N, K, y, o, KC, stream);
 }
 
 }  // namespace
@@ -469,22 +556,28 @@ int token_slots(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 
 
 bool gemv_supported(int M, int N, int K) {
   if (M < 1 || M > 16 || N < 1 || K % kGroup != 0) return false;
-  return smem_bytes(token_slots(M), K) <= 200 * 1024;
+  return pick_kc(token_slots(M), K / kGroup) > 0;
 }
 
-template <int MT>
-qspec_status launch_mode(int qb, const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K,
-                         uint16_t* y, Outs o, cudaStream_t stream) {
-  if (qb == 4) return launch<4, MT>(x, Wp, S, M, N, K, y, o, stream);
-  if (qb == 8) return launch<8, MT>(x, Wp, S, M, N, K, y, o, stream);
-  if (qb == 1) return launch<1, MT>(x, Wp, S, M, N, K, y, o, stream);
-  return launch<0, MT>(x, Wp, S, M, N, K, y, o, stream);
+size_t gemv_workspace_bytes(int M, int N, int K) {
+  if (!gemv_supported(M, N, K)) return 0;
+  const int MT = token_slots(M), G = K / kGroup;
+  return chunk_ws_bytes(MT, N, G, pick_kc(MT, G));
 }
 
 qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
                   uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, cudaStream_t stream) {
   const __half* Sh = reinterpret_cast<const __half*>(S);
-  Outs o{xq_out, xs_out, acc_out, nullptr};
+  const int MT = token_slots(M), G = K / kGroup;
+  const int KC = pick_kc(MT, G);
+  if (KC == 0) return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  Outs o{xq_out, xs_out, acc_out, nullptr, nullptr, nullptr};
+  if (KC > 1) {  // chunk partials and tickets live after the tensor-core path's regions
+    char* base = static_cast<char*>(ws) + al256(linear_tc_workspace_size_all(M, N, K));
+    const size_t tiles = (static_cast<size_t>(N) + 15) / 16;
+    o.part = reinterpret_cast<float*>(base);
+    o.tick = reinterpret_cast<unsigned int*>(base + al256(static_cast<size_t>(KC) * tiles * ((MT + 7) / 8) * 512));
+  }
   int qb = abits == 16 ? 0 : abits;
   // Eight or more tokens that take several staging batches would be quantised by every CTA from
   // shared memory; there the quantiser runs once, in its own kernel (one CTA per token), and the
@@ -496,15 +589,17 @@ qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_
     const qspec_status st = quantise_tokens(abits, x, M, K, codes, s_a, xq_out, xs_out, stream);
     if (st != QSPEC_OK) return st;
     x = codes;
-    o = Outs{nullptr, nullptr, acc_out, s_a};
+    o.xq = nullptr;
+    o.xs = nullptr;
+    o.s_in = s_a;
     qb = 1;
   }
-  switch (token_slots(M)) {
-    case 1: return launch_mode<1>(qb, x, Wp, Sh, M, N, K, y, o, stream);
-    case 2: return launch_mode<2>(qb, x, Wp, Sh, M, N, K, y, o, stream);
-    case 4: return launch_mode<4>(qb, x, Wp, Sh, M, N, K, y, o, stream);
-    case 8: return launch_mode<8>(qb, x, Wp, Sh, M, N, K, y, o, stream);
-    default: return launch_mode<16>(qb, x, Wp, Sh, M, N, K, y, o, stream);
+  switch (MT) {
+    case 1: return launch_mode<1>(qb, x, Wp, Sh, M, N, K, y, o, KC, stream);
+    case 2: return launch_mode<2>(qb, x, Wp, Sh, M, N, K, y, o, KC, stream);
+    case 4: return launch_mode<4>(qb, x, Wp, Sh, M, N, K, y, o, KC, stream);
+    case 8: return launch_mode<8>(qb, x, Wp, Sh, M, N, K, y, o, KC, stream);
+    default: return launch_mode<16>(qb, x, Wp, Sh, M, N, K, y, o, KC, stream);
   }
 }
 

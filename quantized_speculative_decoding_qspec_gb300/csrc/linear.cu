@@ -206,12 +206,8 @@ extern "C" size_t qspec_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0 || M > QSPEC_MAX_M || N % 8 != 0 || K % qspec::kGroup != 0 ||
       N > (int64_t(1) << 30) || K > (int64_t(1) << 30))
     return 0;
-  size_t n = 0;
-  for (int abits : {16, 4, 8}) {
-    const size_t b = qspec::linear_tc_workspace_size(abits, int(M), int(N), int(K));
-    if (b > n) n = b;
-  }
-  return n;
+  const size_t tc = qspec::linear_tc_workspace_size_all(int(M), int(N), int(K));
+  return ((tc + 255) & ~size_t(255)) + qspec::gemv_workspace_bytes(int(M), int(N), int(K));
 }
 
 extern "C" qspec_status qspec_linear_w4a16(const uint16_t* x, const uint8_t* Wp, const uint16_t* S,

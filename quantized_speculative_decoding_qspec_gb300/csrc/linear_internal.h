@@ -29,8 +29,14 @@ qspec_status quantise_tokens(int abits, const uint16_t* x, int M, int K, uint16_
                              int8_t* xq_out, float* xs_out, cudaStream_t stream);
 bool ws_codes(int abits, int M, int N, int K, void* ws, uint16_t** codes, float** s_a);
 
-// Register-fragment MMA GEMV for every mode at decode sizes (M <= 16; the staged activations must fit).
+// The largest tensor-core workspace over the three modes for one shape (the GEMV's own regions
+// follow it).
+size_t linear_tc_workspace_size_all(int M, int N, int K);
+
+// Register-fragment MMA GEMV for every mode at decode sizes (M <= 16; K is split into chunks
+// across CTAs when the staged activations of all K do not fit shared memory).
 bool gemv_supported(int M, int N, int K);
+size_t gemv_workspace_bytes(int M, int N, int K);  // beyond linear_tc_workspace_size_all
 qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
                   uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, cudaStream_t stream);
 

@@ -897,6 +897,12 @@ qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const ui
   }
 }
 
+size_t linear_tc_workspace_size_all(int M, int N, int K) {
+  size_t n = 0;
+  for (int abits : {16, 4, 8}) n = std::max(n, linear_tc_workspace_size(abits, M, N, K));
+  return n;
+}
+
 bool ws_codes(int abits, int M, int N, int K, void* ws, uint16_t** codes, float** s_a) {
   if (abits == 16 || !ws) return false;
   const WsLayout L = ws_layout(abits, M, N, K, num_sms());

@@ -103,10 +103,12 @@ def test_linear_largest_k(q):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 64, 28672), (2, 136, 28672), (16, 256, 14336), (8, 200, 14336),
-                                   (12, 520, 4096)])
+                                   (12, 520, 4096), (4, 520, 28672), (3, 24, 28672), (16, 264, 8192),
+                                   (8, 136, 28672), (13, 40, 28672)])
 def test_linear_staging_widths(q, M, N, K):
-    # one- and two-token staging for long K, and the shapes whose activations do not fit the
-    # GEMV's shared memory (they take the tensor-core kernel)
+    # one- and two-token staging for long K, and the shapes whose staged activations do not fit
+    # the GEMV's shared memory in one piece (K split into 2, 4 or 8 chunks across CTAs, partial
+    # tiles summed by the last chunk; W4A4 with fewer than eight tokens reads all of x for amax)
     linear_case(q, M, N, K)
 
 

@@ -79,8 +79,8 @@ def peaks():
 # CUDA sources each kernel family's launches are built from (a change to any of them invalidates the
 # recorded DRAM traffic)
 KERNEL_SOURCES = {
-    "linear_w4a4": ["gemv.cu", "linear.cu", "common.cuh"],
-    "linear_w4a16": ["gemv.cu", "linear.cu", "common.cuh"],
+    "linear_w4a4": ["gemv.cu", "gemv_impl.cuh", "gemv_a4.cu", "linear.cu", "common.cuh"],
+    "linear_w4a16": ["gemv.cu", "gemv_impl.cuh", "gemv_a16.cu", "linear.cu", "common.cuh"],
     "verify_greedy": ["verify.cu", "common.cuh"],
     "verify_sample": ["verify.cu", "common.cuh"],
 }

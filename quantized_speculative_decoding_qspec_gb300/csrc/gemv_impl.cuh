@@ -1,0 +1,579 @@
+// Both linears at decode sizes (M = 1..16 tokens): register-resident weight fragments fed straight
+// into warp-level tensor-core MMAs.
+//
+// QSpec article ("QSpec実行時の2つの量子化による推論の一致率を調べる"), section
+// "W4A4 と W4A16 量子化": W4A16 keeps the 16-bit activations and converts the 4-bit weights while
+// multiplying; W4A4 also quantises the activations to 4 bits (per token here: s_a = amax / 7 in
+// fp32, codes = clamp(rint(x / s_a), -8, 7)).  Section "QSpec の W4A4 モードと W4A16 モード": both
+// modes read the same packed weights.  At decode sizes the product is a GEMV bound by the weight
+// stream (0.5 B per weight); the tcgen05 path would have to expand every weight to bf16 in TMEM
+// (4x the streamed bytes, written and read back on chip), which measured slower than the HBM stream
+// itself, so here the expanded weights never leave registers:
+//
+//  * a warp owns 16 weight rows x a K slice (x up to 16 tokens in two MMA column blocks of 8).  Lane (g, t) = (lane / 4, lane % 4) loads 16 bytes of
+//    each of its two rows g and g + 8 per 128-channel group: packed words 4t..4t+3, i.e. channels
+//    32t..32t+31 of the group;
+//  * one shift + LOP3 + bf16 subtract turns a nibble pair of a word into an exact bf16x2 code pair
+//    (the packed word keeps channels 2i and 2i+1 in nibbles i and i + 4), which is directly an A
+//    fragment register of mma.m16n8k16: the MMA's 16 k-slots of lane t are mapped onto the
+//    channels lane t holds (a fixed permutation of K inside the group), and the activations are
+//    staged in shared memory in exactly that order, so one 16-byte shared load gives the B
+//    fragments of two MMAs.  W4A4 stages the activation codes, as bf16 (exact), in the same place:
+//    every product and every 128-channel sum is then a small integer, exact in the fp32 MMA
+//    accumulator, so the group sums are the exact integer sums of code * code;
+//  * per group the fp32 MMA result is scaled by s[n, g] and accumulated in fp32; K slices of a
+//    tile are summed through shared memory in a fixed order; W4A4 multiplies by s_a at the end;
+//    y is rounded to bf16 once.
+//
+// Tokens are the MMA's N = 8 side (rows >= M are zero), weight rows its M = 16 side.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#pragma once
+
+#include "common.cuh"
+#include "linear_internal.h"
+
+namespace qspec {
+namespace gemv_impl {
+
+constexpr int kThreads = 512;  // 16 warps, one CTA per SM
+constexpr int kWarps = kThreads / 32;
+constexpr int kStageU = 4;  // 16-byte activation chunks a thread loads per staging batch
+
+// 16 bytes of packed weights, read once: not kept in L1
+__device__ __forceinline__ uint4 ld_weights(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// pair i of a packed word (channels 2i, 2i + 1 of its 8) -> exact bf16x2 codes
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
+  uint32_t v;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(v) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(0x43084308u));
+  const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v),
+                                   __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// a / b rounded to nearest (IEEE), given rb = 1 / b rounded to nearest: Markstein's division
+// refinement -- q0 = a * rb is within one ulp of a / b, the FMA gives the remainder a - b q0
+// exactly, and one more FMA rounds q0 + remainder * rb correctly.  That needs the remainder to be
+// representable: with b >= 2^-100 it is whenever |a / b| >= 1/4, the only quotients whose rounding
+// can change a code (smaller ones give code 0 either way).  The quantiser keeps the IEEE division
+// for smaller b.  Checked exhaustively against the IEEE division for every bf16 amax (b = amax / 7)
+// and every bf16 |a| <= amax: identical codes, identical quotients wherever |a / b| >= 1/4.
+__device__ __forceinline__ float div_rn_markstein(float a, float b, float rb) {
+  const float q0 = a * rb;
+  const float r = fmaf(-b, q0, a);
+  return fmaf(r, rb, q0);
+}
+
+// d += A (16 x 16, row fragments a0..a3) * B (16 x 8, column fragments b0, b1), fp32 accumulate
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// QB: activation bits of the quantised modes -- 4 (W4A4) or 8 (W4A8: the same per-token quantiser
+// with divisor 127 and codes in [-128, 127], a configuration the speculative-decoding-with-
+// quantisation summary on aibr.jp names in its section "中核となる技術的要素"), 0 for W4A16.  The
+// quantised modes quantise the tokens (optional int8 codes / fp32 scales out); ACC: also the int32 group
+// sums (a separate instantiation keeps their stores out of the hot loop when not asked for).
+// MT = token slots staged in shared memory (1, 2, 4, 8 or 16; tokens >= M contribute zeros); the
+// tokens form NB = ceil(MT / 8) MMA column blocks of 8 that share every weight fragment.  D = weight
+// groups in flight per warp (a divisor of the groups per K slice, so that register slots line up
+// with tile boundaries).
+//
+// A warp's work is one stream of (row tile, group) items: the tiles r * stride + blockIdx.x * per_cta
+// + wtile for r = 0, 1, ..., and within each its K slice of groups.  Weights are fetched D items
+// ahead across tile boundaries, so the stream never drains; the first fetches are issued before
+// the kernel waits for its predecessor (no library kernel that may run ahead of this one writes
+// packed weights or scales).
+template <int QB, bool ACC, int MT, int D, bool CHUNK>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ Wp, const __half* __restrict__ S,
+                int M, int N, int K, int KS, int KC_arg, uint16_t* __restrict__ y, int8_t* __restrict__ xq_out,
+                float* __restrict__ xs_out, int32_t* __restrict__ acc_out, const float* __restrict__ s_a_in,
+                float* __restrict__ part, unsigned int* __restrict__ tick) {
+  constexpr bool A4 = QB != 0;                       // activations quantised (W4A4 or W4A8)
+  constexpr bool QUANT = QB == 4 || QB == 8;         // ... here (QB == 1: x holds codes, s_a_in scales)
+  constexpr float kQmax = QB == 8 ? 127.0f : 7.0f;   // codes in [-kQmax - 1, kQmax]
+  extern __shared__ __align__(16) uint8_t sm[];
+  const int G = K / kGroup;
+  // K chunks: CTA c works on groups [gb, gb + Gc) of chunk kc = c % KC (KC = 1 unless the staged
+  // activations of all K would not fit shared memory); the KC partial tiles are summed by the
+  // chunk that finishes last
+  const int KC = CHUNK ? KC_arg : 1;  // (CHUNK: a separate instantiation, so KC == 1 costs nothing)
+  const int kc = blockIdx.x % KC, cb = blockIdx.x / KC;
+  const int Gc = G / KC, gb = kc * Gc;
+  // activations: chunk ((gi * 4 + j) * MT + m) * 4 + t holds x[m, 128 (gb + gi) + 32 t + 8 j .. + 7]
+  uint4* xs = reinterpret_cast<uint4*>(sm);
+  constexpr int NB = (MT + 7) / 8;
+  float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(Gc) * 16 * MT);  // [2][kWarps][NB][32]
+  __shared__ unsigned int red_max[QUANT ? kWarps * MT : 1];
+  __shared__ float s_a[MT], s_r[MT];  // per-token scale and its reciprocal (rounded to nearest)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+
+  const int tiles = (N + 15) / 16;
+  const int per_cta = kWarps / KS;  // row tiles a CTA works on at once
+  const int wtile = warp / KS, ks = warp - wtile * KS;
+  const int gs = Gc / KS, g_beg = ks * gs;  // this warp's groups within the chunk
+  const int stride = (gridDim.x / KC) * per_cta;
+  const int tile0 = cb * per_cta + wtile;
+  const int rounds = (tiles + stride - 1) / stride;  // the same for the KS warps of a tile slot
+  const size_t row_bytes = static_cast<size_t>(K) / 2;
+
+  // fetch cursor: the tile, its row pointers (at the slice's first group) and the group index
+  const uint8_t* f_wlo = Wp;
+  const uint8_t* f_whi = Wp;
+  const __half* f_slo = S;
+  const __half* f_shi = S;
+  bool f_vlo = false, f_vhi = false;
+  int f_tile = tile0, f_i = 0;
+  auto point = [&]() {
+    const int n_lo = f_tile * 16 + g, n_hi = n_lo + 8;
+    f_vlo = f_tile < tiles && n_lo < N;
+    f_vhi = f_tile < tiles && n_hi < N;
+    f_wlo = Wp + static_cast<size_t>(f_vlo ? n_lo : 0) * row_bytes + (gb + g_beg) * 64 + t * 16;
+    f_whi = Wp + static_cast<size_t>(f_vhi ? n_hi : 0) * row_bytes + (gb + g_beg) * 64 + t * 16;
+    f_slo = S + static_cast<size_t>(f_vlo ? n_lo : 0) * G + gb + g_beg;
+    f_shi = S + static_cast<size_t>(f_vhi ? n_hi : 0) * G + gb + g_beg;
+  };
+  uint4 wl[D], wh[D];
+  float sl[D], sh[D];
+  auto fetch = [&](int k) {  // next item of the stream into register slot k
+    wl[k] = f_vlo ? ld_weights(f_wlo + f_i * 64) : make_uint4(0, 0, 0, 0);
+    wh[k] = f_vhi ? ld_weights(f_whi + f_i * 64) : make_uint4(0, 0, 0, 0);
+    sl[k] = f_vlo ? __half2float(f_slo[f_i]) : 0.0f;
+    sh[k] = f_vhi ? __half2float(f_shi[f_i]) : 0.0f;
+    if (++f_i == gs) {
+      f_i = 0;
+      f_tile += stride;
+      point();
+    }
+  };
+  point();
+#pragma unroll
+  for (int k = 0; k < D; ++k) fetch(k);
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // Staging: chunk (gi, j, t) of token m <- x[m, 128 gi + 32 t + 8 j .. + 7].  Slots of tokens
+  // M..MT-1 are never written: they only feed MMA columns that are not stored.  A thread loads its
+  // kU chunks before using any, so one L2 round trip covers them (all of x, for the usual sizes,
+  // which W4A4 then keeps in registers between its two passes).
+  const int per_token = Gc * 16;
+  const int total = M * per_token;
+  constexpr int kU = kStageU;
+  auto locate = [&](int c, int& m, int& v) {
+    m = c / per_token;
+    v = c - m * per_token;  // (gi * 4 + j) * 4 + t
+  };
+  auto src_of = [&](int m, int v) {
+    const int t_ = v & 3, j_ = (v >> 2) & 3, gi = v >> 4;
+    return static_cast<size_t>(m) * K + (gb + gi) * 128 + t_ * 32 + j_ * 8;
+  };
+  auto load_batch = [&](int c0, uint4 (&u)[kU]) {
+#pragma unroll
+    for (int e = 0; e < kU; ++e) {
+      const int c = c0 + e * kThreads;
+      int m = 0, v = 0;
+      if (c < total) locate(c, m, v);
+      u[e] = c < total ? __ldg(reinterpret_cast<const uint4*>(x + src_of(m, v))) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto slot_of = [&](int m, int v) { return ((v >> 2) * MT + m) * 4 + (v & 3); };
+  // W4A4 / W4A8: codes = clamp(rint(x / s_a), -qmax - 1, qmax) of one chunk, as exact bf16 (and the
+  // int8 codes out)
+  auto quantise = [&](int m, int v, uint4 val) {
+    const float sa = s_a[m], rsa = s_r[m];
+    // see div_rn_markstein (checked for the 4-bit divisor; W4A8 keeps the IEEE division)
+    const bool fast = QB == 4 && sa >= 0x1p-100f;
+    uint32_t w[4] = {val.x, val.y, val.z, val.w};
+    uint32_t q8[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float c0f = 0.0f, c1f = 0.0f;
+      if (sa != 0.0f) {
+        const float x0 = bf16_lo(w[i]), x1 = bf16_hi(w[i]);
+        const float q0 = fast ? div_rn_markstein(x0, sa, rsa) : __fdiv_rn(x0, sa);
+        const float q1 = fast ? div_rn_markstein(x1, sa, rsa) : __fdiv_rn(x1, sa);
+        c0f = fminf(fmaxf(rintf(q0), -kQmax - 1.0f), kQmax);
+        c1f = fminf(fmaxf(rintf(q1), -kQmax - 1.0f), kQmax);
+      }
+      w[i] = static_cast<uint32_t>(f32_to_bf16_bits(c0f)) | (static_cast<uint32_t>(f32_to_bf16_bits(c1f)) << 16);
+      q8[i >> 1] |= ((static_cast<uint32_t>(static_cast<int>(c0f)) & 0xFFu) |
+                     ((static_cast<uint32_t>(static_cast<int>(c1f)) & 0xFFu) << 8))
+                    << (16 * (i & 1));
+    }
+    if (xq_out && cb == 0) *reinterpret_cast<uint2*>(xq_out + src_of(m, v)) = make_uint2(q8[0], q8[1]);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  };
+  auto chunk_amax = [](uint4 val) {
+    return max(max(max(val.x & 0x7FFFu, (val.x >> 16) & 0x7FFFu), max(val.y & 0x7FFFu, (val.y >> 16) & 0x7FFFu)),
+               max(max(val.z & 0x7FFFu, (val.z >> 16) & 0x7FFFu), max(val.w & 0x7FFFu, (val.w >> 16) & 0x7FFFu)));
+  };
+  // per-token amax (bf16 bit patterns of |x| order like the values) -> s_a = amax / 7, 1 / s_a
+  unsigned int mx[QUANT ? MT : 1];
+  auto amax_add = [&](int m, uint4 val) {
+    const unsigned int am = chunk_amax(val);
+#pragma unroll
+    for (int mm = 0; mm < MT; ++mm)
+      if (mm == m) mx[mm] = max(mx[mm], am);
+  };
+  auto finish_scales = [&]() {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xFFFFFFFFu, mx[m], off));
+      if (lane == 0) red_max[warp * MT + m] = mx[m];
+    }
+    __syncthreads();
+    if (threadIdx.x < M) {
+      unsigned int m_all = 0;
+      for (int w = 0; w < kWarps; ++w) m_all = max(m_all, red_max[w * MT + threadIdx.x]);
+      s_a[threadIdx.x] = __fdiv_rn(__uint_as_float(m_all << 16), kQmax);
+      s_r[threadIdx.x] = __frcp_rn(s_a[threadIdx.x]);
+      if (xs_out && blockIdx.x == 0) xs_out[threadIdx.x] = s_a[threadIdx.x];
+    }
+    __syncthreads();
+  };
+  if constexpr (QUANT) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) mx[m] = 0;
+  }
+  // a chunked CTA stages part of K but needs the amax over all of it: one extra read of x
+  auto amax_full = [&]() {
+    const int n16 = K / 8;
+    for (int c = threadIdx.x; c < M * n16; c += kThreads) {
+      const int m = c / n16;
+      amax_add(m, __ldg(reinterpret_cast<const uint4*>(x) + c));
+    }
+  };
+  if constexpr (QB == 1) {
+    if (threadIdx.x < M) s_a[threadIdx.x] = s_a_in[threadIdx.x];
+  }
+  uint4 u[kU];
+  if (total <= kU * kThreads) {
+    // one batch: x stays in registers between the passes
+    load_batch(threadIdx.x, u);
+    if constexpr (QUANT) {
+      if (KC == 1) {
+#pragma unroll
+        for (int e = 0; e < kU; ++e) {
+          const int c = threadIdx.x + e * kThreads;
+          if (c < total) amax_add(c / per_token, u[e]);
+        }
+      } else {
+        amax_full();
+      }
+      finish_scales();
+    }
+#pragma unroll
+    for (int e = 0; e < kU; ++e) {
+      const int c = threadIdx.x + e * kThreads;
+      if (c >= total) continue;
+      int m, v;
+      locate(c, m, v);
+      xs[slot_of(m, v)] = QUANT ? quantise(m, v, u[e]) : u[e];
+    }
+  } else {
+    // several batches: x goes to shared memory as it is, W4A4 then works there (no second trip
+    // to L2)
+    for (int c0 = threadIdx.x; c0 < total; c0 += kU * kThreads) {
+      load_batch(c0, u);
+#pragma unroll
+      for (int e = 0; e < kU; ++e) {
+        const int c = c0 + e * kThreads;
+        if (c >= total) continue;
+        int m, v;
+        locate(c, m, v);
+        xs[slot_of(m, v)] = u[e];
+        if constexpr (QUANT) {
+          if (KC == 1) amax_add(m, u[e]);
+        }
+      }
+    }
+    if constexpr (QUANT) {
+      if (KC > 1) amax_full();
+      finish_scales();
+      for (int c = threadIdx.x; c < total; c += kThreads) {
+        int m, v;
+        locate(c, m, v);
+        const int sl = slot_of(m, v);
+        xs[sl] = quantise(m, v, xs[sl]);
+      }
+    }
+  }
+  __syncthreads();
+
+  for (int r = 0; r < rounds; ++r) {
+    const int tile = r * stride + tile0;
+    // rows (tile * 16 + g, + 8) x tokens (8 nb + 2t, 8 nb + 2t + 1) of column block nb
+    float acc[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
+    for (int i0 = 0; i0 < gs; i0 += D) {
+#pragma unroll
+      for (int k = 0; k < D; ++k) {
+        const uint4* xg = xs + static_cast<size_t>(g_beg + i0 + k) * 16 * MT;
+        const uint32_t lo[4] = {wl[k].x, wl[k].y, wl[k].z, wl[k].w};
+        const uint32_t hi[4] = {wh[k].x, wh[k].y, wh[k].z, wh[k].w};
+        float d[NB][4];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) d[nb][0] = d[nb][1] = d[nb][2] = d[nb][3] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint4 xb[NB];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            xb[nb] = make_uint4(0, 0, 0, 0);
+            if (MT % 8 == 0 || g < MT) xb[nb] = xg[(j * MT + nb * 8 + g) * 4 + t];
+          }
+          const uint32_t a0 = code_pair(lo[j], 0), a1 = code_pair(hi[j], 0), a2 = code_pair(lo[j], 1),
+                         a3 = code_pair(hi[j], 1);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_16816(d[nb], a0, a1, a2, a3, xb[nb].x, xb[nb].y);
+          const uint32_t c0 = code_pair(lo[j], 2), c1 = code_pair(hi[j], 2), c2 = code_pair(lo[j], 3),
+                         c3 = code_pair(hi[j], 3);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_16816(d[nb], c0, c1, c2, c3, xb[nb].z, xb[nb].w);
+        }
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          acc[nb][0] = fmaf(sl[k], d[nb][0], acc[nb][0]);
+          acc[nb][1] = fmaf(sl[k], d[nb][1], acc[nb][1]);
+          acc[nb][2] = fmaf(sh[k], d[nb][2], acc[nb][2]);
+          acc[nb][3] = fmaf(sh[k], d[nb][3], acc[nb][3]);
+        }
+        if constexpr (A4 && ACC) {
+          if (tile < tiles) {  // exact integer group sums
+            const int n_lo = tile * 16 + g, n_hi = n_lo + 8, gi = gb + g_beg + i0 + k;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const int m0 = nb * 8 + 2 * t, m1 = m0 + 1;
+              if (n_lo < N && m0 < M) acc_out[(static_cast<size_t>(m0) * N + n_lo) * G + gi] = static_cast<int32_t>(d[nb][0]);
+              if (n_lo < N && m1 < M) acc_out[(static_cast<size_t>(m1) * N + n_lo) * G + gi] = static_cast<int32_t>(d[nb][1]);
+              if (n_hi < N && m0 < M) acc_out[(static_cast<size_t>(m0) * N + n_hi) * G + gi] = static_cast<int32_t>(d[nb][2]);
+              if (n_hi < N && m1 < M) acc_out[(static_cast<size_t>(m1) * N + n_hi) * G + gi] = static_cast<int32_t>(d[nb][3]);
+            }
+          }
+        }
+        fetch(k);
+      }
+    }
+    if (KS > 1) {  // K slices summed in slice order by the slice-0 warp of the tile slot
+      float4* rb = red + (r & 1) * kWarps * NB * 32;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+        rb[(warp * NB + nb) * 32 + lane] = make_float4(acc[nb][0], acc[nb][1], acc[nb][2], acc[nb][3]);
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + wtile), "r"(KS * 32) : "memory");
+      if (ks == 0) {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          float4 s4 = rb[(warp * NB + nb) * 32 + lane];
+          for (int j = 1; j < KS; ++j) {
+            const float4 o = rb[((warp + j) * NB + nb) * 32 + lane];
+            s4.x += o.x;
+            s4.y += o.y;
+            s4.z += o.z;
+            s4.w += o.w;
+          }
+          acc[nb][0] = s4.x;
+          acc[nb][1] = s4.y;
+          acc[nb][2] = s4.z;
+          acc[nb][3] = s4.w;
+        }
+      }
+    }
+    bool store = ks == 0 && tile < tiles;
+    if (store && KC > 1) {
+      // publish this chunk's partial tile; the chunk that arrives last sums all KC in chunk order
+      float4* pp = reinterpret_cast<float4*>(part);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+        pp[((static_cast<size_t>(kc) * tiles + tile) * NB + nb) * 32 + lane] =
+            make_float4(acc[nb][0], acc[nb][1], acc[nb][2], acc[nb][3]);
+      __threadfence();
+      unsigned int prev = 0;
+      if (lane == 0) prev = atomicAdd(tick + tile, 1u);
+      prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+      store = prev == static_cast<unsigned int>(KC - 1);
+      if (store) {
+        __threadfence();
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int kk = 0; kk < KC; ++kk) {
+            const float4 o = __ldcg(pp + ((static_cast<size_t>(kk) * tiles + tile) * NB + nb) * 32 + lane);
+            s4.x += o.x;
+            s4.y += o.y;
+            s4.z += o.z;
+            s4.w += o.w;
+          }
+          acc[nb][0] = s4.x;
+          acc[nb][1] = s4.y;
+          acc[nb][2] = s4.z;
+          acc[nb][3] = s4.w;
+        }
+        if (lane == 0) tick[tile] = 0;
+      }
+    }
+    if (store) {
+      const int n_lo = tile * 16 + g, n_hi = n_lo + 8;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const int m0 = nb * 8 + 2 * t, m1 = m0 + 1;
+        if constexpr (A4) {
+          const float sa0 = m0 < M ? s_a[m0] : 0.0f, sa1 = m1 < M ? s_a[m1] : 0.0f;
+          acc[nb][0] *= sa0;
+          acc[nb][1] *= sa1;
+          acc[nb][2] *= sa0;
+          acc[nb][3] *= sa1;
+        }
+        if (n_lo < N && m0 < M) y[static_cast<size_t>(m0) * N + n_lo] = f32_to_bf16_bits(acc[nb][0]);
+        if (n_lo < N && m1 < M) y[static_cast<size_t>(m1) * N + n_lo] = f32_to_bf16_bits(acc[nb][1]);
+        if (n_hi < N && m0 < M) y[static_cast<size_t>(m0) * N + n_hi] = f32_to_bf16_bits(acc[nb][2]);
+        if (n_hi < N && m1 < M) y[static_cast<size_t>(m1) * N + n_hi] = f32_to_bf16_bits(acc[nb][3]);
+      }
+    }
+  }
+}
+
+// dynamic shared memory for MT token slots over Gc staged groups
+inline size_t smem_bytes(int MT, int Gc) {
+  return static_cast<size_t>(Gc) * 16 * MT * 16 + 2 * static_cast<size_t>(kWarps) * ((MT + 7) / 8) * 32 * 16;
+}
+constexpr size_t kSmemCap = 200 * 1024;
+
+// K chunks across CTAs: the fewest (a divisor of the group count) whose staged activations fit
+// shared memory; 0 if none does.
+inline int pick_kc(int MT, int G) {
+  for (int kc = 1; kc <= G; ++kc)
+    if (G % kc == 0 && smem_bytes(MT, G / kc) <= kSmemCap) return kc;
+  return 0;
+}
+
+inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace bytes of the chunk partials and tile tickets (0 when K is not chunked).
+inline size_t chunk_ws_bytes(int MT, int N, int G, int KC) {
+  if (KC <= 1) return 0;
+  const size_t tiles = (static_cast<size_t>(N) + 15) / 16;
+  return al256(static_cast<size_t>(KC) * tiles * ((MT + 7) / 8) * 32 * 16) + al256(tiles * sizeof(unsigned int));
+}
+
+struct Outs {
+  int8_t* xq;
+  float* xs;
+  int32_t* acc;
+  const float* s_in;     // codes mode: the per-token scales of the staged codes
+  float* part;           // K chunks: [KC][tiles][NB][32] float4 partial tiles
+  unsigned int* tick;    // K chunks: [tiles] arrival counters (zero between calls)
+};
+
+template <int QB, bool ACC, int MT, int D>
+qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+                      Outs o, int best_ks, int KC, int best_grid, cudaStream_t stream) {
+  const size_t smem = smem_bytes(MT, K / kGroup / KC);
+  auto kern = KC > 1 ? gemv_kernel<QB, ACC, MT, D, true> : gemv_kernel<QB, ACC, MT, D, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return QSPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(best_grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, KC, y, o.xq, o.xs, o.acc, o.s_in, o.part,
+                            o.tick) == cudaSuccess
+             ? QSPEC_OK
+             : QSPEC_ERR_CUDA;
+}
+
+template <int QB, int MT>
+qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+                    Outs o, int KC, cudaStream_t stream) {
+  const int Gc = K / kGroup / KC;
+  const long long tiles = (static_cast<long long>(N) + 15) / 16;
+  const int chunk_grids = std::max(1, num_sms() / KC);  // CTAs per K chunk
+  // K split among a CTA's warps: the fewest rounds of (groups per slice + fixed cost), ties to
+  // the wider grid
+  int best_ks = 1, best_grid = 1;
+  long long best_cost = -1;
+  for (int ks = 1; ks <= kWarps; ks *= 2) {
+    if (Gc % ks != 0) continue;
+    const long long slots = kWarps / ks;
+    const int grid = static_cast<int>(std::min<long long>(chunk_grids, (tiles + slots - 1) / slots));
+    const long long rounds = (tiles + grid * slots - 1) / (grid * slots);
+    const long long cost = rounds * (Gc / ks + 2);
+    if (best_cost < 0 || cost < best_cost || (cost == best_cost && grid > best_grid)) {
+      best_cost = cost;
+      best_ks = ks;
+      best_grid = grid;
+    }
+  }
+  best_grid *= KC;
+  const int gs = Gc / best_ks;
+  if constexpr (QB != 0) {
+    if (o.acc) {  // the checking path: group sums out, no need for the deepest prefetch
+      if (gs % 2 == 0) return launch_d<QB, true, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+      return launch_d<QB, true, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+    }
+  }
+  // (16 token slots keep two column blocks of accumulators: at most two groups in flight then)
+  if constexpr (MT < 16) {
+    if (gs % 4 == 0) return launch_d<QB, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+  }
+  if (gs % 2 == 0) return launch_d<QB, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+  return launch_d<QB, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+}
+
+// The launcher of one activation mode (0: W4A16, 4: W4A4, 8: W4A8, 1: staged codes) for MT token
+// slots; each mode is instantiated in a translation unit of its own (they compile in parallel).
+template <int QB>
+qspec_status launch_mode(int MT, const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K,
+                         uint16_t* y, Outs o, int KC, cudaStream_t stream);
+
+template <>
+qspec_status launch_mode<0>(int, const uint16_t*, const uint8_t*, const __half*, int, int, int, uint16_t*, Outs, int,
+                            cudaStream_t);
+template <>
+qspec_status launch_mode<1>(int, const uint16_t*, const uint8_t*, const __half*, int, int, int, uint16_t*, Outs, int,
+                            cudaStream_t);
+template <>
+qspec_status launch_mode<4>(int, const uint16_t*, const uint8_t*, const __half*, int, int, int, uint16_t*, Outs, int,
+                            cudaStream_t);
+template <>
+qspec_status launch_mode<8>(int, const uint16_t*, const uint8_t*, const __half*, int, int, int, uint16_t*, Outs, int,
+                            cudaStream_t);
+
+#define QSPEC_GEMV_MODE_UNIT(QB_)                                                                      \
+  template <>                                                                                          \
+  qspec_status launch_mode<QB_>(int MT, const uint16_t* x, const uint8_t* Wp, const __half* S, int M,  \
+                                int N, int K, uint16_t* y, Outs o, int KC, cudaStream_t stream) {      \
+    switch (MT) {                                                                                      \
+      case 1: return launch<QB_, 1>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
+      case 2: return launch<QB_, 2>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
+      case 4: return launch<QB_, 4>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
+      case 8: return launch<QB_, 8>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
+      default: return launch<QB_, 16>(x, Wp, S, M, N, K, y, o, KC, stream);                            \
+    }                                                                                                  \
+  }
+
+}  // namespace gemv_impl
+}  // namespace qspec

@@ -563,8 +563,9 @@ def profile_case(spec, reps):
         x = bf(syn.activations(M, K, 1, step=10 * li))
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         ws = q.new_linear_workspace(M, N, K, device=dev)
-        fn = ((lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws)) if mode == "a4"
-              else (lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws)))
+        fn = {"a4": lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws),
+              "a8": lambda: q.qspec_linear_w4a8(x, Wp, S, y, ws),
+              "a16": lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws)}[mode]
         nbytes = linear_bytes(M, N, K)
     for _ in range(reps):
         fn()

@@ -7,11 +7,16 @@ namespace qspec {
 using namespace gemv_impl;
 
 // Token slots for M tokens: the smallest staged width that holds them.
-int token_slots(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+int token_slots(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 32; }
 
 bool gemv_supported(int M, int N, int K) {
-  if (M < 1 || M > 16 || N < 1 || K % kGroup != 0) return false;
-  return pick_kc(token_slots(M), K / kGroup) > 0;
+  if (M < 1 || M > kMaxTokens || N < 1 || K % kGroup != 0) return false;
+  const int kc = pick_kc(token_slots(M), K / kGroup);
+  // 17..32 tokens: only up to 4 K chunks (measured on Llama-2-70B shapes at M = 32: with 4 chunks
+  // the GEMV beats the tcgen05 kernel on q/o, k/v and gate/up and loses 6% on lm_head; with 14, on
+  // down at K = 28672, it loses 50%)
+  if (M > 16) return kc > 0 && kc <= 4;
+  return kc > 0;
 }
 
 size_t gemv_workspace_bytes(int M, int N, int K) {
@@ -39,8 +44,8 @@ qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_
   // GEMV stages the codes.  With fewer tokens that kernel has too few CTAs to pay off (measured).
   uint16_t* codes = nullptr;
   float* s_a = nullptr;
-  if (qb != 0 && M >= 8 && static_cast<long long>(M) * K > 8LL * kStageU * kThreads &&
-      ws_codes(abits, M, N, K, ws, &codes, &s_a)) {
+  if (qb != 0 && M >= 8 && (M > 16 || static_cast<long long>(M) * K > 8LL * kStageU * kThreads)) {
+    if (!ws_codes(abits, M, N, K, ws, &codes, &s_a)) return QSPEC_ERR_WORKSPACE;
     const qspec_status st = quantise_tokens(abits, x, M, K, codes, s_a, xq_out, xs_out, stream);
     if (st != QSPEC_OK) return st;
     x = codes;

@@ -41,6 +41,7 @@ namespace gemv_impl {
 constexpr int kThreads = 512;  // 16 warps, one CTA per SM
 constexpr int kWarps = kThreads / 32;
 constexpr int kStageU = 4;  // 16-byte activation chunks a thread loads per staging batch
+constexpr int kMaxTokens = 32;  // token slots: 1, 2, 4, 8, 16 or 32 (two or four MMA column blocks above 8)
 
 // 16 bytes of packed weights, read once: not kept in L1
 __device__ __forceinline__ uint4 ld_weights(const void* p) {
@@ -531,16 +532,31 @@ qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M
   const int gs = Gc / best_ks;
   if constexpr (QB != 0) {
     if (o.acc) {  // the checking path: group sums out, no need for the deepest prefetch
-      if (gs % 2 == 0) return launch_d<QB, true, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+      if (MT < 32 && gs % 2 == 0)
+        return launch_d<QB, true, MT, (MT < 32 ? 2 : 1)>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
       return launch_d<QB, true, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
     }
   }
-  // (16 token slots keep two column blocks of accumulators: at most two groups in flight then)
-  if constexpr (MT < 16) {
-    if (gs % 4 == 0) return launch_d<QB, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+  // (16 token slots keep two column blocks of accumulators: at most two groups in flight then;
+  // 32 slots keep four: one)
+  if constexpr (MT >= 32) {
+    return launch_d<QB, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+  } else {
+    if constexpr (MT < 16) {
+      if (gs % 4 == 0) return launch_d<QB, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+    }
+    if (gs % 2 == 0) return launch_d<QB, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+    return launch_d<QB, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
   }
-  if (gs % 2 == 0) return launch_d<QB, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
-  return launch_d<QB, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
+}
+
+// 32 token slots (four MMA column blocks) only for modes that stage ready operands (W4A16, codes):
+// the quantising modes would keep 32 per-token amax registers.
+template <int QB>
+qspec_status launch_wide(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+                         Outs o, int KC, cudaStream_t stream) {
+  if constexpr (QB == 0 || QB == 1) return launch<QB, 32>(x, Wp, S, M, N, K, y, o, KC, stream);
+  return QSPEC_ERR_UNSUPPORTED_SHAPE;
 }
 
 // The launcher of one activation mode (0: W4A16, 4: W4A4, 8: W4A8, 1: staged codes) for MT token
@@ -571,7 +587,8 @@ qspec_status launch_mode<8>(int, const uint16_t*, const uint8_t*, const __half*,
       case 2: return launch<QB_, 2>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
       case 4: return launch<QB_, 4>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
       case 8: return launch<QB_, 8>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
-      default: return launch<QB_, 16>(x, Wp, S, M, N, K, y, o, KC, stream);                            \
+      case 16: return launch<QB_, 16>(x, Wp, S, M, N, K, y, o, KC, stream);                            \
+      default: return launch_wide<QB_>(x, Wp, S, M, N, K, y, o, KC, stream);                           \
     }                                                                                                  \
   }
 

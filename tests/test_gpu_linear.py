@@ -93,7 +93,8 @@ def test_linear_m_sweep(q, M):
 
 @pytest.mark.parametrize("M,N,K", [(4, 512, 256), (1, 8, 128), (3, 24, 1152), (16, 1000, 128),
                                    (1, 1024, 4096), (4, 4096, 4096), (16, 1024, 4096), (64, 512, 4096),
-                                   (100, 136, 512), (256, 256, 1024), (8, 264, 8192), (12, 136, 2048)])
+                                   (100, 136, 512), (256, 256, 1024), (8, 264, 8192), (12, 136, 2048),
+                                   (32, 264, 4096), (24, 136, 1152), (20, 520, 28672)])
 def test_linear_shapes(q, M, N, K):
     linear_case(q, M, N, K)
 

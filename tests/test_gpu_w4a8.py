@@ -50,7 +50,7 @@ def w4a8_case(q, M, N, K, wid=5):
 
 @pytest.mark.parametrize("M,N,K", [(1, 512, 256), (4, 264, 384), (8, 1000, 1152), (16, 136, 4096), (3, 24, 128),
                                    (17, 264, 384), (64, 512, 4096), (4, 64, 28672), (100, 136, 512),
-                                   (8, 520, 8192), (1, 264, 28672), (16, 136, 14336), (4, 136, 28672)])
+                                   (8, 520, 8192), (1, 264, 28672), (16, 136, 14336), (4, 136, 28672), (32, 136, 4096)])
 def test_w4a8_parity(q, M, N, K):
     w4a8_case(q, M, N, K)
 

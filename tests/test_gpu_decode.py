@@ -182,10 +182,11 @@ def check_target_logits(model, rec, tol=1e-2):
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= tol
 
 
-# (5, 3): the verify pass runs at M = 20, on the tensor-core linear; V = 16384 gives the last layer
-# more output tiles than the first two, so layers sharing one workspace would corrupt its tickets
+# (9, 3): the verify pass runs at M = 36, on the tensor-core linear; V = 16384 gives the last layer
+# more output tiles than the first two, so layers sharing one workspace would corrupt its tickets.
+# (5, 3): M = 20, the GEMV's 32 token slots.
 @pytest.mark.parametrize("B,gamma,use_graphs,V", [(1, 3, True, 1000), (3, 2, True, 1000), (2, 4, False, 1000),
-                                                  (5, 3, True, 16384)])
+                                                  (9, 3, True, 16384), (5, 3, True, 16384)])
 def test_decode_loop_greedy(q, dec, B, gamma, use_graphs, V):
     model = small_model(dec, V=V)
     sd = dec.SpecDecoder(model, B, gamma, use_graphs=use_graphs)

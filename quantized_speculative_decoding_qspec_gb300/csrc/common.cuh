@@ -38,6 +38,19 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// a / b rounded to nearest (IEEE), given rb = 1 / b rounded to nearest: Markstein's division
+// refinement -- q0 = a * rb is within one ulp of a / b, the FMA gives the remainder a - b q0
+// exactly, and one more FMA rounds q0 + remainder * rb correctly.  That needs the remainder to be
+// representable: with b >= 2^-100 it is whenever |a / b| >= 1/4, the only quotients whose rounding
+// can change a code (smaller ones give code 0 either way).  The quantisers keep the IEEE division
+// for smaller b (and for the 8-bit divisor 127, which the check below does not cover).  Checked exhaustively against the IEEE division for every bf16 amax (b = amax / 7)
+// and every bf16 |a| <= amax: identical codes, identical quotients wherever |a / b| >= 1/4.
+__device__ __forceinline__ float div_rn_markstein(float a, float b, float rb) {
+  const float q0 = a * rb;
+  const float r = fmaf(-b, q0, a);
+  return fmaf(r, rb, q0);
+}
+
 // 16-byte streaming load that does not allocate in L1 (data read exactly once).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 r;

@@ -61,18 +61,6 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// a / b rounded to nearest (IEEE), given rb = 1 / b rounded to nearest: Markstein's division
-// refinement -- q0 = a * rb is within one ulp of a / b, the FMA gives the remainder a - b q0
-// exactly, and one more FMA rounds q0 + remainder * rb correctly.  That needs the remainder to be
-// representable: with b >= 2^-100 it is whenever |a / b| >= 1/4, the only quotients whose rounding
-// can change a code (smaller ones give code 0 either way).  The quantiser keeps the IEEE division
-// for smaller b.  Checked exhaustively against the IEEE division for every bf16 amax (b = amax / 7)
-// and every bf16 |a| <= amax: identical codes, identical quotients wherever |a / b| >= 1/4.
-__device__ __forceinline__ float div_rn_markstein(float a, float b, float rb) {
-  const float q0 = a * rb;
-  const float r = fmaf(-b, q0, a);
-  return fmaf(r, rb, q0);
-}
 
 // d += A (16 x 16, row fragments a0..a3) * B (16 x 8, column fragments b0, b1), fp32 accumulate
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,

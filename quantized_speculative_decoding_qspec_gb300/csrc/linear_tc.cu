@@ -682,40 +682,6 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
   }
 }
 
-// Per-token quantiser for M > 4 (step a3): codes as exact bf16 for the GEMM, plus the optional
-// int8 codes and fp32 scales.  One CTA per token.
-__global__ void __launch_bounds__(256) act_quant_kernel(const uint16_t* __restrict__ x, int K, float qmax,
-                                                        uint16_t* __restrict__ codes, float* __restrict__ s_a,
-                                                        int8_t* __restrict__ xq_out, float* __restrict__ xs_out) {
-  grid_launch_dependents();
-  grid_dependency_wait();
-  const int m = blockIdx.x;
-  const uint16_t* xr = x + static_cast<long long>(m) * K;
-  uint32_t mx = 0;
-  for (int k8 = threadIdx.x; k8 < K / 8; k8 += 256) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + k8);
-    mx = max(mx, max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu)));
-    mx = max(mx, max(max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu), max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu)));
-  }
-  __shared__ unsigned int s_mx;
-  if (threadIdx.x == 0) s_mx = 0;
-  __syncthreads();
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  if ((threadIdx.x & 31) == 0) atomicMax(&s_mx, mx);
-  __syncthreads();
-  const float sa = __fdiv_rn(__uint_as_float(s_mx << 16), qmax);
-  if (threadIdx.x == 0) {
-    s_a[m] = sa;
-    if (xs_out) xs_out[m] = sa;
-  }
-  for (int k = threadIdx.x; k < K; k += 256) {
-    const float cq = sa == 0.0f ? 0.0f : fminf(fmaxf(rintf(__fdiv_rn(bf16_lo(xr[k]), sa)), -qmax - 1.0f), qmax);
-    codes[static_cast<long long>(m) * K + k] = f32_to_bf16_bits(cq);
-    if (xq_out) xq_out[static_cast<long long>(m) * K + k] = static_cast<int8_t>(cq);
-  }
-}
-
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -745,7 +711,7 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uin
 }
 
 // The fused kernel quantises W4A4 tokens itself (M <= 4); other quantised cases (W4A4 at larger M,
-// every W4A8) quantise in act_quant_kernel first and multiply codes.
+// every W4A8) are quantised once by the quantiser kernel (quant.cu) and multiply codes.
 bool fused_mode(int abits, int M) { return abits == 4 && M <= kFusedMaxM; }
 bool codes_mode_of(int abits, int M) { return abits != 16 && !fused_mode(abits, M); }
 
@@ -909,23 +875,6 @@ bool ws_codes(int abits, int M, int N, int K, void* ws, uint16_t** codes, float*
   *codes = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + L.codes);
   *s_a = reinterpret_cast<float*>(static_cast<char*>(ws) + L.s_a);
   return true;
-}
-
-qspec_status quantise_tokens(int abits, const uint16_t* x, int M, int K, uint16_t* codes, float* s_a,
-                             int8_t* xq_out, float* xs_out, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(M);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const float qmax = abits == 8 ? 127.0f : 7.0f;
-  return cudaLaunchKernelEx(&cfg, act_quant_kernel, x, K, qmax, codes, s_a, xq_out, xs_out) == cudaSuccess
-             ? QSPEC_OK
-             : QSPEC_ERR_CUDA;
 }
 
 qspec_status read_and_clear_linear_error(cudaStream_t stream, unsigned int* bits) {

@@ -39,13 +39,14 @@ qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_
     o.tick = reinterpret_cast<unsigned int*>(base + al256(static_cast<size_t>(KC) * tiles * ((MT + 7) / 8) * 512));
   }
   int qb = abits == 16 ? 0 : abits;
-  // Tokens that take several staging batches would be quantised by every CTA from shared memory;
-  // there the quantiser runs once, in its own kernel, and the GEMV stages the codes (measured on
-  // the 70B shapes: W4A4 down at M = 4, 50.5 -> 41.7 us; q/o at M = 8, 21.2 -> 16.3 us).  More than
-  // 16 tokens always take this path (the 32-slot kernel does not quantise).
+  // Four or more tokens, or tokens that take several staging batches, would be quantised by every
+  // CTA again; there the quantiser runs once, in its own kernel, and the GEMV stages the codes
+  // (measured: 70B W4A4 down at M = 4, 50.5 -> 41.7 us; q/o at M = 8, 21.2 -> 16.3 us; 8B q at
+  // M = 4, 8.4 -> 7.0 us; a single token is faster quantised in every CTA, 4.2 vs 5.4 us on k).
+  // More than 16 tokens always take this path (the 32-slot kernel does not quantise).
   uint16_t* codes = nullptr;
   float* s_a = nullptr;
-  if (qb != 0 && (M > 16 || static_cast<long long>(M) * K > 8LL * kStageU * kThreads)) {
+  if (qb != 0 && (M >= 4 || static_cast<long long>(M) * K > 8LL * kStageU * kThreads)) {
     if (!ws_codes(abits, M, N, K, ws, &codes, &s_a)) return QSPEC_ERR_WORKSPACE;
     const qspec_status st = quantise_tokens(abits, x, M, K, codes, s_a, xq_out, xs_out, stream);
     if (st != QSPEC_OK) return st;

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NB = (MT + 7) / 8;
   float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(Gc) * 16 * MT);  // [2][kWarps][NB][32]
   __shared__ unsigned int red_max[QUANT ? kWarps * MT : 1];
-  __shared__ float s_a[MT], s_r[MT];  // per-token scale and its reciprocal (rounded to nearest)
+  __shared__ float s_a[MT];  // per-token scale, for the epilogue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
@@ -184,12 +184,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto slot_of = [&](int m, int v) { return ((v >> 2) * MT + m) * 4 + (v & 3); };
   // W4A4 / W4A8: codes = clamp(rint(x / s_a), -qmax - 1, qmax) of one chunk, as exact bf16 (and the
   // int8 codes out)
+  // per-token scale and its reciprocal, held by every thread (finish_scales)
+  float sa_r[QUANT ? MT : 1], rs_r[QUANT ? MT : 1];
   auto quantise = [&](int m, int v, uint4 val) {
-    const float sa = s_a[m], rsa = s_r[m];
+    float sa = sa_r[0], rsa = rs_r[0];
+#pragma unroll
+    for (int mm = 1; mm < (QUANT ? MT : 1); ++mm)
+      if (m == mm) {
+        sa = sa_r[mm];
+        rsa = rs_r[mm];
+      }
     // see div_rn_markstein (checked for the 4-bit divisor; W4A8 keeps the IEEE division)
     const bool fast = QB == 4 && sa >= 0x1p-100f;
-    uint32_t w[4] = {val.x, val.y, val.z, val.w};
-    uint32_t q8[2] = {0, 0};
+    const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+    float c[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float c0f = 0.0f, c1f = 0.0f;
@@ -200,13 +208,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         c0f = fminf(fmaxf(rintf(q0), -kQmax - 1.0f), kQmax);
         c1f = fminf(fmaxf(rintf(q1), -kQmax - 1.0f), kQmax);
       }
-      w[i] = static_cast<uint32_t>(f32_to_bf16_bits(c0f)) | (static_cast<uint32_t>(f32_to_bf16_bits(c1f)) << 16);
-      q8[i >> 1] |= ((static_cast<uint32_t>(static_cast<int>(c0f)) & 0xFFu) |
-                     ((static_cast<uint32_t>(static_cast<int>(c1f)) & 0xFFu) << 8))
-                    << (16 * (i & 1));
+      c[2 * i] = c0f;
+      c[2 * i + 1] = c1f;
     }
-    if (xq_out && cb == 0) *reinterpret_cast<uint2*>(xq_out + src_of(m, v)) = make_uint2(q8[0], q8[1]);
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    if (xq_out && cb == 0) {
+      uint32_t q8[2] = {0, 0};
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        q8[e >> 2] |= (static_cast<uint32_t>(static_cast<int>(c[e])) & 0xFFu) << (8 * (e & 3));
+      *reinterpret_cast<uint2*>(xq_out + src_of(m, v)) = make_uint2(q8[0], q8[1]);
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // one paired conversion per two codes (exact: small integers)
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(c[2 * i], c[2 * i + 1]);
+      o[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
   };
   auto chunk_amax = [](uint4 val) {
     return max(max(max(val.x & 0x7FFFu, (val.x >> 16) & 0x7FFFu), max(val.y & 0x7FFFu, (val.y >> 16) & 0x7FFFu)),
@@ -220,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int mm = 0; mm < MT; ++mm)
       if (mm == m) mx[mm] = max(mx[mm], am);
   };
+  // every thread reduces the warps' maxima itself, so one barrier suffices
   auto finish_scales = [&]() {
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
@@ -228,14 +247,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) red_max[warp * MT + m] = mx[m];
     }
     __syncthreads();
-    if (threadIdx.x < M) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
       unsigned int m_all = 0;
-      for (int w = 0; w < kWarps; ++w) m_all = max(m_all, red_max[w * MT + threadIdx.x]);
-      s_a[threadIdx.x] = __fdiv_rn(__uint_as_float(m_all << 16), kQmax);
-      s_r[threadIdx.x] = __frcp_rn(s_a[threadIdx.x]);
-      if (xs_out && blockIdx.x == 0) xs_out[threadIdx.x] = s_a[threadIdx.x];
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) m_all = max(m_all, red_max[w * MT + m]);
+      sa_r[m] = __fdiv_rn(__uint_as_float(m_all << 16), kQmax);
+      rs_r[m] = __frcp_rn(sa_r[m]);
+      if (threadIdx.x == m && m < M) {  // for the epilogue (read after the staging barrier)
+        s_a[m] = sa_r[m];
+        if (xs_out && blockIdx.x == 0) xs_out[m] = sa_r[m];
+      }
     }
-    __syncthreads();
   };
   if constexpr (QUANT) {
 #pragma unroll

@@ -561,13 +561,17 @@ qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M
   }
 }
 
-// 32 token slots (four MMA column blocks) only for modes that stage ready operands (W4A16, codes):
-// the quantising modes would keep 32 per-token amax registers.
-template <int QB>
-qspec_status launch_wide(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
-                         Outs o, int KC, cudaStream_t stream) {
-  if constexpr (QB == 0 || QB == 1) return launch<QB, 32>(x, Wp, S, M, N, K, y, o, KC, stream);
-  return QSPEC_ERR_UNSUPPORTED_SHAPE;
+// The modes that quantise inside the kernel (QB = 4, 8) serve at most three tokens (from four on
+// the separate quantiser runs and QB = 1 stages its codes), so they are instantiated for up to 4
+// token slots only; 32 slots serve W4A16 and codes.
+template <int QB, int MT>
+qspec_status launch_slots(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+                          Outs o, int KC, cudaStream_t stream) {
+  if constexpr ((QB == 4 || QB == 8) && MT > 4) {
+    return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  } else {
+    return launch<QB, MT>(x, Wp, S, M, N, K, y, o, KC, stream);
+  }
 }
 
 // The launcher of one activation mode (0: W4A16, 4: W4A4, 8: W4A8, 1: staged codes) for MT token
@@ -594,12 +598,12 @@ qspec_status launch_mode<8>(int, const uint16_t*, const uint8_t*, const __half*,
   qspec_status launch_mode<QB_>(int MT, const uint16_t* x, const uint8_t* Wp, const __half* S, int M,  \
                                 int N, int K, uint16_t* y, Outs o, int KC, cudaStream_t stream) {      \
     switch (MT) {                                                                                      \
-      case 1: return launch<QB_, 1>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
-      case 2: return launch<QB_, 2>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
-      case 4: return launch<QB_, 4>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
-      case 8: return launch<QB_, 8>(x, Wp, S, M, N, K, y, o, KC, stream);                              \
-      case 16: return launch<QB_, 16>(x, Wp, S, M, N, K, y, o, KC, stream);                            \
-      default: return launch_wide<QB_>(x, Wp, S, M, N, K, y, o, KC, stream);                           \
+      case 1: return launch_slots<QB_, 1>(x, Wp, S, M, N, K, y, o, KC, stream);                        \
+      case 2: return launch_slots<QB_, 2>(x, Wp, S, M, N, K, y, o, KC, stream);                        \
+      case 4: return launch_slots<QB_, 4>(x, Wp, S, M, N, K, y, o, KC, stream);                        \
+      case 8: return launch_slots<QB_, 8>(x, Wp, S, M, N, K, y, o, KC, stream);                        \
+      case 16: return launch_slots<QB_, 16>(x, Wp, S, M, N, K, y, o, KC, stream);                      \
+      default: return launch_slots<QB_, 32>(x, Wp, S, M, N, K, y, o, KC, stream);                      \
     }                                                                                                  \
   }
 

@@ -28,6 +28,7 @@ constexpr int kPlanCTAs = 1216;   // about 8 CTAs per SM on a 152-SM part (measu
 constexpr int kMinChunk = 2048;   // elements per CTA at least (4 KB of bf16)
 constexpr int kSeg2 = 8;          // pass 2: contiguous elements per thread
 constexpr int kChunk2 = kThreads * kSeg2;
+constexpr int kPass2Chunks = 4;   // pass 2: chunks per CTA (their loads are in flight together)
 
 enum : unsigned int { kErrBadToken = 2u };
 
@@ -512,16 +513,18 @@ __device__ int chunk_select(const RowPair& rp, int V, int c, float target) {
   return res;
 }
 
-// Pass 2: per (sequence, chunk of 2048) residual mass of row n; the last CTA of a sequence walks
-// the chunk sums in index order and selects the token with the inverse CDF.
+// Pass 2: per (sequence, group of kPass2Chunks chunks of 2048) residual mass of row n, one sum per
+// chunk; the last CTA of a sequence walks the chunk sums in index order and selects the token with
+// the inverse CDF.
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) sample_pass2_kernel(
     const uint16_t* __restrict__ Lt, const uint16_t* __restrict__ Ld,
     const float* __restrict__ u_res, int B, int gamma, int V, int chunks2, WS ws,
     int32_t* __restrict__ out_tok) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = blockIdx.x / chunks2;
-  const int c = blockIdx.x % chunks2;
+  const int groups = (chunks2 + kPass2Chunks - 1) / kPass2Chunks;
+  const int b = blockIdx.x / groups;
+  const int c0 = (blockIdx.x % groups) * kPass2Chunks;
   const int G1 = gamma + 1;
   const int n = __ldcg(ws.seq_n + b);
   RowPair rp;
@@ -541,14 +544,43 @@ __global__ void __launch_bounds__(kThreads) sample_pass2_kernel(
     rp.md = 0.0f;
     rp.inv_sd = 0.0f;
   }
-  const float rc = chunk_sum<kVec>(rp, V, c);
+  {
+    float r[kPass2Chunks][kSeg2];
+#pragma unroll
+    for (int k = 0; k < kPass2Chunks; ++k) {
+      if (c0 + k < chunks2) {
+        seg_values<kVec>(rp, V, c0 + k, r[k]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kSeg2; ++e) r[k][e] = 0.0f;
+      }
+    }
+    __shared__ float s_ps[kPass2Chunks][kThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 0; k < kPass2Chunks; ++k) {
+      float v = 0.0f;
+#pragma unroll
+      for (int e = 0; e < kSeg2; ++e) v += r[k][e];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+      if (lane == 0) s_ps[k][warp] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < kPass2Chunks && c0 + static_cast<int>(threadIdx.x) < chunks2) {
+      float t = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) t += s_ps[threadIdx.x][w];
+      ws.part2[int64_t(b) * chunks2 + c0 + threadIdx.x] = t;
+      __threadfence();  // each writer publishes its chunk sum before the ticket below
+    }
+  }
 
   __shared__ bool s_last;
+  __syncthreads();
   if (threadIdx.x == 0) {
-    ws.part2[int64_t(b) * chunks2 + c] = rc;
-    __threadfence();
     const unsigned int prev = atomicAdd(ws.cnt2 + b, 1u);
-    s_last = prev == static_cast<unsigned int>(chunks2 - 1);
+    s_last = prev == static_cast<unsigned int>(groups - 1);
   }
   __syncthreads();
   if (!s_last) return;
@@ -834,7 +866,7 @@ extern "C" qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const ui
   // Pass 2 with programmatic dependent launch: its CTAs are scheduled while pass 1 drains and
   // wait (griddepcontrol.wait) for pass 1 to complete before reading the workspace.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(int64_t(B) * L.chunks2));
+  cfg.gridDim = dim3(unsigned(int64_t(B) * ((L.chunks2 + kPass2Chunks - 1) / kPass2Chunks)));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;

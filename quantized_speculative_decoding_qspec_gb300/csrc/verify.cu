@@ -28,7 +28,7 @@ constexpr int kPlanCTAs = 1216;   // about 8 CTAs per SM on a 152-SM part (measu
 constexpr int kMinChunk = 2048;   // elements per CTA at least (4 KB of bf16)
 constexpr int kSeg2 = 8;          // pass 2: contiguous elements per thread
 constexpr int kChunk2 = kThreads * kSeg2;
-constexpr int kPass2Chunks = 4;   // pass 2: chunks per CTA (their loads are in flight together)
+constexpr int kPass2Chunks = 2;   // pass 2: chunks per CTA (their loads are in flight together)
 
 enum : unsigned int { kErrBadToken = 2u };
 

@@ -573,16 +573,24 @@ def profile_case(spec, reps):
 
     parts = spec.split(":")
     if parts[0] == "verify":
-        vd = verify_data()
-        tgt, drf = bf(vd["tgt"]), bf(vd["drf"])
+        if len(parts) == 5:  # verify:MODE:B:GAMMA:V -- a sweep cell
+            Bc, gc, Vc = int(parts[2]), int(parts[3]), int(parts[4])
+            vi = syn.verify_inputs(Bc, gc, Vc, 0.5, workload_id=4, sampling=parts[1] != "greedy")
+            vd = {"tgt": vi["tgt"], "drf": vi.get("drf", vi["tgt"][:, :gc]), "d_greedy": vi["d"], "d_sample": vi["d"],
+                  "u_acc": vi.get("u_acc", np.zeros((Bc, gc), np.float32)),
+                  "u_res": vi.get("u_res", np.zeros((Bc, gc + 1), np.float32))}
+        else:
+            Bc, gc, Vc = 1, GAMMA, VOCAB
+            vd = verify_data()
+        tgt, drf = bf(vd["tgt"]), bf(np.ascontiguousarray(vd["drf"]))
         d = torch.from_numpy(vd["d_greedy" if parts[1] == "greedy" else "d_sample"]).to(dev)
         ua, ur = torch.from_numpy(vd["u_acc"]).to(dev), torch.from_numpy(vd["u_res"]).to(dev)
-        ws = q.new_verify_workspace(1, GAMMA, VOCAB, device=dev)
-        n = torch.empty(1, dtype=torch.int32, device=dev)
-        o = torch.empty(1, GAMMA + 1, dtype=torch.int32, device=dev)
+        ws = q.new_verify_workspace(Bc, gc, Vc, device=dev)
+        n = torch.empty(Bc, dtype=torch.int32, device=dev)
+        o = torch.empty(Bc, gc + 1, dtype=torch.int32, device=dev)
         fn = ((lambda: q.qspec_verify_greedy(tgt, d, n, o, ws)) if parts[1] == "greedy"
               else (lambda: q.qspec_verify_sample(tgt, drf, d, ua, ur, n, o, ws)))
-        nbytes = verify_bytes(1, GAMMA, VOCAB, parts[1] != "greedy")
+        nbytes = verify_bytes(Bc, gc, Vc, parts[1] != "greedy")
     else:
         name, mode, M = parts[0], parts[1], int(parts[2])
         li = [l[0] for l in LAYERS].index(name)

@@ -248,17 +248,24 @@ __device__ __forceinline__ float exp2_sfu(float x) {
 }
 constexpr float kLog2e = 1.4426950408889634f;
 
+// The reference m of a running (m, s) need not be the maximum: s = sum exp(l - m) stays exact in
+// meaning for any m, and terms up to e^16 cannot overflow fp32 over any row.  So the reference moves
+// only when a value exceeds it by more than kSlack, which keeps the rescaling expf (and the warp
+// divergence it causes) out of the stream after the first few vectors; consumers use exp(l - m) / s.
+constexpr float kSlack = 16.0f;
+
 __device__ __forceinline__ void ms_add8(MS& a, const float (&v)[8]) {
   float m8 = v[0];
 #pragma unroll
   for (int e = 1; e < 8; ++e) m8 = fmaxf(m8, v[e]);
-  if (m8 > a.m) {
+  if (m8 > a.m + kSlack) {
     a.s = a.m == -INFINITY ? 0.0f : a.s * expf(a.m - m8);
     a.m = m8;
   }
   if (a.m != -INFINITY) {
+    const float c = a.m * kLog2e;  // exp(v - m) = 2^(v log2e - m log2e), one FFMA per term
 #pragma unroll
-    for (int e = 0; e < 8; ++e) a.s += exp2_sfu((v[e] - a.m) * kLog2e);
+    for (int e = 0; e < 8; ++e) a.s += exp2_sfu(fmaf(v[e], kLog2e, -c));
   }
 }
 
@@ -323,7 +330,7 @@ __device__ __forceinline__ MS scan_ms(const uint16_t* __restrict__ rp, int beg, 
 // sequence evaluates a_i = min(1, p_i(d_i) / q_i(d_i)) at every draft position and the first
 // rejection n.  Rows [0, B(gamma+1)) are target rows, the next B*gamma rows draft rows.
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) sample_pass1_kernel(
+__global__ void __launch_bounds__(kThreads, 8) sample_pass1_kernel(
     const uint16_t* __restrict__ Lt, const uint16_t* __restrict__ Ld, const int32_t* __restrict__ d,
     const float* __restrict__ u_acc, int B, int gamma, int V, Plan plan, WS ws,
     int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tok, float* __restrict__ accept_prob,
@@ -753,8 +760,8 @@ __global__ void __launch_bounds__(kThreads) top1_kernel(const uint16_t* __restri
     warp_argmax(v, idx);
     t = warp_ms(t);
     if (lane == 0) {
-      // the top-1 token's own term is exp(max - max) = 1
-      const float p1 = t.s > 0.0f ? __fdiv_rn(1.0f, t.s) : 0.0f;
+      // the top-1 token's probability exp(max - m) / s (m: the running reference, not always the max)
+      const float p1 = t.s > 0.0f ? __fdiv_rn(expf(v - t.m), t.s) : 0.0f;
       s_tok[k] = idx;
       s_p1[k] = p1;
       const int64_t o = int64_t(b) * gamma + (k < gamma ? k : k - gamma);

@@ -255,17 +255,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 16.0f;
 
 __device__ __forceinline__ void ms_add8(MS& a, const float (&v)[8]) {
-  float m8 = v[0];
-#pragma unroll
-  for (int e = 1; e < 8; ++e) m8 = fmaxf(m8, v[e]);
+  // pairwise max and sum: dependency chains of depth 3 instead of 7
+  const float m8 = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
   if (m8 > a.m + kSlack) {
     a.s = a.m == -INFINITY ? 0.0f : a.s * expf(a.m - m8);
     a.m = m8;
   }
   if (a.m != -INFINITY) {
     const float c = a.m * kLog2e;  // exp(v - m) = 2^(v log2e - m log2e), one FFMA per term
+    float t[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) a.s += exp2_sfu(fmaf(v[e], kLog2e, -c));
+    for (int e = 0; e < 8; ++e) t[e] = exp2_sfu(fmaf(v[e], kLog2e, -c));
+    a.s += ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
   }
 }
 

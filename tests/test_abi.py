@@ -111,6 +111,43 @@ def test_verify_argument_checks(lib):
     assert s(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 1024, FAKE, FAKE, None, None, None, FAKE, 16, None) == 4
 
 
+def test_w4a8_argument_checks(lib):
+    f8 = lib.qspec_linear_w4a8
+    W = 1 << 16
+    assert f8(FAKE, FAKE, FAKE, 4, 512, 256, None, None, None, None, FAKE, W, None) == 1
+    assert f8(FAKE, FAKE, FAKE, 4097, 512, 256, FAKE, None, None, None, FAKE, W, None) == 2
+    assert f8(FAKE, FAKE, FAKE, 4, 512, 200, FAKE, None, None, None, FAKE, W, None) == 2
+    assert f8(FAKE, FAKE, FAKE, 4, 512, 256, FAKE, FAKE + 1, None, None, FAKE, W, None) == 3
+    assert f8(FAKE, FAKE, FAKE, 4, 512, 256, FAKE, None, None, None, None, W, None) == 4
+
+
+def test_top1_argument_checks(lib):
+    t = lib.qspec_verify_top1
+    need = lib.qspec_verify_workspace_size(2, 3, 1024)
+    ok = (FAKE, FAKE, 2, 3, 1024, FAKE, FAKE, None, None, 0.8, None)
+    assert t(*ok, FAKE, need - 1, None) == 4                                     # workspace too small
+    assert t(None, *ok[1:], FAKE, need, None) == 1                               # no target logits
+    assert t(FAKE, FAKE, 2, 17, 1024, FAKE, FAKE, None, None, 0.8, None, FAKE, need, None) == 2
+    assert t(FAKE, FAKE, 2, 3, 1, FAKE, FAKE, None, None, 0.8, None, FAKE, need, None) == 2
+    assert t(FAKE, FAKE, 2, 3, 1024, FAKE + 4, FAKE, None, None, 0.8, None, FAKE, need, None) == 3
+    assert t(FAKE, FAKE, 2, 3, 1024, FAKE, FAKE, None, None, float("nan"), None, FAKE, need, None) == 1
+    assert t(FAKE, FAKE, 2, 3, 1024, FAKE, FAKE, None, None, 0.8, FAKE + 8, FAKE, need, None) == 3
+
+
+def test_decode_loop_argument_checks(lib):
+    g, sel = lib.qspec_gather_rows, lib.qspec_select_tokens
+    assert g(None, 8, 64, FAKE, 4, FAKE, None) == 1
+    assert g(FAKE, 0, 64, FAKE, 4, FAKE, None) == 1
+    assert g(FAKE, 8, 6, FAKE, 4, FAKE, None) == 2                               # rows of 6 bytes
+    assert g(FAKE, 8, 64, FAKE + 2, 4, FAKE, None) == 3                          # misaligned ids
+    assert g(FAKE + 4, 8, 2048, FAKE, 4, FAKE, None) == 3                        # 16-byte rows need 16-byte bases
+    assert sel(None, 4, 1024, None, FAKE, None) == 1
+    assert sel(FAKE, 0, 1024, None, FAKE, None) == 1
+    assert sel(FAKE, 4, 1, None, FAKE, None) == 2
+    assert sel(FAKE + 8, 4, 1024, None, FAKE, None) == 3
+    assert sel(FAKE, 4, 1024, FAKE + 1, FAKE, None) == 3
+
+
 def test_product_path_has_no_fallback():
     """The binding never imports the oracle and fails loudly without the library."""
     from quantized_speculative_decoding_qspec_gb300 import qspec as q

@@ -101,6 +101,22 @@ def test_select_sampling(q, R, V, flat):
     assert exact >= R - max(1, R // 16)
 
 
+def test_select_degenerate_rows(q):
+    # a row of only -inf gives token 0 (the documented choice: the distribution is undefined); a
+    # single finite value is chosen by both rules whatever the uniform
+    V = 4096
+    L = np.full((3, V), -np.inf, dtype=np.float32)
+    L[1, 1234] = -3.0
+    L[2, V - 1] = 7.0
+    bits = syn.f32_to_bf16_bits(L)
+    tok = torch.empty(3, dtype=torch.int32, device=DEV)
+    q.qspec_select_tokens(bf16_dev(bits), tok)
+    assert tok.cpu().numpy().tolist() == [0, 1234, V - 1]
+    q.qspec_select_tokens(bf16_dev(bits), tok, u=f32_dev(np.array([0.5, 0.999, 0.0], np.float32)))
+    q.qspec_check_status()
+    assert tok.cpu().numpy().tolist() == [0, 1234, V - 1]
+
+
 # ---------------------------------------------------------------- the toy model and the loop
 
 def small_model(dec, V=1000, workload_id=3):

@@ -113,6 +113,11 @@ def test_linear_staging_widths(q, M, N, K):
     linear_case(q, M, N, K)
 
 
+def test_linear_maximum_tokens(q):
+    # the largest M the boundary accepts (4096 tokens), a ragged N tail, both modes
+    linear_case(q, 4096, 40, 256)
+
+
 def test_w4a4_extreme_codes(q):
     # -8 codes in the weights (not produced by the packer but accepted), +-7 activations everywhere
     N, K, M = 16, 256, 2

@@ -50,6 +50,7 @@ typedef enum {
 #define QSPEC_MAX_M 4096            /* tokens per linear call                                    */
 #define QSPEC_MAX_GAMMA 16          /* draft length                                              */
 #define QSPEC_MAX_V (1 << 24)       /* vocabulary                                                */
+#define QSPEC_MAX_TREE 64           /* candidate nodes of a verification tree                    */
 
 /*
  * qspec_pack_weights -- symmetric per-group INT4 weight quantiser and packer (step a1).
@@ -228,6 +229,35 @@ qspec_status qspec_verify_top1(const uint16_t* tgt_logits, const uint16_t* draft
                                int32_t gamma, int32_t V, int32_t* tgt_top1, int32_t* draft_top1,
                                float* tgt_p1, float* draft_p1, float high, double* tally, void* ws,
                                size_t ws_bytes, qspec_stream_t stream);
+
+/*
+ * qspec_verify_tree_greedy -- greedy verification of a tree of candidates (step f4).
+ *
+ * The speculative-decoding-with-quantisation summary (aibr.jp), sections "先行研究との差別化
+ * ポイント" and "中核となる技術的要素", names tree-style verification (candidates expanded as a tree;
+ * its cost grows exponentially with the tree) without giving an algorithm.  This is the greedy rule
+ * of qspec_verify_greedy carried over from a chain to a tree: node j (j < T) holds token
+ * tree_tok[b,j] and parent tree_parent[b,j] (-1: the committed prefix; otherwise an earlier node,
+ * parent < j).  Target row 0 scores the token after the prefix, row j + 1 the token after node j.
+ *     t[r]  = argmax_v tgt_logits[b,r,v]                 (lowest index among equal maxima)
+ *     walk: cur = prefix (row 0); while some child j of cur has tree_tok[b,j] == t[row of cur]:
+ *           accept the lowest-index such j, cur = j (row j + 1)
+ *     out[b] = (tokens of the accepted path, t[row where the walk stopped], -1, ...)
+ * A chain (parent j - 1) reproduces qspec_verify_greedy.
+ *
+ *   tgt_logits   [B, T+1, V] bf16;  tree_tok, tree_parent [B, T] int32
+ *   accept_len   [B] int32 (output) -- accepted nodes (depth of the path)
+ *   out_tok      [B, T+1] int32 (output);  accept_nodes [B, T] int32 (output, node ids, -1 fill) or NULL
+ *   ws, ws_bytes device workspace, >= qspec_verify_tree_workspace_size(B, T, V), zero-filled once;
+ *                qspec_check_status(ws) reports invalid nodes (token outside [0, V) or a parent not in
+ *                [-1, j-1]) as QSPEC_ERR_INVALID_ARG; such nodes never match.
+ *   1 <= B, 1 <= T <= QSPEC_MAX_TREE, 2 <= V <= 2^24, B*(T+1)*V < 2^40.  Bit-exact.
+ */
+size_t qspec_verify_tree_workspace_size(int32_t B, int32_t T, int32_t V);
+qspec_status qspec_verify_tree_greedy(const uint16_t* tgt_logits, const int32_t* tree_tok,
+                                      const int32_t* tree_parent, int32_t B, int32_t T, int32_t V,
+                                      int32_t* accept_len, int32_t* out_tok, int32_t* accept_nodes,
+                                      void* ws, size_t ws_bytes, qspec_stream_t stream);
 
 /*
  * qspec_verify_greedy_noalloc -- qspec_verify_greedy for callers that cannot allocate device memory.

@@ -300,6 +300,48 @@ def verify_greedy(tgt_bits, draft_tok):
 
 
 # ----------------------------------------------------------------------------------------------
+# f4: tree verification (greedy)   [SD+Q summary] "先行研究との差別化ポイント", "中核となる技術的要素"
+#     name tree-style verification without an algorithm; this is the greedy rule on a tree
+# ----------------------------------------------------------------------------------------------
+
+
+def verify_tree_greedy(tgt_bits, tree_tok, tree_parent):
+    """Greedy verification of a candidate tree per sequence.
+
+    tgt_bits: bf16 bits [B, T+1, V] (row 0: the token after the committed prefix; row j+1: the token
+    after node j); tree_tok, tree_parent int [B, T] (parent -1 is the prefix, otherwise an earlier
+    node).  From the prefix, repeatedly accept the lowest-index child whose token equals the target's
+    most likely token at the current row; stop when no child matches and emit the target's token.
+    Nodes with a token outside [0, V) or a parent outside [-1, j-1] never match.
+    Returns (accept_len int32 [B], out_tok int32 [B, T+1] (-1 fill), accept_nodes int32 [B, T] (-1 fill)).
+    """
+    L = bf16_to_f32(tgt_bits)
+    B, R, V = L.shape
+    T = R - 1
+    tok = np.asarray(tree_tok)
+    par = np.asarray(tree_parent)
+    n = np.zeros(B, dtype=np.int32)
+    out = np.full((B, R), -1, dtype=np.int32)
+    nodes = np.full((B, T), -1, dtype=np.int32)
+    for b in range(B):
+        t = [first_argmax(L[b, r]) for r in range(R)]
+        valid = [0 <= int(tok[b, j]) < V and -1 <= int(par[b, j]) < j for j in range(T)]
+        cur, row, path = -1, 0, []
+        while True:
+            children = [j for j in range(T) if valid[j] and int(par[b, j]) == cur and int(tok[b, j]) == t[row]]
+            if not children:
+                break
+            cur = min(children)
+            path.append(cur)
+            row = cur + 1
+        n[b] = len(path)
+        out[b, :len(path)] = [int(tok[b, j]) for j in path]
+        out[b, len(path)] = t[row]
+        nodes[b, :len(path)] = path
+    return n, out, nodes
+
+
+# ----------------------------------------------------------------------------------------------
 # a7, a8: sampling verify  [SD-tutorial] "samplingでもtargetの確率分布を保つ", eq. a(x), eq. p'(x)
 # ----------------------------------------------------------------------------------------------
 

@@ -798,6 +798,116 @@ __global__ void __launch_bounds__(kThreads) top1_kernel(const uint16_t* __restri
   }
 }
 
+// ------------------------------------------------------------------ tree verification (greedy)
+
+// Candidates form a tree instead of a chain: node j holds a token and its parent (-1: the committed
+// prefix, else an earlier node), target row 0 scores the token after the prefix and row j + 1 the
+// token after node j.  Greedy: from the prefix, follow the child whose token equals the target's
+// most likely token at the current row (the lowest-index child if several), as long as one exists;
+// the target's token where the walk stops is emitted after the accepted path.
+struct TreeLayout {
+  Plan p;
+  size_t err, cnt, part, total;
+};
+
+TreeLayout tree_layout(int B, int T, int V) {
+  TreeLayout L;
+  L.p = plan_rows(int64_t(B) * (T + 1), V);
+  size_t off = 0;
+  L.err = off;  off += 256;  // first: qspec_check_status reads the error word at the start
+  L.cnt = off;  off = align256(off + sizeof(unsigned int) * B);
+  L.part = off; off = align256(off + sizeof(float2) * size_t(B) * (T + 1) * L.p.chunks);
+  L.total = off;
+  return L;
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) tree_kernel(const uint16_t* __restrict__ L,
+                                                        const int32_t* __restrict__ tok,
+                                                        const int32_t* __restrict__ parent, int T, int V,
+                                                        Plan plan, unsigned int* __restrict__ err,
+                                                        unsigned int* __restrict__ cnt, float2* __restrict__ part,
+                                                        int32_t* __restrict__ accept_len,
+                                                        int32_t* __restrict__ out_tok,
+                                                        int32_t* __restrict__ accept_nodes) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t row = blockIdx.x / plan.chunks;
+  const int c = blockIdx.x % plan.chunks;
+  const int beg = c * plan.chunk_len;
+  const int end = min(V, beg + plan.chunk_len);
+  float bv = -INFINITY;
+  int bi = INT_MAX;
+  scan_argmax<kVec>(L + row * V, beg, end, bv, bi);
+  block_argmax(bv, bi);
+
+  __shared__ bool s_last;
+  const int R = T + 1;
+  const int b = static_cast<int>(row / R);
+  if (threadIdx.x == 0) {
+    part[row * plan.chunks + c] = make_float2(bv, __int_as_float(bi));
+    __threadfence();
+    const unsigned int prev = atomicAdd(cnt + b, 1u);
+    s_last = prev == static_cast<unsigned int>(R * plan.chunks - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  __shared__ int s_t[QSPEC_MAX_TREE + 1];
+  __shared__ int s_tok[QSPEC_MAX_TREE], s_par[QSPEC_MAX_TREE];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < R; i += kThreads / 32) {
+    const int64_t r = int64_t(b) * R + i;
+    float v = -INFINITY;
+    int k = INT_MAX;
+    for (int cc = lane; cc < plan.chunks; cc += 32) {
+      const float2 pp = __ldcg(part + r * plan.chunks + cc);
+      argmax_take(v, k, pp.x, __float_as_int(pp.y));
+    }
+    warp_argmax(v, k);
+    if (lane == 0) s_t[i] = k;
+  }
+  for (int j = threadIdx.x; j < T; j += kThreads) {
+    const int x = tok[int64_t(b) * T + j], p = parent[int64_t(b) * T + j];
+    const bool ok = x >= 0 && x < V && p >= -1 && p < j;  // parents come before their children
+    if (!ok) atomicOr(err, kErrBadToken);
+    s_tok[j] = ok ? x : -1;  // an invalid node never matches
+    s_par[j] = ok ? p : -2;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // walk: lanes test the nodes in parallel; the ballot's lowest set bit is the lowest-index child
+    int cur = -1, r = 0, depth = 0;
+    for (;;) {
+      const int t = s_t[r];
+      int found = -1;
+      for (int j0 = 0; j0 < T && found < 0; j0 += 32) {
+        const int j = j0 + lane;
+        const bool hit = j < T && s_par[j] == cur && s_tok[j] == t;
+        const unsigned int m = __ballot_sync(0xFFFFFFFFu, hit);
+        if (m) found = j0 + __ffs(m) - 1;
+      }
+      if (found < 0) break;
+      if (lane == 0) {
+        out_tok[int64_t(b) * R + depth] = s_tok[found];
+        if (accept_nodes) accept_nodes[int64_t(b) * T + depth] = found;
+      }
+      ++depth;
+      cur = found;
+      r = found + 1;
+    }
+    if (lane == 0) {
+      accept_len[b] = depth;
+      out_tok[int64_t(b) * R + depth] = s_t[r];
+      cnt[b] = 0;
+    }
+    for (int k = depth + 1 + lane; k < R; k += 32) out_tok[int64_t(b) * R + k] = -1;
+    if (accept_nodes)
+      for (int k = depth + lane; k < T; k += 32) accept_nodes[int64_t(b) * T + k] = -1;
+  }
+}
+
 qspec_status check_verify_args(const void* tgt, const int32_t* d, int B, int gamma, int V,
                                const int32_t* accept_len, const int32_t* out_tok, void* ws,
                                size_t ws_bytes) {
@@ -917,6 +1027,38 @@ extern "C" qspec_status qspec_verify_top1(const uint16_t* tgt_logits, const uint
                       int(B), int(gamma), int(V), L.pt, w, tgt_top1, draft_top1, tgt_p1, draft_p1, high, tally);
   return launch_pdl(top1_kernel<false>, dim3(unsigned(blocks)), dim3(kThreads), 0, s, tgt_logits, draft_logits,
                     int(B), int(gamma), int(V), L.pt, w, tgt_top1, draft_top1, tgt_p1, draft_p1, high, tally);
+}
+
+extern "C" size_t qspec_verify_tree_workspace_size(int32_t B, int32_t T, int32_t V) {
+  if (B <= 0 || T <= 0 || T > QSPEC_MAX_TREE || V < 2 || V > QSPEC_MAX_V) return 0;
+  return tree_layout(B, T, V).total;
+}
+
+extern "C" qspec_status qspec_verify_tree_greedy(const uint16_t* tgt_logits, const int32_t* tree_tok,
+                                                 const int32_t* tree_parent, int32_t B, int32_t T, int32_t V,
+                                                 int32_t* accept_len, int32_t* out_tok, int32_t* accept_nodes,
+                                                 void* ws, size_t ws_bytes, qspec_stream_t stream) {
+  if (!tgt_logits || !tree_tok || !tree_parent || !accept_len || !out_tok) return QSPEC_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || V <= 0) return QSPEC_ERR_INVALID_ARG;
+  if (T > QSPEC_MAX_TREE || V < 2 || V > QSPEC_MAX_V || int64_t(B) * (T + 1) * int64_t(V) >= (int64_t(1) << 40))
+    return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(tgt_logits) || !aligned16(tree_tok) || !aligned16(tree_parent) || !aligned16(accept_len) ||
+      !aligned16(out_tok) || (accept_nodes && !aligned16(accept_nodes)))
+    return QSPEC_ERR_MISALIGNED;
+  if (!ws || !aligned16(ws)) return ws ? QSPEC_ERR_MISALIGNED : QSPEC_ERR_WORKSPACE;
+  const TreeLayout L = tree_layout(B, T, V);
+  if (ws_bytes < L.total) return QSPEC_ERR_WORKSPACE;
+  char* w = static_cast<char*>(ws);
+  unsigned int* err = reinterpret_cast<unsigned int*>(w + L.err);
+  unsigned int* cnt = reinterpret_cast<unsigned int*>(w + L.cnt);
+  float2* part = reinterpret_cast<float2*>(w + L.part);
+  const int64_t blocks = int64_t(B) * (T + 1) * L.p.chunks;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (V % 8 == 0)
+    return launch_pdl(tree_kernel<true>, dim3(unsigned(blocks)), dim3(kThreads), 0, s, tgt_logits, tree_tok,
+                      tree_parent, int(T), int(V), L.p, err, cnt, part, accept_len, out_tok, accept_nodes);
+  return launch_pdl(tree_kernel<false>, dim3(unsigned(blocks)), dim3(kThreads), 0, s, tgt_logits, tree_tok,
+                    tree_parent, int(T), int(V), L.p, err, cnt, part, accept_len, out_tok, accept_nodes);
 }
 
 // ------------------------------------------------------------------ allocation-free greedy verify

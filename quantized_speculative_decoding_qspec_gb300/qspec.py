@@ -41,6 +41,8 @@ SIGNATURES = {
     "qspec_verify_top1": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_float, _P, _P,
                                          ctypes.c_size_t, _P]),
     "qspec_verify_greedy_noalloc": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "qspec_verify_tree_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32]),
+    "qspec_verify_tree_greedy": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qspec_gather_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _P, _P]),
     "qspec_select_tokens": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
     "qspec_check_status": (ctypes.c_int, [_P, _P]),
@@ -240,6 +242,31 @@ def qspec_select_tokens(logits, tok, u=None, stream=None):
     _dt(logits, torch.bfloat16, "logits"); _dt(tok, torch.int32, "tok"); _dt(u, torch.float32, "u")
     R, V = logits.shape
     _check("qspec_select_tokens", load().qspec_select_tokens(_ptr(logits), R, V, _ptr(u), _ptr(tok), _stream(stream)))
+
+
+def qspec_verify_tree_workspace_size(B, T, V):
+    return int(load().qspec_verify_tree_workspace_size(B, T, V))
+
+
+def new_tree_workspace(B, T, V, device="cuda"):
+    """A zero-filled tree-verify workspace (zero once; calls keep it ready)."""
+    n = qspec_verify_tree_workspace_size(B, T, V)
+    if n == 0:
+        raise ValueError("invalid tree shape")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def qspec_verify_tree_greedy(tgt_logits, tree_tok, tree_parent, accept_len, out_tok, ws, accept_nodes=None,
+                             stream=None):
+    """Greedy verify of a candidate tree: tgt_logits bf16 [B, T+1, V], tree_tok / tree_parent int32 [B, T]."""
+    _dt(tgt_logits, torch.bfloat16, "tgt_logits"); _dt(tree_tok, torch.int32, "tree_tok")
+    _dt(tree_parent, torch.int32, "tree_parent"); _dt(accept_len, torch.int32, "accept_len")
+    _dt(out_tok, torch.int32, "out_tok"); _dt(accept_nodes, torch.int32, "accept_nodes"); _dt(ws, torch.uint8, "ws")
+    B, R, V = tgt_logits.shape
+    _check("qspec_verify_tree_greedy",
+           load().qspec_verify_tree_greedy(_ptr(tgt_logits), _ptr(tree_tok), _ptr(tree_parent), B, R - 1, V,
+                                           _ptr(accept_len), _ptr(out_tok), _ptr(accept_nodes), _ptr(ws),
+                                           ws.numel(), _stream(stream)))
 
 
 def qspec_check_status(ws=None, stream=None):

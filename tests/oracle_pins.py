@@ -402,6 +402,62 @@ def check_greedy_equivalence(o):
     assert accepted > 0 and calls < L  # the draft is useful in this toy setup
 
 
+# ---------------------------------------------------------------- f4: tree verification (greedy)
+
+def check_tree_chain_is_greedy(o):
+    # a chain (node j's parent is j - 1) is the ordinary greedy verification
+    rng = np.random.default_rng(21)
+    for trial in range(30):
+        gamma, V = int(rng.integers(1, 6)), int(rng.integers(2, 6))
+        targ = rng.integers(0, V, size=gamma + 1)
+        L = _onehot_logits([list(targ)], V)
+        d = np.where(rng.random(gamma) < 0.6, targ[:gamma], rng.integers(0, V, size=gamma))[None]
+        n, out, _ = o.verify_greedy(L, d)
+        tn, tout, nodes = o.verify_tree_greedy(L, d, np.arange(-1, gamma - 1)[None])
+        assert tn.tolist() == n.tolist() and tout.tolist() == out.tolist()
+        assert nodes[0, :n[0]].tolist() == list(range(n[0]))
+
+
+def check_tree_bruteforce(o):
+    # every tree over 4 nodes (each parent any earlier node or the prefix), tokens in {0, 1}: the
+    # accepted path is the deepest node whose whole root path matches the target's argmax of each
+    # parent row, taking the lowest-index node among equal-token siblings at every level
+    V, T = 2, 4
+    rng = np.random.default_rng(3)
+    for parents in product(*[range(-1, j) for j in range(T)]):
+        for toks in product(range(V), repeat=T):
+            targ = rng.integers(0, V, size=T + 1)
+            L = _onehot_logits([list(targ)], V)
+            n, out, nodes = o.verify_tree_greedy(L, np.array([toks]), np.array([parents]))
+            def ok(j):  # j is reached: its chain matches and it is the first matching sibling
+                p = parents[j]
+                row = 0 if p < 0 else p + 1
+                if toks[j] != targ[row]:
+                    return False
+                if any(parents[k] == p and toks[k] == toks[j] for k in range(j)):
+                    return False
+                return p < 0 or ok(p)
+            reached = [j for j in range(T) if ok(j)]
+            depth = lambda j: 1 if parents[j] < 0 else 1 + depth(parents[j])
+            last = max(reached, key=depth) if reached else None
+            want = []
+            j = last
+            while j is not None and j >= 0:
+                want.insert(0, j)
+                j = parents[j] if parents[j] >= 0 else None
+            assert nodes[0, :n[0]].tolist() == want, (parents, toks, targ)
+            stop_row = 0 if last is None else last + 1
+            assert out[0, n[0]] == targ[stop_row]
+
+
+def check_tree_invalid_nodes(o):
+    L = _onehot_logits([[1, 0, 1, 0]], 3)
+    # node 0: token out of range; node 1: parent refers forward (to node 2, whose row wants token 0);
+    # node 2: valid child of the prefix
+    n, out, nodes = o.verify_tree_greedy(L, np.array([[5, 0, 1]]), np.array([[-1, 2, -1]]))
+    assert n[0] == 1 and nodes[0].tolist() == [2, -1, -1] and out[0].tolist() == [1, 0, -1, -1]
+
+
 # ---------------------------------------------------------------- a7, a8: sampling verify
 
 def check_sampling_worked_example(o):
@@ -654,6 +710,7 @@ ALL_FAST = [
     check_greedy_tutorial_example, check_greedy_bruteforce, check_greedy_ties,
     check_greedy_equivalence, check_sampling_worked_example, check_sampling_from_logits,
     check_top1_closed_forms, check_top1_tally, check_select_token, check_toy_forward_onehot,
-    check_w4a8_quantiser, check_w4a8_linear,
+    check_w4a8_quantiser, check_w4a8_linear, check_tree_chain_is_greedy, check_tree_bruteforce,
+    check_tree_invalid_nodes,
     check_decode_loop_greedy, check_decode_loop_sampling_marginal,
 ]

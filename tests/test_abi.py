@@ -148,6 +148,18 @@ def test_decode_loop_argument_checks(lib):
     assert sel(FAKE, 4, 1024, FAKE + 1, FAKE, None) == 3
 
 
+def test_tree_argument_checks(lib):
+    t = lib.qspec_verify_tree_greedy
+    need = lib.qspec_verify_tree_workspace_size(2, 7, 1024)
+    assert need > 0 and lib.qspec_verify_tree_workspace_size(2, 65, 1024) == 0
+    assert lib.qspec_verify_tree_workspace_size(0, 7, 1024) == 0
+    assert t(FAKE, FAKE, FAKE, 2, 7, 1024, FAKE, FAKE, None, FAKE, need - 1, None) == 4
+    assert t(FAKE, None, FAKE, 2, 7, 1024, FAKE, FAKE, None, FAKE, need, None) == 1
+    assert t(FAKE, FAKE, FAKE, 2, 65, 1024, FAKE, FAKE, None, FAKE, need, None) == 2
+    assert t(FAKE, FAKE, FAKE + 4, 2, 7, 1024, FAKE, FAKE, None, FAKE, need, None) == 3
+    assert t(FAKE, FAKE, FAKE, 2, 7, 1024, FAKE, FAKE, FAKE + 8, FAKE, need, None) == 3
+
+
 def test_product_path_has_no_fallback():
     """The binding never imports the oracle and fails loudly without the library."""
     from quantized_speculative_decoding_qspec_gb300 import qspec as q

@@ -56,6 +56,11 @@ MUTATIONS = [
     ("draft does not see its own tokens", "l = draft(seq + d)", "l = draft(seq)"),
     ("toy model runs verify mode when drafting", 'y = linear_w4a4(x, Wp, S)["y"] if draft_mode else linear_w4a16(x, Wp, S)',
      "y = linear_w4a16(x, Wp, S)"),
+    ("tree walk scores a child with its own row", "children = [j for j in range(T) if valid[j] and int(par[b, j]) == cur and int(tok[b, j]) == t[row]]",
+     "children = [j for j in range(T) if valid[j] and int(par[b, j]) == cur and int(tok[b, j]) == t[j + 1]]"),
+    ("tree walk takes the highest-index sibling", "cur = min(children)", "cur = max(children)"),
+    ("tree walk ignores the parent", "children = [j for j in range(T) if valid[j] and int(par[b, j]) == cur and int(tok[b, j]) == t[row]]",
+     "children = [j for j in range(T) if valid[j] and j > cur and int(tok[b, j]) == t[row]]"),
     ("E[T] exponent off by one", "return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)",
      "return (1.0 - alpha ** gamma) / (1.0 - alpha)"),
 ]

@@ -217,6 +217,7 @@ extern "C" qspec_status qspec_linear_w4a16(const uint16_t* x, const uint8_t* Wp,
   if (st != QSPEC_OK) return st;
   if (!ws) return QSPEC_ERR_WORKSPACE;
   if (!qspec::aligned16(ws)) return QSPEC_ERR_MISALIGNED;
+  if (ws_bytes < qspec_linear_workspace_size(M, N, K)) return QSPEC_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (qspec::gemv_supported(int(M), int(N), int(K)))
     return qspec::gemv(16, x, Wp, S, int(M), int(N), int(K), y, nullptr, nullptr, nullptr, ws, s);
@@ -237,6 +238,7 @@ qspec_status linear_quantised(int abits, const uint16_t* x, const uint8_t* Wp, c
     return QSPEC_ERR_MISALIGNED;
   if (!ws) return QSPEC_ERR_WORKSPACE;
   if (!qspec::aligned16(ws)) return QSPEC_ERR_MISALIGNED;
+  if (ws_bytes < qspec_linear_workspace_size(M, N, K)) return QSPEC_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (qspec::gemv_supported(int(M), int(N), int(K)))
     return qspec::gemv(abits, x, Wp, S, int(M), int(N), int(K), y, xq_out, xs_out, acc_out, ws, s);

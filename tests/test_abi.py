@@ -77,6 +77,9 @@ def test_linear_argument_checks(lib):
     assert f4(FAKE, FAKE, FAKE, 4, 512, 256, FAKE, None, None, FAKE + 2, FAKE, W, None) == 3
     assert f4(FAKE, FAKE, FAKE, 4, 512, 384 + 1, FAKE, None, None, None, FAKE, W, None) == 2
     assert f4(FAKE, FAKE, FAKE, 4, 512, 256, FAKE, None, None, None, None, W, None) == 4
+    need = lib.qspec_linear_workspace_size(16, 264, 8192)                      # a K-chunked GEMV shape
+    assert f16(FAKE, FAKE, FAKE, 16, 264, 8192, FAKE, FAKE, need - 256, None) == 4
+    assert f4(FAKE, FAKE, FAKE, 16, 264, 8192, FAKE, None, None, None, FAKE, need - 256, None) == 4
 
 
 def test_linear_workspace_size_rejects_bad_shapes(lib):

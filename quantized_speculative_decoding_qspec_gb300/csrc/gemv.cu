@@ -48,7 +48,7 @@ qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_
   float* s_a = nullptr;
   if (qb != 0 && (M >= 4 || static_cast<long long>(M) * K > 8LL * kStageU * kThreads)) {
     if (!ws_codes(abits, M, N, K, ws, &codes, &s_a)) return QSPEC_ERR_WORKSPACE;
-    const qspec_status st = quantise_tokens(abits, x, M, K, codes, s_a, xq_out, xs_out, stream);
+    const qspec_status st = quantise_tokens(abits, x, M, K, true, codes, s_a, xq_out, xs_out, stream);
     if (st != QSPEC_OK) return st;
     x = codes;
     o.xq = nullptr;

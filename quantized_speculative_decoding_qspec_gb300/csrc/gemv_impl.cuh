@@ -18,7 +18,9 @@
 //    fragment register of mma.m16n8k16: the MMA's 16 k-slots of lane t are mapped onto the
 //    channels lane t holds (a fixed permutation of K inside the group), and the activations are
 //    staged in shared memory in exactly that order, so one 16-byte shared load gives the B
-//    fragments of two MMAs.  W4A4 stages the activation codes, as bf16 (exact), in the same place:
+//    fragments of two MMAs.  W4A4 and W4A8 multiply in fp16 instead: the weight nibbles convert
+//    without shifts to codes or 16 x codes (code_pair_f16_lo / _hi) and the activation codes are
+//    staged in the same place with those meeting a 16 x weight code divided by 16 (all exact):
 //    every product and every 128-channel sum is then a small integer, exact in the fp32 MMA
 //    accumulator, so the group sums are the exact integer sums of code * code;
 //  * per group the fp32 MMA result is scaled by s[n, g] and accumulated in fp32; K slices of a
@@ -61,14 +63,57 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// The integer-code modes (W4A4, W4A8, staged codes) multiply in fp16, whose 10-bit mantissa takes
+// a nibble at bits 0..3 or 4..7 of each half without shifting it: XOR into 1032.0 (0x6408) gives
+// 1024 + (nibble ^ 8) = 1032 + code, XOR into 1152.0 (0x6480) at bits 4..7 gives 1152 + 16 code.
+// So pairs 0 and 2 of a word (the latter after one 8-bit shift) convert to (code, code') and pairs
+// 1 and 3 to 16 (code, code'), all exact; the activation codes those pairs meet are staged divided
+// by 16 (exact in fp16), so every product is code * code exactly.  One shift per word instead of
+// three; the W4A16 mode keeps bf16 activations and the bf16 conversion above.
+__device__ __forceinline__ uint32_t code_pair_f16_lo(uint32_t w) {
+  uint32_t v;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(v) : "r"(w), "r"(0x000F000Fu), "r"(0x64086408u));
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&v), __halves2half2(__ushort_as_half(0x6408),
+                                                                                __ushort_as_half(0x6408)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t code_pair_f16_hi(uint32_t w) {  // 16 x the codes
+  uint32_t v;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(v) : "r"(w), "r"(0x00F000F0u), "r"(0x64806480u));
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&v), __halves2half2(__ushort_as_half(0x6480),
+                                                                                __ushort_as_half(0x6480)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
 
-// d += A (16 x 16, row fragments a0..a3) * B (16 x 8, column fragments b0, b1), fp32 accumulate
+// Eight activation codes (as floats) -> the staged fp16 chunk: elements 2, 3, 6, 7 (the channels of
+// pairs 1 and 3) divided by 16.
+__device__ __forceinline__ uint4 codes_to_f16_chunk(const float (&c)[8]) {
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float f = (i & 1) ? 0.0625f : 1.0f;
+    const __half2 h = __floats2half2_rn(c[2 * i] * f, c[2 * i + 1] * f);
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// d += A (16 x 16, row fragments a0..a3) * B (16 x 8, column fragments b0, b1), fp32 accumulate;
+// F16: fp16 operands (the integer-code modes), else bf16
+template <bool F16>
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (F16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
 
 // QB: activation bits of the quantised modes -- 4 (W4A4) or 8 (W4A8: the same per-token quantiser
@@ -93,7 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* __restrict__ xs_out, int32_t* __restrict__ acc_out, const float* __restrict__ s_a_in,
                 float* __restrict__ part, unsigned int* __restrict__ tick) {
   constexpr bool A4 = QB != 0;                       // activations quantised (W4A4 or W4A8)
-  constexpr bool QUANT = QB == 4 || QB == 8;         // ... here (QB == 1: x holds codes, s_a_in scales)
+  constexpr bool QUANT = QB == 4 || QB == 8;         // ... here (QB == 1: x holds the staged fp16
+                                                     // code chunks, s_a_in the scales)
   constexpr float kQmax = QB == 8 ? 127.0f : 7.0f;   // codes in [-kQmax - 1, kQmax]
   extern __shared__ __align__(16) uint8_t sm[];
   const int G = K / kGroup;
@@ -218,14 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         q8[e >> 2] |= (static_cast<uint32_t>(static_cast<int>(c[e])) & 0xFFu) << (8 * (e & 3));
       *reinterpret_cast<uint2*>(xq_out + src_of(m, v)) = make_uint2(q8[0], q8[1]);
     }
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {  // one paired conversion per two codes (exact: small integers)
-      const __nv_bfloat162 b2 = __floats2bfloat162_rn(c[2 * i], c[2 * i + 1]);
-      o[i] = *reinterpret_cast<const uint32_t*>(&b2);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
+    return codes_to_f16_chunk(c);  // exact: small integers and their sixteenths
   };
+
   auto chunk_amax = [](uint4 val) {
     return max(max(max(val.x & 0x7FFFu, (val.x >> 16) & 0x7FFFu), max(val.y & 0x7FFFu, (val.y >> 16) & 0x7FFFu)),
                max(max(val.z & 0x7FFFu, (val.z >> 16) & 0x7FFFu), max(val.w & 0x7FFFu, (val.w >> 16) & 0x7FFFu)));
@@ -352,14 +393,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             xb[nb] = make_uint4(0, 0, 0, 0);
             if (MT % 8 == 0 || g < MT) xb[nb] = xg[(j * MT + nb * 8 + g) * 4 + t];
           }
-          const uint32_t a0 = code_pair(lo[j], 0), a1 = code_pair(hi[j], 0), a2 = code_pair(lo[j], 1),
-                         a3 = code_pair(hi[j], 1);
+          if constexpr (A4) {  // integer codes: fp16, one shift per word (see code_pair_f16_lo)
+            const uint32_t l8 = lo[j] >> 8, h8 = hi[j] >> 8;
+            const uint32_t a0 = code_pair_f16_lo(lo[j]), a1 = code_pair_f16_lo(hi[j]),
+                           a2 = code_pair_f16_hi(lo[j]), a3 = code_pair_f16_hi(hi[j]);
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_16816(d[nb], a0, a1, a2, a3, xb[nb].x, xb[nb].y);
-          const uint32_t c0 = code_pair(lo[j], 2), c1 = code_pair(hi[j], 2), c2 = code_pair(lo[j], 3),
-                         c3 = code_pair(hi[j], 3);
+            for (int nb = 0; nb < NB; ++nb) mma_16816<true>(d[nb], a0, a1, a2, a3, xb[nb].x, xb[nb].y);
+            const uint32_t c0 = code_pair_f16_lo(l8), c1 = code_pair_f16_lo(h8), c2 = code_pair_f16_hi(l8),
+                           c3 = code_pair_f16_hi(h8);
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_16816(d[nb], c0, c1, c2, c3, xb[nb].z, xb[nb].w);
+            for (int nb = 0; nb < NB; ++nb) mma_16816<true>(d[nb], c0, c1, c2, c3, xb[nb].z, xb[nb].w);
+          } else {
+            const uint32_t a0 = code_pair(lo[j], 0), a1 = code_pair(hi[j], 0), a2 = code_pair(lo[j], 1),
+                           a3 = code_pair(hi[j], 1);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_16816<false>(d[nb], a0, a1, a2, a3, xb[nb].x, xb[nb].y);
+            const uint32_t c0 = code_pair(lo[j], 2), c1 = code_pair(hi[j], 2), c2 = code_pair(lo[j], 3),
+                           c3 = code_pair(hi[j], 3);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_16816<false>(d[nb], c0, c1, c2, c3, xb[nb].z, xb[nb].w);
+          }
         }
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {

@@ -22,11 +22,12 @@ qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const ui
                        int N, int K, uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out,
                        void* ws, size_t ws_bytes, cudaStream_t stream);
 
-// The per-token quantiser as its own kernel (one CTA per token): bf16 codes [M, K] and fp32 scales
-// [M], plus the optional int8 codes and scales out.  ws_codes gives the workspace's code and scale
+// The per-token quantiser as its own kernel (one CTA per token): codes [M, K] and fp32 scales [M],
+// plus the optional int8 codes and scales out.  The codes are bf16 for the tensor-core path; with
+// gemv_layout they are the GEMV's staged fp16 chunks (elements 2, 3, 6, 7 of each 8 divided by 16).  ws_codes gives the workspace's code and scale
 // buffers for a quantised mode (false for W4A16).
-qspec_status quantise_tokens(int abits, const uint16_t* x, int M, int K, uint16_t* codes, float* s_a,
-                             int8_t* xq_out, float* xs_out, cudaStream_t stream);
+qspec_status quantise_tokens(int abits, const uint16_t* x, int M, int K, bool gemv_layout, uint16_t* codes,
+                             float* s_a, int8_t* xq_out, float* xs_out, cudaStream_t stream);
 bool ws_codes(int abits, int M, int N, int K, void* ws, uint16_t** codes, float** s_a);
 
 // The largest tensor-core workspace over the three modes for one shape (the GEMV's own regions

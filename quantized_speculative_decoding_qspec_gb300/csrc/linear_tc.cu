@@ -824,7 +824,7 @@ qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const ui
     return QSPEC_ERR_CUDA;
 
   if (codes_mode) {
-    const qspec_status st = quantise_tokens(abits, x, M, K, codes, s_a, xq_out, xs_out, stream);
+    const qspec_status st = quantise_tokens(abits, x, M, K, false, codes, s_a, xq_out, xs_out, stream);
     if (st != QSPEC_OK) return st;
   }
 

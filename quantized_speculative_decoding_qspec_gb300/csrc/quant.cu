@@ -14,8 +14,10 @@ namespace {
 constexpr int kQThreads = 1024;
 
 // One CTA per token: 16-byte loads of the row for the amax (bf16 bit patterns of |x| order like the
-// values), then a second pass (from L2) writing 8 codes per 16-byte store.
-__global__ void __launch_bounds__(kQThreads) quantise_kernel(const uint16_t* __restrict__ x, int K, int qbits,
+// values), then a second pass (from L2) writing 8 codes per 16-byte store: bf16 codes for the
+// tensor-core path, or (f16 set) the GEMV's staged fp16 chunk, whose elements 2, 3, 6, 7 hold the
+// code / 16 (exact in fp16).
+__global__ void __launch_bounds__(kQThreads) quantise_kernel(const uint16_t* __restrict__ x, int K, int qbits, bool f16,
                                                              uint16_t* __restrict__ codes, float* __restrict__ s_a,
                                                              int8_t* __restrict__ xq_out, float* __restrict__ xs_out) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -68,7 +70,13 @@ __global__ void __launch_bounds__(kQThreads) quantise_kernel(const uint16_t* __r
         c0 = fminf(fmaxf(rintf(d0), -qmax - 1.0f), qmax);
         c1 = fminf(fmaxf(rintf(d1), -qmax - 1.0f), qmax);
       }
-      c[i] = static_cast<uint32_t>(f32_to_bf16_bits(c0)) | (static_cast<uint32_t>(f32_to_bf16_bits(c1)) << 16);
+      if (f16) {
+        const float f = (i & 1) ? 0.0625f : 1.0f;
+        const __half2 h = __floats2half2_rn(c0 * f, c1 * f);
+        c[i] = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        c[i] = static_cast<uint32_t>(f32_to_bf16_bits(c0)) | (static_cast<uint32_t>(f32_to_bf16_bits(c1)) << 16);
+      }
       q8[i >> 1] |= ((static_cast<uint32_t>(static_cast<int>(c0)) & 0xFFu) |
                      ((static_cast<uint32_t>(static_cast<int>(c1)) & 0xFFu) << 8))
                     << (16 * (i & 1));
@@ -80,9 +88,10 @@ __global__ void __launch_bounds__(kQThreads) quantise_kernel(const uint16_t* __r
 
 }  // namespace
 
-qspec_status quantise_tokens(int abits, const uint16_t* x, int M, int K, uint16_t* codes, float* s_a,
-                             int8_t* xq_out, float* xs_out, cudaStream_t stream) {
-  return launch_pdl(quantise_kernel, dim3(M), dim3(kQThreads), 0, stream, x, K, abits, codes, s_a, xq_out, xs_out);
+qspec_status quantise_tokens(int abits, const uint16_t* x, int M, int K, bool gemv_layout, uint16_t* codes,
+                             float* s_a, int8_t* xq_out, float* xs_out, cudaStream_t stream) {
+  return launch_pdl(quantise_kernel, dim3(M), dim3(kQThreads), 0, stream, x, K, abits, gemv_layout, codes, s_a,
+                    xq_out, xs_out);
 }
 
 }  // namespace qspec

@@ -249,25 +249,32 @@ __device__ __forceinline__ float exp2_sfu(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // The reference m of a running (m, s) need not be the maximum: s = sum exp(l - m) stays exact in
-// meaning for any m, and terms up to e^16 cannot overflow fp32 over any row.  So the reference moves
-// only when a value exceeds it by more than kSlack, which keeps the rescaling expf (and the warp
-// divergence it causes) out of the stream after the first few vectors; consumers use exp(l - m) / s.
-constexpr float kSlack = 16.0f;
+// meaning for any m, and terms up to 2^24 cannot overflow fp32 over any row.  So the eight terms of
+// a vector are taken against the current m first, and m moves only when their sum reaches 2^24 (a
+// value more than ~16.6 above m) or is not finite (m still -inf, or an infinite / NaN logit): then
+// the vector is redone against max(m, its maximum).  The common path carries no max and no branch
+// per value; consumers use exp(l - m) / s.
+constexpr float kMoveSum = 16777216.0f;  // 2^24
+
+__device__ __forceinline__ float exp_sum8(const float (&v)[8], float m) {
+  const float c = m * kLog2e;  // exp(v - m) = 2^(v log2e - m log2e), one FFMA per term
+  float t[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) t[e] = exp2_sfu(fmaf(v[e], kLog2e, -c));
+  return ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));  // pairwise: depth 3
+}
 
 __device__ __forceinline__ void ms_add8(MS& a, const float (&v)[8]) {
-  // pairwise max and sum: dependency chains of depth 3 instead of 7
-  const float m8 = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
-  if (m8 > a.m + kSlack) {
-    a.s = a.m == -INFINITY ? 0.0f : a.s * expf(a.m - m8);
-    a.m = m8;
+  float sb = exp_sum8(v, a.m);
+  if (!(sb < kMoveSum)) {
+    const float m8 = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+    if (m8 > a.m) {
+      a.s = a.m == -INFINITY ? 0.0f : a.s * expf(a.m - m8);
+      a.m = m8;
+    }
+    sb = a.m == -INFINITY ? 0.0f : exp_sum8(v, a.m);
   }
-  if (a.m != -INFINITY) {
-    const float c = a.m * kLog2e;  // exp(v - m) = 2^(v log2e - m log2e), one FFMA per term
-    float t[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) t[e] = exp2_sfu(fmaf(v[e], kLog2e, -c));
-    a.s += ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
-  }
+  a.s += sb;
 }
 
 __device__ __forceinline__ MS warp_ms(MS a) {

@@ -3,6 +3,9 @@
 Every function only marshals arguments (torch tensors -> device pointers and sizes, the current
 CUDA stream) and raises ``QSpecError`` on a non-OK status.  All computation happens in the CUDA
 library; there is no fallback of any kind -- if the library is missing, loading fails loudly.
+The sizes passed to the library come from the leading input's shape; every other tensor must hold
+at least the elements the call reads or writes (ValueError otherwise, before any launch), since
+the C ABI sees plain pointers and cannot check them itself.
 """
 from __future__ import annotations
 
@@ -108,10 +111,17 @@ def _dt(t, dtype, name):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _need(t, n, name):
+    """The library writes or reads n elements of t: refuse a smaller tensor before any launch."""
+    if t is not None and t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call needs {n}")
+
+
 def qspec_pack_weights(W, Wp, S, stream=None):
     """W bf16 [N, K] -> Wp uint8 [N, K/2], S fp16 [N, K/128] (outputs written in place)."""
     _dt(W, torch.bfloat16, "W"); _dt(Wp, torch.uint8, "Wp"); _dt(S, torch.float16, "S")
     N, K = W.shape
+    _need(Wp, N * (K // 2), "Wp"); _need(S, N * (K // 128), "S")
     _check("qspec_pack_weights", load().qspec_pack_weights(_ptr(W), N, K, _ptr(Wp), _ptr(S), _stream(stream)))
 
 
@@ -129,12 +139,18 @@ def new_linear_workspace(M, N, K, device="cuda"):
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
+def _need_linear(M, N, K, Wp, S, y, xq_out=None, xs_out=None, acc_out=None):
+    _need(Wp, N * (K // 2), "Wp"); _need(S, N * (K // 128), "S"); _need(y, M * N, "y")
+    _need(xq_out, M * K, "xq_out"); _need(xs_out, M, "xs_out"); _need(acc_out, M * N * (K // 128), "acc_out")
+
+
 def qspec_linear_w4a16(x, Wp, S, y, ws, stream=None):
     """y bf16 [M, N] = x bf16 [M, K] . dequant(Wp, S)^T."""
     _dt(x, torch.bfloat16, "x"); _dt(Wp, torch.uint8, "Wp"); _dt(S, torch.float16, "S"); _dt(y, torch.bfloat16, "y")
     _dt(ws, torch.uint8, "ws")
     M, K = x.shape
     N = Wp.shape[0]
+    _need_linear(M, N, K, Wp, S, y)
     _check("qspec_linear_w4a16",
            load().qspec_linear_w4a16(_ptr(x), _ptr(Wp), _ptr(S), M, N, K, _ptr(y), _ptr(ws), ws.numel(),
                                      _stream(stream)))
@@ -147,6 +163,7 @@ def qspec_linear_w4a4(x, Wp, S, y, ws, xq_out=None, xs_out=None, acc_out=None, s
     _dt(ws, torch.uint8, "ws")
     M, K = x.shape
     N = Wp.shape[0]
+    _need_linear(M, N, K, Wp, S, y, xq_out, xs_out, acc_out)
     _check("qspec_linear_w4a4",
            load().qspec_linear_w4a4(_ptr(x), _ptr(Wp), _ptr(S), M, N, K, _ptr(y), _ptr(xq_out), _ptr(xs_out),
                                     _ptr(acc_out), _ptr(ws), ws.numel(), _stream(stream)))
@@ -159,6 +176,7 @@ def qspec_linear_w4a8(x, Wp, S, y, ws, xq_out=None, xs_out=None, acc_out=None, s
     _dt(ws, torch.uint8, "ws")
     M, K = x.shape
     N = Wp.shape[0]
+    _need_linear(M, N, K, Wp, S, y, xq_out, xs_out, acc_out)
     _check("qspec_linear_w4a8",
            load().qspec_linear_w4a8(_ptr(x), _ptr(Wp), _ptr(S), M, N, K, _ptr(y), _ptr(xq_out), _ptr(xs_out),
                                     _ptr(acc_out), _ptr(ws), ws.numel(), _stream(stream)))
@@ -168,12 +186,18 @@ def qspec_verify_workspace_size(B, gamma, V):
     return int(load().qspec_verify_workspace_size(B, gamma, V))
 
 
+def _need_greedy(B, G1, draft_tok, accept_len, out_tok, tgt_argmax):
+    _need(draft_tok, B * (G1 - 1), "draft_tok"); _need(accept_len, B, "accept_len")
+    _need(out_tok, B * G1, "out_tok"); _need(tgt_argmax, B * G1, "tgt_argmax")
+
+
 def qspec_verify_greedy(tgt_logits, draft_tok, accept_len, out_tok, ws, tgt_argmax=None, stream=None):
     """Greedy verify: tgt_logits bf16 [B, gamma+1, V], draft_tok int32 [B, gamma]."""
     _dt(tgt_logits, torch.bfloat16, "tgt_logits"); _dt(draft_tok, torch.int32, "draft_tok")
     _dt(accept_len, torch.int32, "accept_len"); _dt(out_tok, torch.int32, "out_tok")
     _dt(tgt_argmax, torch.int32, "tgt_argmax"); _dt(ws, torch.uint8, "ws")
     B, G1, V = tgt_logits.shape
+    _need_greedy(B, G1, draft_tok, accept_len, out_tok, tgt_argmax)
     _check("qspec_verify_greedy",
            load().qspec_verify_greedy(_ptr(tgt_logits), _ptr(draft_tok), B, G1 - 1, V, _ptr(accept_len),
                                       _ptr(out_tok), _ptr(tgt_argmax), _ptr(ws), ws.numel(), _stream(stream)))
@@ -185,6 +209,7 @@ def qspec_verify_greedy_noalloc(tgt_logits, draft_tok, accept_len, out_tok, tgt_
     _dt(accept_len, torch.int32, "accept_len"); _dt(out_tok, torch.int32, "out_tok")
     _dt(tgt_argmax, torch.int32, "tgt_argmax")
     B, G1, V = tgt_logits.shape
+    _need_greedy(B, G1, draft_tok, accept_len, out_tok, tgt_argmax)
     _check("qspec_verify_greedy_noalloc",
            load().qspec_verify_greedy_noalloc(_ptr(tgt_logits), _ptr(draft_tok), B, G1 - 1, V, _ptr(accept_len),
                                               _ptr(out_tok), _ptr(tgt_argmax), _stream(stream)))
@@ -200,6 +225,11 @@ def qspec_verify_sample(tgt_logits, draft_logits, draft_tok, u_accept, u_resampl
     for name, t in (("accept_prob", accept_prob), ("p_tok", p_tok), ("q_tok", q_tok)):
         _dt(t, torch.float32, name)
     B, G1, V = tgt_logits.shape
+    g = G1 - 1
+    _need(draft_logits, B * g * V, "draft_logits"); _need(draft_tok, B * g, "draft_tok")
+    _need(u_accept, B * g, "u_accept"); _need(u_resample, B * G1, "u_resample")
+    _need(accept_len, B, "accept_len"); _need(out_tok, B * G1, "out_tok")
+    _need(accept_prob, B * g, "accept_prob"); _need(p_tok, B * g, "p_tok"); _need(q_tok, B * g, "q_tok")
     _check("qspec_verify_sample",
            load().qspec_verify_sample(_ptr(tgt_logits), _ptr(draft_logits), _ptr(draft_tok), _ptr(u_accept),
                                       _ptr(u_resample), B, G1 - 1, V, _ptr(accept_len), _ptr(out_tok),
@@ -218,6 +248,10 @@ def qspec_verify_top1(tgt_logits, draft_logits, tgt_top1, draft_top1, ws, tgt_p1
     if tally is not None and tally.numel() < 8:
         raise ValueError("tally needs 8 fp64 entries")
     B, G1, V = tgt_logits.shape
+    g = G1 - 1
+    _need(draft_logits, B * g * V, "draft_logits")
+    _need(tgt_top1, B * g, "tgt_top1"); _need(draft_top1, B * g, "draft_top1")
+    _need(tgt_p1, B * g, "tgt_p1"); _need(draft_p1, B * g, "draft_p1")
     _check("qspec_verify_top1",
            load().qspec_verify_top1(_ptr(tgt_logits), _ptr(draft_logits), B, G1 - 1, V, _ptr(tgt_top1),
                                     _ptr(draft_top1), _ptr(tgt_p1), _ptr(draft_p1), float(high), _ptr(tally),
@@ -241,6 +275,7 @@ def qspec_select_tokens(logits, tok, u=None, stream=None):
     """Next token per row of bf16 logits [R, V]: argmax when u is None, else an inverse-CDF draw with u [R]."""
     _dt(logits, torch.bfloat16, "logits"); _dt(tok, torch.int32, "tok"); _dt(u, torch.float32, "u")
     R, V = logits.shape
+    _need(tok, R, "tok"); _need(u, R, "u")
     _check("qspec_select_tokens", load().qspec_select_tokens(_ptr(logits), R, V, _ptr(u), _ptr(tok), _stream(stream)))
 
 
@@ -263,6 +298,9 @@ def qspec_verify_tree_greedy(tgt_logits, tree_tok, tree_parent, accept_len, out_
     _dt(tree_parent, torch.int32, "tree_parent"); _dt(accept_len, torch.int32, "accept_len")
     _dt(out_tok, torch.int32, "out_tok"); _dt(accept_nodes, torch.int32, "accept_nodes"); _dt(ws, torch.uint8, "ws")
     B, R, V = tgt_logits.shape
+    T = R - 1
+    _need(tree_tok, B * T, "tree_tok"); _need(tree_parent, B * T, "tree_parent")
+    _need(accept_len, B, "accept_len"); _need(out_tok, B * R, "out_tok"); _need(accept_nodes, B * T, "accept_nodes")
     _check("qspec_verify_tree_greedy",
            load().qspec_verify_tree_greedy(_ptr(tgt_logits), _ptr(tree_tok), _ptr(tree_parent), B, R - 1, V,
                                            _ptr(accept_len), _ptr(out_tok), _ptr(accept_nodes), _ptr(ws),

@@ -30,6 +30,58 @@ def bf16_bits(values):
     return bits
 
 
+# ---------------------------------------------------------------- bf16 rounding of fp64 results
+#
+# Every expected W4A4 / W4A8 output and every toy-model layer output is the fp64 result rounded to
+# bf16 once (round to nearest, ties to even).  bf16 has 7 stored mantissa bits and fp32's exponent
+# range: the spacing is 2^-7 on [1, 2), the largest finite value is (2 - 2^-7) * 2^127 (0x7F7F),
+# the smallest subnormal 2^-133 (0x0001).  The expected bit patterns below are worked by hand from
+# those facts.
+
+def check_bf16_rounding(o):
+    cases = [
+        (1.0 + 2.0 ** -8, 0x3F80),                    # halfway between 1 and 1 + 2^-7: even mantissa 0
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),                # halfway between mantissas 1 and 2: up to 2
+        (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81),       # just above the tie (fp32 would round it to the tie)
+        (1.0 + 2.0 ** -8 - 2.0 ** -40, 0x3F80),       # just below the tie
+        (-(1.0 + 2.0 ** -8), 0xBF80),                 # the tie rule is symmetric in sign
+        (-(1.0 + 3 * 2.0 ** -8), 0xBF82),
+        ((2.0 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),     # the largest finite bf16 is kept
+        ((2.0 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),     # halfway to 2^128: odd mantissa 0x7F rounds up to inf
+        ((2.0 - 2.0 ** -8) * 2.0 ** 127 - 2.0 ** 100, 0x7F7F),  # just below that: the largest finite
+        (-(2.0 - 2.0 ** -8) * 2.0 ** 127, 0xFF80),
+        (2.0 ** -133, 0x0001),                        # smallest subnormal
+        (2.0 ** -134, 0x0000),                        # halfway between 0 and 2^-133: to 0 (even)
+        (3 * 2.0 ** -134, 0x0002),                    # halfway between 1 and 2 subnormal steps: to 2
+        (2.0 ** -134 + 2.0 ** -160, 0x0001),          # just above the subnormal tie
+        (-(2.0 ** -134), 0x8000),                     # a negative tie to zero keeps the sign
+        (2.0 ** -126 - 2.0 ** -134, 0x0080),          # halfway between 127 and 128 steps: the smallest normal
+        (1.5 * 2.0 ** -126 + 2.0 ** -134, 0x00C0),    # normal range at the bottom exponent: spacing 2^-133
+        (-0.0, 0x8000), (0.0, 0x0000), (np.inf, 0x7F80), (-np.inf, 0xFF80),
+        (3.0, 0x4040), (-2.0 ** 40, 0xD380), (1.0 / 3.0, 0x3EAB),  # 1/3 = 0x3EAAAAAB in fp32: up to 0x3EAB
+    ]
+    x = np.array([c[0] for c in cases], dtype=np.float64)
+    want = np.array([c[1] for c in cases], dtype=np.uint16)
+    got = np.asarray(o.f64_to_bf16_bits(x), dtype=np.uint16)
+    for xi, w, g in zip(x, want, got):
+        assert w == g, f"bf16({xi!r}) = {int(g):#06x}, expected {int(w):#06x}"
+    vals = np.asarray(o.f64_to_bf16_value(x), dtype=np.float64)
+    back = (want.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    assert np.array_equal(np.signbit(vals), np.signbit(back)) and np.array_equal(vals, back)
+
+    # values that are fp32 numbers: the textbook integer rounding of the fp32 bit pattern (add
+    # 0x7FFF plus the lowest kept bit, drop 16 bits) over random normal, subnormal and tie patterns
+    rng = np.random.default_rng(5)
+    u = rng.integers(0, 2 ** 32, size=20000, dtype=np.uint64).astype(np.uint32)
+    u[:2000] &= np.uint32(0x807FFFFF)                 # subnormal fp32 inputs
+    u[2000:4000] = (u[2000:4000] & np.uint32(0xFFFF0000)) | np.uint32(0x8000)  # exact ties
+    f = u.view(np.float32)
+    keep = np.isfinite(f) & (np.abs(f.astype(np.float64)) < (2.0 - 2.0 ** -8) * 2.0 ** 127)
+    u, f = u[keep], f[keep]
+    ref = ((u.astype(np.uint64) + 0x7FFF + ((u.astype(np.uint64) >> 16) & 1)) >> 16).astype(np.uint16)
+    assert np.array_equal(np.asarray(o.f64_to_bf16_bits(f.astype(np.float64)), dtype=np.uint16), ref)
+
+
 # ---------------------------------------------------------------- a1: weight quantiser / packer
 
 def check_pack_layout(o):
@@ -704,7 +756,7 @@ def check_top1_tally(o):
 
 
 ALL_FAST = [
-    check_pack_layout, check_weight_grid_roundtrip, check_weight_hand_cases, check_pack_end_to_end,
+    check_bf16_rounding, check_pack_layout, check_weight_grid_roundtrip, check_weight_hand_cases, check_pack_end_to_end,
     check_w4a16_onehot_and_grid, check_w4a16_error_bound, check_act_quant_hand_cases,
     check_w4a4_bruteforce, check_w4a4_extremes, check_w4a4_constant_activation, check_softmax,
     check_greedy_tutorial_example, check_greedy_bruteforce, check_greedy_ties,

@@ -11,6 +11,13 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), 
 
 # (name, text in the oracle, replacement)
 MUTATIONS = [
+    ("bf16 ties away from zero", "r = np.rint(xf / spacing) * spacing",
+     "r = np.trunc(xf / spacing + np.copysign(0.5, xf)) * spacing"),
+    ("bf16 rounded through fp32 first", "x = np.asarray(x, dtype=np.float64)\n    out = np.array(x, copy=True)",
+     "x = np.asarray(x, dtype=np.float32).astype(np.float64)\n    out = np.array(x, copy=True)"),
+    ("bf16 subnormal exponent floor off by one", "e = np.maximum(e2 - 1, -126)", "e = np.maximum(e2 - 1, -127)"),
+    ("bf16 overflows at the largest finite value", "r = np.where(np.abs(r) > bf16_max,",
+     "r = np.where(np.abs(r) >= bf16_max,"),
     ("weight divisor 8", "s32 = amax / np.float32(7.0)", "s32 = amax / np.float32(8.0)"),
     ("weight scale not fp16-rounded before coding", "s = S.astype(np.float32)[:, :, None]",
      "s = s32[:, :, None]"),

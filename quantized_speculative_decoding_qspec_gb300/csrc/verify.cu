@@ -10,6 +10,7 @@
 // keeps every SM streaming; the per-sequence combine runs in whichever CTA of the sequence finishes
 // last (an atomic ticket per sequence, no spinning).  Counters are reset by that CTA, so the
 // workspace is ready for the next call.
+#include <cuda.h>
 #include <float.h>
 #include <limits.h>
 #include <math.h>
@@ -1070,34 +1071,84 @@ extern "C" qspec_status qspec_verify_tree_greedy(const uint16_t* tgt_logits, con
 
 // ------------------------------------------------------------------ allocation-free greedy verify
 //
-// Some callers cannot allocate device memory at the point where they verify: code that runs while
-// a CUDA graph is being captured, plug-ins that execute inside another runtime's memory plan (a
-// serving engine that forbids allocation during a decode step), or plain C hosts without access to
-// an allocator.  For them, qspec_verify_greedy_noalloc uses scratch memory that lives inside this
-// library: a fixed array of device memory that every GPU loading the library holds until exit.
-// The pages have no counterpart of this; it is a deployment convenience only.
+// Some callers cannot allocate device memory at the point where they verify: plug-ins that execute
+// inside another runtime's fixed memory plan (a serving engine that forbids allocation during a
+// decode step), or plain C hosts without access to an allocator.  For them,
+// qspec_verify_greedy_noalloc uses scratch memory that lives inside this library: a fixed array of
+// device memory that every GPU loading the library holds until exit.  The pages have no counterpart
+// of this; it is a deployment convenience only.
 
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = QSPEC_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
+// The array's device address belongs to the copy of this module loaded in one CUDA context, so the
+// cache is keyed on the context's process-unique id (a context created after another was destroyed,
+// e.g. after cudaDeviceReset, gets a new id, never a stale address).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device.  cudaGetSymbolAddress runs once per
-// device, with that device current, on the first call made there.
-qspec_status noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QSPEC_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+struct CtxFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+CtxFns ctx_fns() {
+  static CtxFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return QSPEC_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  return fns;
+}
+
+// Id of the context current on this thread; false if none is current or the driver cannot say.
+bool current_ctx_id(unsigned long long* id) {
+  const CtxFns f = ctx_fns();
+  CUcontext ctx = nullptr;
+  if (!f.get_current || !f.get_id || f.get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return f.get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+constexpr int kNoAllocCacheSlots = 64;
+std::mutex g_noalloc_mu;
+unsigned long long g_noalloc_ctx[kNoAllocCacheSlots] = {};
+void* g_noalloc_ptr[kNoAllocCacheSlots] = {};
+int g_noalloc_used = 0;
+
+// Device address of the scratch array in the current context.  cudaGetSymbolAddress runs once per
+// context (normally once per device, in its primary context), with that context current, on the
+// first call made there; later calls in that context take the cached address.
+qspec_status noalloc_scratch(void** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  unsigned long long id = 0;
+  bool have_id = current_ctx_id(&id);
+  if (have_id) {
+    for (int i = 0; i < g_noalloc_used; ++i)
+      if (g_noalloc_ctx[i] == id) {
+        *out = g_noalloc_ptr[i];
+        return QSPEC_OK;
+      }
   }
-  *out = g_noalloc_ptr[dev];
+  // (the lookup also initialises the runtime's context on this thread's device if none was current)
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return QSPEC_ERR_CUDA;
+  if (!have_id) have_id = current_ctx_id(&id);
+  if (have_id && g_noalloc_used < kNoAllocCacheSlots) {  // (a full table only skips the caching)
+    g_noalloc_ctx[g_noalloc_used] = id;
+    g_noalloc_ptr[g_noalloc_used] = p;
+    ++g_noalloc_used;
+  }
+  *out = p;
   return QSPEC_OK;
 }
 

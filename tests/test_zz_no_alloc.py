@@ -1,9 +1,11 @@
 """qspec_verify_greedy_noalloc: greedy verify for callers that cannot allocate device memory.
 
-Such callers (code running during CUDA-graph capture, plug-ins inside another runtime's fixed memory
-plan, C hosts without an allocator) get an entry point whose scratch lives in a fixed device array
-inside the library.  Its outputs must equal those of the workspace-taking qspec_verify_greedy, on
-consecutive calls that reuse the shared array.  This file is collected last on purpose.
+Such callers (plug-ins inside another runtime's fixed memory plan, C hosts without an allocator) get
+an entry point whose scratch lives in a fixed device array inside the library.  Its outputs must
+equal those of the workspace-taking qspec_verify_greedy, on consecutive calls that reuse the shared
+array.  The file name sorts last so that pytest collects it after every other test: a run that stops
+at the first failure (-x) has then already run the rest of the suite when this one fails.  The tests
+also pass alone in a fresh process.
 """
 import ctypes
 

@@ -40,7 +40,7 @@ typedef enum {
   QSPEC_ERR_INVALID_ARG = 1,        /* null pointer, negative or zero size, bad token id        */
   QSPEC_ERR_UNSUPPORTED_SHAPE = 2,  /* size outside the documented limits                        */
   QSPEC_ERR_MISALIGNED = 3,         /* a base pointer is not 16-byte aligned                     */
-  QSPEC_ERR_WORKSPACE = 4,          /* workspace missing or smaller than required                */
+  QSPEC_ERR_WORKSPACE = 4,          /* workspace missing, too small, or laid out for another shape */
   QSPEC_ERR_CUDA = 5,               /* a CUDA runtime/driver call or a launch failed             */
   QSPEC_ERR_TIMEOUT = 6             /* a kernel gave up a bounded wait and returned early        */
 } qspec_status;
@@ -89,8 +89,15 @@ qspec_status qspec_pack_weights(const uint16_t* W, int64_t N, int64_t K, uint8_t
  *                 range is split between SMs, and the W4A4 activation codes.  A call leaves the
  *                 workspace ready for the next call OF THE SAME (M, N, K); its layout depends on the
  *                 shape, so calls of different shapes (for instance the layers of a model) need
- *                 workspaces of their own, or a zero-fill in between
- *   1 <= M <= 4096, N % 8 == 0, K % 128 == 0.
+ *                 workspaces of their own, or a zero-fill in between.  The workspace's header records
+ *                 the (M, N, K) of the first call that uses its regions; a later call of another shape
+ *                 that would use them touches neither the workspace nor y and makes the next
+ *                 qspec_check_status return QSPEC_ERR_WORKSPACE.  (Calls whose kernels use no region,
+ *                 such as one to three tokens on the decode-size path when K fits on chip, run on
+ *                 any large-enough workspace.)
+ *   1 <= M <= 4096, N % 8 == 0, K % 128 == 0; QSPEC_ERR_UNSUPPORTED_SHAPE for the (very large)
+ *   shapes whose tensor-core work units would not fit 32-bit counters, and QSPEC_ERR_CUDA if the
+ *   driver offers no tensor-map encoder (there is no other path).
  * The fp32 summation order depends on the device's SM count, so results are reproducible on one
  * device but may differ in the last bits between devices.
  */
@@ -263,17 +270,22 @@ qspec_status qspec_verify_tree_greedy(const uint16_t* tgt_logits, const int32_t*
  * qspec_verify_greedy_noalloc -- qspec_verify_greedy for callers that cannot allocate device memory.
  *
  * The pages have no counterpart of this entry point.  Some callers cannot call cudaMalloc where they
- * verify: code running while a CUDA graph is captured, plug-ins executing inside another runtime's
- * fixed memory plan, or C hosts with no allocator at hand.  This variant takes no workspace: its
- * scratch (error word, per-sequence tickets, per-chunk partial argmaxes) is a fixed array of
- * QSPEC_NOALLOC_SCRATCH_BYTES of device memory inside the library, which every GPU that loads the
- * library holds until the process exits.  It allocates nothing and calls no allocating routine.
+ * verify: plug-ins executing inside another runtime's fixed memory plan (a serving engine that
+ * forbids allocation during a decode step), or C hosts with no allocator at hand.  This variant takes
+ * no workspace: its scratch (error word, per-sequence tickets, per-chunk partial argmaxes) is a fixed
+ * array of QSPEC_NOALLOC_SCRATCH_BYTES of device memory inside the library, which every GPU that
+ * loads the library holds until the process exits.  It allocates nothing and calls no allocating
+ * routine.
  *
  *   Arguments and results as qspec_verify_greedy (bit-identical outputs), without ws / ws_bytes.
- *   Shapes whose scratch would exceed QSPEC_NOALLOC_SCRATCH_BYTES are rejected with
- *   QSPEC_ERR_UNSUPPORTED_SHAPE before anything is enqueued (B*(gamma+1) up to about 32 000 rows fit).
- *   The first call on a device looks up the array's device address (once per device, with that
- *   device current); make that first call before any stream capture.
+ *   Size limit: with R = B*(gamma+1) rows and C chunks per row (C = 1 once R >= 1216, otherwise at
+ *   most ceil(1216 / R) and at most ceil(V / 2048)), the call needs
+ *       256 + round_up_256(4*B) + 8*R*C  <=  QSPEC_NOALLOC_SCRATCH_BYTES
+ *   bytes; that is up to about 26 000 rows at gamma = 1 and 31 700 at gamma = 15.  Larger shapes are
+ *   rejected with QSPEC_ERR_UNSUPPORTED_SHAPE before anything is enqueued.
+ *   The first call in a CUDA context (normally once per device, in its primary context) looks up the
+ *   array's device address with that context current and caches it for the context; make that first
+ *   call before any stream capture.
  *   Every call shares the one array and clears its error word and tickets on `stream` first, so
  *   calls that overlap on the GPU (different streams, or concurrent graphs) race and must not be
  *   issued.  Draft-token range errors are not reported by qspec_check_status for this variant;
@@ -320,8 +332,9 @@ qspec_status qspec_select_tokens(const uint16_t* logits, int32_t R, int32_t V, c
  * qspec_check_status -- synchronises `stream`, then reports (and clears) the error words that the
  * kernels set on the device: the verify workspace's word when `ws` is not NULL, and the library's
  * own words for the linear and decode-loop kernels of the current device.  QSPEC_ERR_TIMEOUT if a
- * kernel gave up a bounded wait, QSPEC_ERR_INVALID_ARG if a draft token id or a gather id was out of
- * range, QSPEC_ERR_CUDA if the stream reported an error, QSPEC_OK otherwise.
+ * kernel gave up a bounded wait, QSPEC_ERR_WORKSPACE if a linear call found its workspace laid out
+ * for another shape, QSPEC_ERR_INVALID_ARG if a draft token id or a gather id was out of range,
+ * QSPEC_ERR_CUDA if the stream reported an error, QSPEC_OK otherwise.
  */
 qspec_status qspec_check_status(void* ws, qspec_stream_t stream);
 

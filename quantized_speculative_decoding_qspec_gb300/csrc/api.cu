@@ -37,7 +37,8 @@ extern "C" qspec_status qspec_check_status(void* ws, qspec_stream_t stream) {
                 cudaStreamSynchronize(s) != cudaSuccess))
       return QSPEC_ERR_CUDA;
   }
-  if (lin & 1u) return QSPEC_ERR_TIMEOUT;
+  if (lin & qspec::kErrTimeout) return QSPEC_ERR_TIMEOUT;
+  if (lin & qspec::kErrWorkspace) return QSPEC_ERR_WORKSPACE;
   if ((ver & 2u) || (dec & 4u)) return QSPEC_ERR_INVALID_ARG;
   return QSPEC_OK;
 }

@@ -26,12 +26,13 @@ size_t gemv_workspace_bytes(int M, int N, int K) {
 }
 
 qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
-                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, cudaStream_t stream) {
+                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, const WsGuard& guard,
+                  cudaStream_t stream) {
   const __half* Sh = reinterpret_cast<const __half*>(S);
   const int MT = token_slots(M), G = K / kGroup;
   const int KC = pick_kc(MT, G);
   if (KC == 0) return QSPEC_ERR_UNSUPPORTED_SHAPE;
-  Outs o{xq_out, xs_out, acc_out, nullptr, nullptr, nullptr};
+  Outs o{xq_out, xs_out, acc_out, nullptr, nullptr, nullptr, guard};
   if (KC > 1) {  // chunk partials and tickets live after the tensor-core path's regions
     char* base = static_cast<char*>(ws) + al256(linear_tc_workspace_size_all(M, N, K));
     const size_t tiles = (static_cast<size_t>(N) + 15) / 16;
@@ -48,7 +49,7 @@ qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_
   float* s_a = nullptr;
   if (qb != 0 && (M >= 4 || static_cast<long long>(M) * K > 8LL * kStageU * kThreads)) {
     if (!ws_codes(abits, M, N, K, ws, &codes, &s_a)) return QSPEC_ERR_WORKSPACE;
-    const qspec_status st = quantise_tokens(abits, x, M, K, true, codes, s_a, xq_out, xs_out, stream);
+    const qspec_status st = quantise_tokens(abits, x, M, K, true, codes, s_a, xq_out, xs_out, guard, stream);
     if (st != QSPEC_OK) return st;
     x = codes;
     o.xq = nullptr;

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ Wp, const __half* __restrict__ S,
                 int M, int N, int K, int KS, int KC_arg, uint16_t* __restrict__ y, int8_t* __restrict__ xq_out,
                 float* __restrict__ xs_out, int32_t* __restrict__ acc_out, const float* __restrict__ s_a_in,
-                float* __restrict__ part, unsigned int* __restrict__ tick) {
+                float* __restrict__ part, unsigned int* __restrict__ tick, const WsGuard guard) {
   constexpr bool A4 = QB != 0;                       // activations quantised (W4A4 or W4A8)
   constexpr bool QUANT = QB == 4 || QB == 8;         // ... here (QB == 1: x holds the staged fp16
                                                      // code chunks, s_a_in the scales)
@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float4* red = reinterpret_cast<float4*>(xs + static_cast<size_t>(Gc) * 16 * MT);  // [2][kWarps][NB][32]
   __shared__ unsigned int red_max[QUANT ? kWarps * MT : 1];
   __shared__ float s_a[MT];  // per-token scale, for the epilogue
+  __shared__ int ws_ok;      // K chunks: the workspace holds this shape's layout (or none yet)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
@@ -202,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the chunk partials and tickets live in the linear workspace; its claim is read after staging
+  if (CHUNK && threadIdx.x == 0) ws_ok = ws_claim(guard) ? 1 : 0;
 
   // Staging: chunk (gi, j, t) of token m <- x[m, 128 gi + 32 t + 8 j .. + 7].  Slots of tokens
   // M..MT-1 are never written: they only feed MMA columns that are not stored.  A thread loads its
@@ -369,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  if (CHUNK && !ws_ok) return;  // (uniform over the CTA) another shape's layout: touch nothing
 
   for (int r = 0; r < rounds; ++r) {
     const int tile = r * stride + tile0;
@@ -545,6 +549,7 @@ struct Outs {
   const float* s_in;     // codes mode: the per-token scales of the staged codes
   float* part;           // K chunks: [KC][tiles][NB][32] float4 partial tiles
   unsigned int* tick;    // K chunks: [tiles] arrival counters (zero between calls)
+  WsGuard guard;         // the workspace's layout claim
 };
 
 template <int QB, bool ACC, int MT, int D>
@@ -565,7 +570,7 @@ qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, KC, y, o.xq, o.xs, o.acc, o.s_in, o.part,
-                            o.tick) == cudaSuccess
+                            o.tick, o.guard) == cudaSuccess
              ? QSPEC_OK
              : QSPEC_ERR_CUDA;
 }

@@ -34,8 +34,59 @@
 
 namespace qspec {
 
-// Error bits set by linear kernels that give up a bounded wait (read by qspec_check_status).
+// Error bits of the linear kernels (read and cleared by qspec_check_status): kErrTimeout when a
+// kernel gave up a bounded wait, kErrWorkspace when a workspace held another shape's layout.
 __device__ unsigned int g_linear_error = 0;
+
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+std::mutex g_err_mu;
+constexpr int kErrSlots = 64;
+unsigned long long g_err_ctx[kErrSlots] = {};
+unsigned int* g_err_ptr[kErrSlots] = {};
+int g_err_used = 0;
+
+bool ctx_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+}  // namespace
+
+// The error word's address belongs to the module copy of one CUDA context: cached per context id
+// (process-unique, so a context created after another was destroyed never sees a stale address).
+unsigned int* linear_error_word() {
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  unsigned long long id = 0;
+  bool have_id = ctx_id(&id);
+  if (have_id)
+    for (int i = 0; i < g_err_used; ++i)
+      if (g_err_ctx[i] == id) return g_err_ptr[i];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_linear_error) != cudaSuccess) return nullptr;
+  if (!have_id) have_id = ctx_id(&id);
+  if (have_id && g_err_used < kErrSlots) {
+    g_err_ctx[g_err_used] = id;
+    g_err_ptr[g_err_used] = static_cast<unsigned int*>(p);
+    ++g_err_used;
+  }
+  return static_cast<unsigned int*>(p);
+}
 
 namespace {
 
@@ -66,6 +117,7 @@ __host__ __device__ constexpr int num_stages(int NM) {
 struct Misc {
   uint32_t tmem_base;
   int abort_flag;
+  int ws_bad;
   int last;
   unsigned int amax_bits[kFusedMaxM];
   float s_a[kFusedMaxM];
@@ -89,6 +141,7 @@ struct TcArgs {
   int32_t* acc_out;
   int8_t* xq_out;
   float* xs_out;
+  WsGuard guard;          // the workspace's layout claim
 };
 
 constexpr uint32_t kSuspendNs = 2000;  // hardware suspend per try_wait while a phase is incomplete
@@ -231,6 +284,9 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
     misc->abort_flag = 0;
     misc->last = 0;
     for (int i = 0; i < kFusedMaxM; ++i) misc->amax_bits[i] = 0;
+    // the workspace must hold this shape's layout (or none yet); otherwise nothing is touched.  The
+    // claim may run before the dependency wait: the header only ever goes from 0 to a tag.
+    misc->ws_bad = ws_claim(a.guard) ? 0 : 1;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -245,6 +301,10 @@ __global__ void __launch_bounds__(tc_threads(NM), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
+  if (misc->ws_bad) {  // (uniform over the CTA)
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
 
   // Programmatic dependent launch: let the next kernel start launching; wait for the previous one
   // before touching global memory.
@@ -752,7 +812,7 @@ WsLayout ws_layout(int abits, int M, int N, int K, int P) {
   const int NM = pick_nm(abits, M);
   const long long T = (static_cast<long long>(N) + 127) / 128 * ((M + NM - 1) / NM);
   WsLayout L;
-  size_t off = 0;
+  size_t off = kWsHeader;  // the layout header comes first
   L.ticket = off;  off = al256(off + sizeof(unsigned int) * T);
   L.partial = off; off = al256(off + sizeof(float) * size_t(P) * 2 * 128 * NM);
   // quantised codes and scales: used by the codes mode here, and by the GEMV when it quantises
@@ -790,7 +850,7 @@ bool linear_tc_supported(int abits, int M, int N, int K) {
   if (M < 1 || M > QSPEC_MAX_M || N < 8 || K < kGroup) return false;
   const int NM = pick_nm(abits, M);
   const long long U = (static_cast<long long>(N) + 127) / 128 * ((M + NM - 1) / NM) * (K / kGroup);
-  return U < (1LL << 31) && encode_fn() != nullptr;  // the device side counts units in 32 bits
+  return U < (1LL << 31);  // the device side counts units in 32 bits
 }
 
 size_t linear_tc_workspace_size(int abits, int M, int N, int K) {
@@ -799,7 +859,7 @@ size_t linear_tc_workspace_size(int abits, int M, int N, int K) {
 
 qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
                        uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, size_t ws_bytes,
-                       cudaStream_t stream) {
+                       const WsGuard& guard, cudaStream_t stream) {
   const int NM = pick_nm(abits, M);
   const int T_m = (M + NM - 1) / NM;
   const long long T = (static_cast<long long>(N) + 127) / 128 * T_m;
@@ -824,7 +884,7 @@ qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const ui
     return QSPEC_ERR_CUDA;
 
   if (codes_mode) {
-    const qspec_status st = quantise_tokens(abits, x, M, K, false, codes, s_a, xq_out, xs_out, stream);
+    const qspec_status st = quantise_tokens(abits, x, M, K, false, codes, s_a, xq_out, xs_out, guard, stream);
     if (st != QSPEC_OK) return st;
   }
 
@@ -845,6 +905,7 @@ qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const ui
   args.acc_out = acc_out;
   args.xq_out = xq_out;
   args.xs_out = xs_out;
+  args.guard = guard;
 
   if (abits == 16) {
     switch (NM) {

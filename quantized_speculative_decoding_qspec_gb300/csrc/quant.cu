@@ -19,7 +19,11 @@ constexpr int kQThreads = 1024;
 // code / 16 (exact in fp16).
 __global__ void __launch_bounds__(kQThreads) quantise_kernel(const uint16_t* __restrict__ x, int K, int qbits, bool f16,
                                                              uint16_t* __restrict__ codes, float* __restrict__ s_a,
-                                                             int8_t* __restrict__ xq_out, float* __restrict__ xs_out) {
+                                                             int8_t* __restrict__ xq_out, float* __restrict__ xs_out,
+                                                             const WsGuard guard) {
+  __shared__ int s_ok;
+  // the codes go to the linear workspace: it must hold this shape's layout (or none yet)
+  if (threadIdx.x == 0) s_ok = ws_claim(guard) ? 1 : 0;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int m = blockIdx.x;
@@ -37,6 +41,7 @@ __global__ void __launch_bounds__(kQThreads) quantise_kernel(const uint16_t* __r
   for (int off = 16; off >= 1; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
   if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = mx;
   __syncthreads();
+  if (!s_ok) return;  // (uniform over the CTA: written before the barrier above)
   if (threadIdx.x < 32) {
     unsigned int v = s_w[threadIdx.x];
 #pragma unroll
@@ -89,9 +94,9 @@ __global__ void __launch_bounds__(kQThreads) quantise_kernel(const uint16_t* __r
 }  // namespace
 
 qspec_status quantise_tokens(int abits, const uint16_t* x, int M, int K, bool gemv_layout, uint16_t* codes,
-                             float* s_a, int8_t* xq_out, float* xs_out, cudaStream_t stream) {
+                             float* s_a, int8_t* xq_out, float* xs_out, const WsGuard& guard, cudaStream_t stream) {
   return launch_pdl(quantise_kernel, dim3(M), dim3(kQThreads), 0, stream, x, K, abits, gemv_layout, codes, s_a,
-                    xq_out, xs_out);
+                    xq_out, xs_out, guard);
 }
 
 }  // namespace qspec

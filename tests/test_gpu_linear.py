@@ -208,3 +208,81 @@ def test_fullsize_sampled_rows(q, name):
             ulp = bf16_ulp_distance(bf16_host_bits(y)[:, rows], oracle.f64_to_bf16_bits(r["y"]))
             assert ulp.max() <= 1
     q.qspec_check_status()
+
+
+# ---- Llama-2-70B shapes above the decode sizes (the tensor-core kernel, stream-K over many SMs)
+
+LLAMA70B_TC = {"gate_up": (28672, 8192, 2), "down": (8192, 28672, 3)}  # N, K, layer index of the sweep
+
+
+@pytest.mark.parametrize("name", list(LLAMA70B_TC))
+def test_fullsize_70b_tensor_core_sampled_rows(q, name):
+    # the M = 64, 128, 256 cells of the Llama-2-70B sweep, both modes, on sampled output rows (the
+    # first and last rows always among them); every token tile and K contributor of a sampled row
+    # takes part in its value
+    N, K, li = LLAMA70B_TC[name]
+    W = syn.weights(N, K, 3, layer=li)
+    Wp, S = packed_dev(q, W)
+    rng = np.random.default_rng(N + K)
+    rows = np.unique(np.concatenate([[0, N - 1], rng.choice(N, size=126, replace=False)]))
+    Wp_ref, S_ref = oracle.pack_weights(W[rows])
+    assert np.array_equal(Wp.cpu().numpy()[rows], Wp_ref)
+    assert np.array_equal(S.cpu().numpy()[rows].view(np.uint16), S_ref.view(np.uint16))
+    rows_dev = torch.from_numpy(rows).to(DEV)
+    for M in (64, 128, 256):
+        X = syn.activations(M, K, 3, step=M)
+        x = bf16_dev(X)
+        ws = q.new_linear_workspace(M, N, K)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+        q.qspec_linear_w4a16(x, Wp, S, y, ws)
+        ref = oracle.linear_w4a16(X, Wp_ref, S_ref)
+        err = rel_fro(bf16_host_f64(y[:, rows_dev]), ref)
+        assert err <= W4A16_TOL, f"W4A16 {name} M={M}: rel err {err}"
+        y4 = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+        xs = torch.empty(M, dtype=torch.float32, device=DEV)
+        acc = torch.empty(M, N, K // 128, dtype=torch.int32, device=DEV)
+        q.qspec_linear_w4a4(x, Wp, S, y4, ws, xs_out=xs, acc_out=acc)
+        r = oracle.linear_w4a4(X, Wp_ref, S_ref)
+        assert np.array_equal(xs.cpu().numpy().view(np.uint32), r["s_a"].view(np.uint32))
+        assert np.array_equal(acc[:, rows_dev].cpu().numpy(), r["acc"]), f"W4A4 {name} M={M}: group sums"
+        ulp = bf16_ulp_distance(bf16_host_bits(y4[:, rows_dev]), oracle.f64_to_bf16_bits(r["y"]))
+        assert ulp.max() <= 1, f"W4A4 {name} M={M}: max ulp {ulp.max()}"
+        del acc
+        q.qspec_check_status()
+
+
+def test_workspace_of_another_shape_is_refused(q):
+    # A workspace records the (M, N, K) of the calls that use its regions.  W4A4 at M = 8 writes the
+    # quantised codes there; W4A16 at M = 64 (tensor-core kernel: tickets, partial sums) on the same
+    # workspace must then touch nothing and report QSPEC_ERR_WORKSPACE, leaving y as it was.
+    N, K = 264, 1024
+    W = syn.weights(N, K, 4)
+    Wp, S, Wp_ref, S_ref = check_pack(q, W)
+    Xa, Xb, X1 = syn.activations(8, K, 4, step=1), syn.activations(64, K, 4, step=2), syn.activations(1, K, 4, step=3)
+    n = max(q.qspec_linear_workspace_size(8, N, K), q.qspec_linear_workspace_size(64, N, K))
+    ws = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    ya = torch.empty(8, N, dtype=torch.bfloat16, device=DEV)
+    q.qspec_linear_w4a4(bf16_dev(Xa), Wp, S, ya, ws)
+    q.qspec_check_status()
+    yb = torch.full((64, N), 3.0, dtype=torch.bfloat16, device=DEV)
+    q.qspec_linear_w4a16(bf16_dev(Xb), Wp, S, yb, ws)
+    with pytest.raises(q.QSpecError) as e:
+        q.qspec_check_status()
+    assert q.STATUS[e.value.code] == "QSPEC_ERR_WORKSPACE"
+    assert bool((yb.float() == 3.0).all())
+    q.qspec_check_status()  # the error was reported once and cleared
+    # a zero-fill hands the workspace to the other shape: now M = 64 works and M = 8 is refused
+    ws.zero_()
+    q.qspec_linear_w4a16(bf16_dev(Xb), Wp, S, yb, ws)
+    q.qspec_check_status()
+    assert rel_fro(bf16_host_f64(yb), oracle.linear_w4a16(Xb, Wp_ref, S_ref)) <= W4A16_TOL
+    q.qspec_linear_w4a4(bf16_dev(Xa), Wp, S, ya, ws)
+    with pytest.raises(q.QSpecError) as e:
+        q.qspec_check_status()
+    assert q.STATUS[e.value.code] == "QSPEC_ERR_WORKSPACE"
+    # calls that use no region of the workspace (one token, quantised inside the GEMV) run on it
+    y1 = torch.empty(1, N, dtype=torch.bfloat16, device=DEV)
+    q.qspec_linear_w4a4(bf16_dev(X1), Wp, S, y1, ws)
+    q.qspec_check_status()
+    r = oracle.linear_w4a4(X1, Wp_ref, S_ref)
+    assert bf16_ulp_distance(bf16_host_bits(y1), oracle.f64_to_bf16_bits(r["y"])).max() <= 1

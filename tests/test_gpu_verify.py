@@ -191,3 +191,14 @@ def test_expected_tokens_on_gpu(q):
     se = T.std() / math.sqrt(B)
     assert abs(T.mean() - oracle.expected_tokens(alpha_eff, gamma)) < 4 * se
     assert np.abs(got["accept_prob"] - alpha_eff).max() < PROB_TOL
+
+
+def test_sample_parity_largest_sweep_cell(q):
+    # the largest cell of the sampling sweep: 64 sequences, gamma = 7, V = 152064 (1920 CTAs in pass 1,
+    # two vocabulary chunks per row)
+    B, gamma, V, sigma = 64, 7, 152064, 0.5
+    inp = syn.verify_inputs(B, gamma, V, sigma, workload_id=104, sampling=True)
+    got = run_sample(q, inp, reps=1)
+    ref = oracle.verify_sample(inp["tgt"], inp["drf"], inp["d"], inp["u_acc"], inp["u_res"])
+    exact = compare_sample(got, ref, inp["u_acc"])
+    assert exact >= B - max(1, B // 16)

@@ -140,6 +140,50 @@ qspec_status qspec_linear_w4a8(const uint16_t* x, const uint8_t* Wp, const uint1
                                int32_t* acc_out, void* ws, size_t ws_bytes, qspec_stream_t stream);
 
 /*
+ * qspec_linear_pass -- one launch for a pass of decode-size linears in one mode (steps a2, a3 + a4,
+ * or the W4A8 configuration of f3), e.g. every linear of a decoder layer and the lm_head.
+ *
+ * QSpec article, section "QSpec の W4A4 モードと W4A16 モード": a draft pass runs every linear of
+ * the model in W4A4 mode and a verify pass runs them in W4A16 mode, over the same packed weights.
+ * Each layer l of the pass computes exactly what qspec_linear_w4a16 / _w4a4 / _w4a8 compute for it
+ * (same definitions, same tolerances; the fp32 summation order may differ in the last bits):
+ *     y_l = x_l . dequant(Wp_l, S_l)^T          (abits = 16)
+ *     y_l = s_a . sum_g s . acc                  (abits = 4 or 8, x_l quantised per token)
+ * The layers run in order on one persistent grid (one CTA per SM): the weight stream continues
+ * across layer boundaries and the next layer's activations are copied on chip while the current
+ * layer streams.  A layer with `after` set reads what earlier layers of the pass wrote: every CTA
+ * finishes the earlier layers and waits for all others (a grid-wide barrier with an iteration limit;
+ * if it expires, the pass stops and qspec_check_status returns QSPEC_ERR_TIMEOUT).  Without `after`,
+ * a layer's x must not be the y of an earlier layer of the same pass.
+ *
+ *   abits     16 (W4A16), 4 (W4A4) or 8 (W4A8)
+ *   M         tokens, 1 <= M <= QSPEC_PASS_MAX_M (the same for every layer)
+ *   layers    HOST array of n_layers descriptors, 1 <= n_layers <= QSPEC_PASS_MAX_LAYERS; each:
+ *               x [M, K] bf16, Wp [N, K/2] uint8, S [N, K/128] fp16 (from qspec_pack_weights),
+ *               y [M, N] bf16 (output); N % 8 == 0, K % 128 == 0, and the staged activations must
+ *               fit on chip: slots(M) * K <= 102400 with slots(M) = 1, 2, 4 for M = 1, 2, 3..4
+ *               (K <= 25600 at M = 4); `reserved` must be 0
+ *   ws, ws_bytes  device workspace of >= qspec_linear_pass_workspace_size() bytes, zero-filled
+ *             before its first use (it holds the grid barrier's counters, which every pass leaves
+ *             ready for the next); passes that share a workspace must not overlap on the GPU
+ * The descriptors are read during the call (they may be reused or freed when it returns).
+ */
+#define QSPEC_PASS_MAX_LAYERS 16
+#define QSPEC_PASS_MAX_M 4
+typedef struct {
+  const uint16_t* x;
+  const uint8_t* Wp;
+  const uint16_t* S;
+  uint16_t* y;
+  int64_t N, K;
+  int32_t after;     /* nonzero: this layer reads outputs of earlier layers of the pass */
+  int32_t reserved;  /* must be 0 */
+} qspec_pass_layer;
+size_t qspec_linear_pass_workspace_size(void);
+qspec_status qspec_linear_pass(int32_t abits, int64_t M, const qspec_pass_layer* layers, int32_t n_layers,
+                               void* ws, size_t ws_bytes, qspec_stream_t stream);
+
+/*
  * qspec_linear_workspace_size -- bytes of device workspace the linear calls need for an [M, K] x
  * [N, K] product on the CURRENT device (the size depends on its SM count).  0 for invalid sizes.
  */

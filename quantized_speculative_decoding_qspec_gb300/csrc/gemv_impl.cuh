@@ -54,8 +54,12 @@ __device__ __forceinline__ uint4 ld_weights(const void* p) {
   return r;
 }
 
-// pair i of a packed word (channels 2i, 2i + 1 of its 8) -> exact bf16x2 codes
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
+// W4A16 (bf16): pair i of a packed word (channels 2i, 2i + 1 of its 8) shifted to bits 0..3 / 16..19
+// with its top bit flipped into bf16 128.0 is 128 + (nibble ^ 8) = 136 + code; one bf16x2 subtract
+// gives the exact code pair, which is directly an MMA operand register.  (Leaving the 136 in and
+// removing 136 x the group's activation sum afterwards measured slower here: the saving is one
+// subtract per pair, the price a sum per staged chunk on the critical path of every launch.)
+__device__ __forceinline__ uint32_t code_pair_bf16(uint32_t w, int i) {
   uint32_t v;
   asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(v) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(0x43084308u));
   const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v),
@@ -66,23 +70,38 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, int i) {
 // The integer-code modes (W4A4, W4A8, staged codes) multiply in fp16, whose 10-bit mantissa takes
 // a nibble at bits 0..3 or 4..7 of each half without shifting it: XOR into 1032.0 (0x6408) gives
 // 1024 + (nibble ^ 8) = 1032 + code, XOR into 1152.0 (0x6480) at bits 4..7 gives 1152 + 16 code.
-// So pairs 0 and 2 of a word (the latter after one 8-bit shift) convert to (code, code') and pairs
-// 1 and 3 to 16 (code, code'), all exact; the activation codes those pairs meet are staged divided
-// by 16 (exact in fp16), so every product is code * code exactly.  One shift per word instead of
-// three; the W4A16 mode keeps bf16 activations and the bf16 conversion above.
-__device__ __forceinline__ uint32_t code_pair_f16_lo(uint32_t w) {
+// So pairs 0 and 2 of a word (the latter after one 8-bit shift) convert to 1032 + (code, code') and
+// pairs 1 and 3 to 1152 + 16 (code, code'), all exact; the activation codes those pairs meet are
+// staged divided by 16 (exact in fp16).  The offsets stay in ("offset form": no subtraction per
+// pair): their contribution, 1032 x (activation codes of channels 0, 1, 4, 5 of every 8) + 72 x
+// (channels 2, 3, 6, 7), is computed once per (token, group) while the codes are staged and removed
+// from the MMA result.  Every product and partial sum is an integer below 2^24 (W4A8 included),
+// exact in the fp32 accumulator, and so is the offset removed: the group sums stay exact.
+__device__ __forceinline__ uint32_t off_pair_f16_lo(uint32_t w) {
   uint32_t v;
   asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(v) : "r"(w), "r"(0x000F000Fu), "r"(0x64086408u));
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&v), __halves2half2(__ushort_as_half(0x6408),
-                                                                                __ushort_as_half(0x6408)));
-  return *reinterpret_cast<const uint32_t*>(&r);
+  return v;
 }
-__device__ __forceinline__ uint32_t code_pair_f16_hi(uint32_t w) {  // 16 x the codes
+__device__ __forceinline__ uint32_t off_pair_f16_hi(uint32_t w) {
   uint32_t v;
   asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(v) : "r"(w), "r"(0x00F000F0u), "r"(0x64806480u));
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&v), __halves2half2(__ushort_as_half(0x6480),
-                                                                                __ushort_as_half(0x6480)));
-  return *reinterpret_cast<const uint32_t*>(&r);
+  return v;
+}
+
+// What the offsets add for one staged code chunk (8 channels of one token): 1032 x (elements 0, 1,
+// 4, 5) + 1152 x (elements 2, 3, 6, 7, which hold code / 16); exact.
+__device__ __forceinline__ float chunk_offset_f16(uint4 c) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&c.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&c.y));
+  const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&c.z));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&c.w));
+  return 1032.0f * ((a.x + a.y) + (e.x + e.y)) + 1152.0f * ((b.x + b.y) + (f.x + f.y));
+}
+// Sum over the 16 lanes of a half-warp (the 16 chunks of one token's 128-channel group).
+__device__ __forceinline__ float sum16(float v) {
+#pragma unroll
+  for (int off = 1; off < 16; off <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+  return v;
 }
 
 // Eight activation codes (as floats) -> the staged fp16 chunk: elements 2, 3, 6, 7 (the channels of
@@ -116,6 +135,68 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
   }
 }
 
+// One item of a warp's stream: rows (g, g + 8) of a 16-row tile x one 128-channel group x the NB
+// column blocks of 8 tokens, in 8 MMAs (the group's four 32-channel quarters j, two k16 steps each).
+// Integer-code modes (F16) keep the weight codes offset and corr (the group's [MT] offsets) removes
+// them; W4A16 converts exactly and has no offsets.
+template <bool F16, int NB, int MT>
+__device__ __forceinline__ void item_mma(float (&d)[NB][4], const uint4& wl, const uint4& wh, const uint4* xg,
+                                         const float* corr, int g, int t) {
+  const uint32_t lo[4] = {wl.x, wl.y, wl.z, wl.w};
+  const uint32_t hi[4] = {wh.x, wh.y, wh.z, wh.w};
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) d[nb][0] = d[nb][1] = d[nb][2] = d[nb][3] = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 xb[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      xb[nb] = make_uint4(0, 0, 0, 0);
+      if (MT % 8 == 0 || g < MT) xb[nb] = xg[(j * MT + nb * 8 + g) * 4 + t];
+    }
+    if constexpr (F16) {
+      const uint32_t l8 = lo[j] >> 8, h8 = hi[j] >> 8;
+      const uint32_t a0 = off_pair_f16_lo(lo[j]), a1 = off_pair_f16_lo(hi[j]), a2 = off_pair_f16_hi(lo[j]),
+                     a3 = off_pair_f16_hi(hi[j]);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) mma_16816<true>(d[nb], a0, a1, a2, a3, xb[nb].x, xb[nb].y);
+      const uint32_t c0 = off_pair_f16_lo(l8), c1 = off_pair_f16_lo(h8), c2 = off_pair_f16_hi(l8),
+                     c3 = off_pair_f16_hi(h8);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) mma_16816<true>(d[nb], c0, c1, c2, c3, xb[nb].z, xb[nb].w);
+    } else {
+      const uint32_t a0 = code_pair_bf16(lo[j], 0), a1 = code_pair_bf16(hi[j], 0), a2 = code_pair_bf16(lo[j], 1),
+                     a3 = code_pair_bf16(hi[j], 1);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) mma_16816<false>(d[nb], a0, a1, a2, a3, xb[nb].x, xb[nb].y);
+      const uint32_t c0 = code_pair_bf16(lo[j], 2), c1 = code_pair_bf16(hi[j], 2), c2 = code_pair_bf16(lo[j], 3),
+                     c3 = code_pair_bf16(hi[j], 3);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) mma_16816<false>(d[nb], c0, c1, c2, c3, xb[nb].z, xb[nb].w);
+    }
+  }
+  if constexpr (!F16) return;
+  // remove the offsets: tokens (8 nb + 2t, + 1), the same for both rows
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    const int m0 = nb * 8 + 2 * t;
+    float c0 = 0.0f, c1 = 0.0f;
+    if constexpr (MT % 2 == 0) {
+      if (m0 < MT) {
+        const float2 cc = *reinterpret_cast<const float2*>(corr + m0);
+        c0 = cc.x;
+        c1 = cc.y;
+      }
+    } else {
+      if (m0 < MT) c0 = corr[m0];
+    }
+    d[nb][0] -= c0;
+    d[nb][1] -= c1;
+    d[nb][2] -= c0;
+    d[nb][3] -= c1;
+  }
+}
+
 // QB: activation bits of the quantised modes -- 4 (W4A4) or 8 (W4A8: the same per-token quantiser
 // with divisor 127 and codes in [-128, 127], a configuration the speculative-decoding-with-
 // quantisation summary on aibr.jp names in its section "中核となる技術的要素"), 0 for W4A16.  The
@@ -123,8 +204,8 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // sums (a separate instantiation keeps their stores out of the hot loop when not asked for).
 // MT = token slots staged in shared memory (1, 2, 4, 8 or 16; tokens >= M contribute zeros); the
 // tokens form NB = ceil(MT / 8) MMA column blocks of 8 that share every weight fragment.  D = weight
-// groups in flight per warp (a divisor of the groups per K slice, so that register slots line up
-// with tile boundaries).
+// groups in flight per warp (a divisor of the groups per K slice, so that the slots line up with
+// tile boundaries).
 //
 // A warp's work is one stream of (row tile, group) items: the tiles r * stride + blockIdx.x * per_cta
 // + wtile for r = 0, 1, ..., and within each its K slice of groups.  Weights are fetched D items
@@ -186,15 +267,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   uint4 wl[D], wh[D];
   float sl[D], sh[D];
-  auto fetch = [&](int k) {  // next item of the stream into register slot k
-    wl[k] = f_vlo ? ld_weights(f_wlo + f_i * 64) : make_uint4(0, 0, 0, 0);
-    wh[k] = f_vhi ? ld_weights(f_whi + f_i * 64) : make_uint4(0, 0, 0, 0);
-    sl[k] = f_vlo ? __half2float(f_slo[f_i]) : 0.0f;
-    sh[k] = f_vhi ? __half2float(f_shi[f_i]) : 0.0f;
-    if (++f_i == gs) {
-      f_i = 0;
-      f_tile += stride;
-      point();
+  // next item of the stream into register slot k; the D slots are refilled in order and the slice
+  // length is a multiple of D, so the cursor can only leave its tile after slot D - 1
+  auto fetch = [&](int k) {
+    wl[k] = f_vlo ? ld_weights(f_wlo + (f_i + k) * 64) : make_uint4(0, 0, 0, 0);
+    wh[k] = f_vhi ? ld_weights(f_whi + (f_i + k) * 64) : make_uint4(0, 0, 0, 0);
+    sl[k] = f_vlo ? __half2float(f_slo[f_i + k]) : 0.0f;
+    sh[k] = f_vhi ? __half2float(f_shi[f_i + k]) : 0.0f;
+    if (k == D - 1) {
+      f_i += D;
+      if (f_i == gs) {
+        f_i = 0;
+        f_tile += stride;
+        point();
+      }
     }
   };
   point();
@@ -319,6 +405,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (QB == 1) {
     if (threadIdx.x < M) s_a[threadIdx.x] = s_a_in[threadIdx.x];
   }
+  // offsets the integer codes carry (see off_pair_f16_*), per (group of this chunk, token): the 16 chunks of a
+  // token's group sit on 16 consecutive lanes (the chunk order below), so every warp reduces them with
+  // four shuffles and the group's first lane writes the sum; all lanes take part (uniform loops)
+  float* corr = reinterpret_cast<float*>(red + 2 * kWarps * NB * 32);  // [Gc][MT]
+  auto put_corr = [&](int c, const uint4& staged) {
+    if constexpr (!A4) return;  // W4A16 converts its codes exactly: no offsets
+    float o = 0.0f;
+    if (c < total) o = chunk_offset_f16(staged);
+    o = sum16(o);
+    if (c < total && (lane & 15) == 0) {
+      int m, v;
+      locate(c, m, v);
+      corr[(v >> 4) * MT + m] = o;
+    }
+  };
   uint4 u[kU];
   if (total <= kU * kThreads) {
     // one batch: x stays in registers between the passes
@@ -338,36 +439,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < kU; ++e) {
       const int c = threadIdx.x + e * kThreads;
-      if (c >= total) continue;
-      int m, v;
-      locate(c, m, v);
-      xs[slot_of(m, v)] = QUANT ? quantise(m, v, u[e]) : u[e];
+      uint4 st = make_uint4(0, 0, 0, 0);
+      if (c < total) {
+        int m, v;
+        locate(c, m, v);
+        st = QUANT ? quantise(m, v, u[e]) : u[e];
+        xs[slot_of(m, v)] = st;
+      }
+      put_corr(c, st);
     }
   } else {
     // several batches: x goes to shared memory as it is, W4A4 then works there (no second trip
     // to L2)
-    for (int c0 = threadIdx.x; c0 < total; c0 += kU * kThreads) {
-      load_batch(c0, u);
+    for (int b0 = 0; b0 < total; b0 += kU * kThreads) {
+      load_batch(b0 + threadIdx.x, u);
 #pragma unroll
       for (int e = 0; e < kU; ++e) {
-        const int c = c0 + e * kThreads;
-        if (c >= total) continue;
-        int m, v;
-        locate(c, m, v);
-        xs[slot_of(m, v)] = u[e];
-        if constexpr (QUANT) {
-          if (KC == 1) amax_add(m, u[e]);
+        const int c = b0 + threadIdx.x + e * kThreads;
+        if (c < total) {
+          int m, v;
+          locate(c, m, v);
+          xs[slot_of(m, v)] = u[e];
+          if constexpr (QUANT) {
+            if (KC == 1) amax_add(m, u[e]);
+          }
         }
+        if constexpr (!QUANT) put_corr(c, u[e]);
       }
     }
     if constexpr (QUANT) {
       if (KC > 1) amax_full();
       finish_scales();
-      for (int c = threadIdx.x; c < total; c += kThreads) {
-        int m, v;
-        locate(c, m, v);
-        const int sl = slot_of(m, v);
-        xs[sl] = quantise(m, v, xs[sl]);
+      for (int c0 = 0; c0 < total; c0 += kThreads) {
+        const int c = c0 + threadIdx.x;
+        uint4 st = make_uint4(0, 0, 0, 0);
+        if (c < total) {
+          int m, v;
+          locate(c, m, v);
+          const int sl_ = slot_of(m, v);
+          st = quantise(m, v, xs[sl_]);
+          xs[sl_] = st;
+        }
+        put_corr(c, st);
       }
     }
   }
@@ -384,40 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < D; ++k) {
         const uint4* xg = xs + static_cast<size_t>(g_beg + i0 + k) * 16 * MT;
-        const uint32_t lo[4] = {wl[k].x, wl[k].y, wl[k].z, wl[k].w};
-        const uint32_t hi[4] = {wh[k].x, wh[k].y, wh[k].z, wh[k].w};
         float d[NB][4];
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) d[nb][0] = d[nb][1] = d[nb][2] = d[nb][3] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint4 xb[NB];
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            xb[nb] = make_uint4(0, 0, 0, 0);
-            if (MT % 8 == 0 || g < MT) xb[nb] = xg[(j * MT + nb * 8 + g) * 4 + t];
-          }
-          if constexpr (A4) {  // integer codes: fp16, one shift per word (see code_pair_f16_lo)
-            const uint32_t l8 = lo[j] >> 8, h8 = hi[j] >> 8;
-            const uint32_t a0 = code_pair_f16_lo(lo[j]), a1 = code_pair_f16_lo(hi[j]),
-                           a2 = code_pair_f16_hi(lo[j]), a3 = code_pair_f16_hi(hi[j]);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_16816<true>(d[nb], a0, a1, a2, a3, xb[nb].x, xb[nb].y);
-            const uint32_t c0 = code_pair_f16_lo(l8), c1 = code_pair_f16_lo(h8), c2 = code_pair_f16_hi(l8),
-                           c3 = code_pair_f16_hi(h8);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_16816<true>(d[nb], c0, c1, c2, c3, xb[nb].z, xb[nb].w);
-          } else {
-            const uint32_t a0 = code_pair(lo[j], 0), a1 = code_pair(hi[j], 0), a2 = code_pair(lo[j], 1),
-                           a3 = code_pair(hi[j], 1);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_16816<false>(d[nb], a0, a1, a2, a3, xb[nb].x, xb[nb].y);
-            const uint32_t c0 = code_pair(lo[j], 2), c1 = code_pair(hi[j], 2), c2 = code_pair(lo[j], 3),
-                           c3 = code_pair(hi[j], 3);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_16816<false>(d[nb], c0, c1, c2, c3, xb[nb].z, xb[nb].w);
-          }
-        }
+        item_mma<A4, NB, MT>(d, wl[k], wh[k], xg, corr + (g_beg + i0 + k) * MT, g, t);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
           acc[nb][0] = fmaf(sl[k], d[nb][0], acc[nb][0]);
@@ -519,9 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// dynamic shared memory for MT token slots over Gc staged groups
+// dynamic shared memory for MT token slots over Gc staged groups (activations, K-slice reduction
+// buffer, offsets of the integer-code modes)
 inline size_t smem_bytes(int MT, int Gc) {
-  return static_cast<size_t>(Gc) * 16 * MT * 16 + 2 * static_cast<size_t>(kWarps) * ((MT + 7) / 8) * 32 * 16;
+  return static_cast<size_t>(Gc) * 16 * MT * 16 + 2 * static_cast<size_t>(kWarps) * ((MT + 7) / 8) * 32 * 16 +
+         static_cast<size_t>(Gc) * MT * sizeof(float);
 }
 constexpr size_t kSmemCap = 200 * 1024;
 
@@ -575,48 +658,48 @@ qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int
              : QSPEC_ERR_CUDA;
 }
 
-template <int QB, int MT>
-qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
-                    Outs o, int KC, cudaStream_t stream) {
-  const int Gc = K / kGroup / KC;
-  const long long tiles = (static_cast<long long>(N) + 15) / 16;
+// K split among a CTA's warps: the fewest rounds of (groups per slice + fixed cost), ties to the
+// wider grid, among the splits whose slices hold a multiple of D groups; false if there is none.
+inline bool pick_ks(long long tiles, int Gc, int KC, int D, int* best_ks, int* best_grid) {
   const int chunk_grids = std::max(1, num_sms() / KC);  // CTAs per K chunk
-  // K split among a CTA's warps: the fewest rounds of (groups per slice + fixed cost), ties to
-  // the wider grid
-  int best_ks = 1, best_grid = 1;
   long long best_cost = -1;
   for (int ks = 1; ks <= kWarps; ks *= 2) {
-    if (Gc % ks != 0) continue;
+    if (Gc % ks != 0 || (Gc / ks) % D != 0) continue;
     const long long slots = kWarps / ks;
     const int grid = static_cast<int>(std::min<long long>(chunk_grids, (tiles + slots - 1) / slots));
     const long long rounds = (tiles + grid * slots - 1) / (grid * slots);
     const long long cost = rounds * (Gc / ks + 2);
-    if (best_cost < 0 || cost < best_cost || (cost == best_cost && grid > best_grid)) {
+    if (best_cost < 0 || cost < best_cost || (cost == best_cost && grid > *best_grid)) {
       best_cost = cost;
-      best_ks = ks;
-      best_grid = grid;
+      *best_ks = ks;
+      *best_grid = grid;
     }
   }
-  best_grid *= KC;
-  const int gs = Gc / best_ks;
+  return best_cost >= 0;
+}
+
+template <int QB, bool ACC, int MT, int D>
+qspec_status launch_depth(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+                          Outs o, int KC, cudaStream_t stream) {
+  int ks = 1, grid = 1;
+  const long long tiles = (static_cast<long long>(N) + 15) / 16;
+  if (!pick_ks(tiles, K / kGroup / KC, KC, D, &ks, &grid)) {
+    if constexpr (D > 1) return launch_depth<QB, ACC, MT, D / 2>(x, Wp, S, M, N, K, y, o, KC, stream);
+    return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  }
+  return launch_d<QB, ACC, MT, D>(x, Wp, S, M, N, K, y, o, ks, KC, grid * KC, stream);
+}
+
+// Groups in flight per warp (the weights wait in 8 registers per group and lane): 4 up to eight
+// tokens, 2 for sixteen (two column blocks of accumulators), 1 for 32; the checking path (int32
+// group sums out) at most 2.
+template <int QB, int MT>
+qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+                    Outs o, int KC, cudaStream_t stream) {
   if constexpr (QB != 0) {
-    if (o.acc) {  // the checking path: group sums out, no need for the deepest prefetch
-      if (MT < 32 && gs % 2 == 0)
-        return launch_d<QB, true, MT, (MT < 32 ? 2 : 1)>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
-      return launch_d<QB, true, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
-    }
+    if (o.acc) return launch_depth<QB, true, MT, (MT < 32 ? 2 : 1)>(x, Wp, S, M, N, K, y, o, KC, stream);
   }
-  // (16 token slots keep two column blocks of accumulators: at most two groups in flight then;
-  // 32 slots keep four: one)
-  if constexpr (MT >= 32) {
-    return launch_d<QB, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
-  } else {
-    if constexpr (MT < 16) {
-      if (gs % 4 == 0) return launch_d<QB, false, MT, 4>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
-    }
-    if (gs % 2 == 0) return launch_d<QB, false, MT, 2>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
-    return launch_d<QB, false, MT, 1>(x, Wp, S, M, N, K, y, o, best_ks, KC, best_grid, stream);
-  }
+  return launch_depth<QB, false, MT, (MT < 16 ? 4 : (MT < 32 ? 2 : 1))>(x, Wp, S, M, N, K, y, o, KC, stream);
 }
 
 // The modes that quantise inside the kernel (QB = 4, 8) serve at most three tokens (from four on

@@ -1,6 +1,7 @@
 // Internal interface between the linear entry points and their kernel families.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,6 +60,12 @@ size_t gemv_workspace_bytes(int M, int N, int K);  // beyond linear_tc_workspace
 qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
                   uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, const WsGuard& guard,
                   cudaStream_t stream);
+
+// A 2-D tensor map for TMA loads (dims {inner, outer} elements of type dt, row pitch row_bytes, box
+// {box_inner, box_outer}, 128-byte swizzle or none); out-of-range boxes read as zeros.  False if the
+// driver offers no encoder or rejects the arguments.
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 
 // Reads (synchronously) and clears the error bits the linear kernels set on the current device.
 qspec_status read_and_clear_linear_error(cudaStream_t stream, unsigned int* bits);

@@ -48,6 +48,8 @@ SIGNATURES = {
     "qspec_verify_tree_greedy": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qspec_gather_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _P, _P]),
     "qspec_select_tokens": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
+    "qspec_linear_pass_workspace_size": (ctypes.c_size_t, []),
+    "qspec_linear_pass": (ctypes.c_int, [_I32, _I64, _P, _I32, _P, ctypes.c_size_t, _P]),
     "qspec_check_status": (ctypes.c_int, [_P, _P]),
     "qspec_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -180,6 +182,59 @@ def qspec_linear_w4a8(x, Wp, S, y, ws, xq_out=None, xs_out=None, acc_out=None, s
     _check("qspec_linear_w4a8",
            load().qspec_linear_w4a8(_ptr(x), _ptr(Wp), _ptr(S), M, N, K, _ptr(y), _ptr(xq_out), _ptr(xs_out),
                                     _ptr(acc_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+class PassLayer(ctypes.Structure):
+    """One layer of qspec_linear_pass (the C struct qspec_pass_layer)."""
+    _fields_ = [("x", ctypes.c_void_p), ("Wp", ctypes.c_void_p), ("S", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("after", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+def qspec_linear_pass_workspace_size():
+    return int(load().qspec_linear_pass_workspace_size())
+
+
+def new_pass_workspace(device="cuda"):
+    """A zero-filled linear-pass workspace (zero once; passes keep it ready)."""
+    return torch.zeros(qspec_linear_pass_workspace_size(), dtype=torch.uint8, device=device)
+
+
+class LinearPass:
+    """A pass of decode-size linears in one mode, described once and launched with run().
+
+    layers: list of (x, Wp, S, y, after) -- x bf16 [M, K] (the same M for all), Wp uint8 [N, K/2],
+    S fp16 [N, K/128], y bf16 [M, N], after: the layer reads outputs of earlier layers of the pass.
+    abits: 16 (W4A16), 4 (W4A4) or 8 (W4A8).  The tensors must stay alive while the pass is used.
+    """
+
+    def __init__(self, abits, layers, ws):
+        _dt(ws, torch.uint8, "ws")
+        if not layers:
+            raise ValueError("a pass needs at least one layer")
+        self.M = layers[0][0].shape[0]
+        self.abits = int(abits)
+        self.ws = ws
+        self.arr = (PassLayer * len(layers))()
+        self._keep = []
+        for i, (x, Wp, S, y, after) in enumerate(layers):
+            _dt(x, torch.bfloat16, "x"); _dt(Wp, torch.uint8, "Wp"); _dt(S, torch.float16, "S")
+            _dt(y, torch.bfloat16, "y")
+            M, K = x.shape
+            if M != self.M:
+                raise ValueError("every layer of a pass has the same number of tokens")
+            N = Wp.shape[0]
+            _need_linear(M, N, K, Wp, S, y)
+            self.arr[i] = PassLayer(_ptr(x), _ptr(Wp), _ptr(S), _ptr(y), N, K, 1 if after else 0, 0)
+            self._keep += [x, Wp, S, y]
+
+    def run(self, stream=None):
+        _check("qspec_linear_pass", load().qspec_linear_pass(self.abits, self.M, self.arr, len(self.arr),
+                                                             _ptr(self.ws), self.ws.numel(), _stream(stream)))
+
+
+def qspec_linear_pass(abits, layers, ws, stream=None):
+    """One launch over a list of (x, Wp, S, y, after) linears in one mode (see LinearPass)."""
+    LinearPass(abits, layers, ws).run(stream)
 
 
 def qspec_verify_workspace_size(B, gamma, V):

@@ -170,3 +170,33 @@ def test_product_path_has_no_fallback():
     assert "oracle" not in src.replace("no fallback", "")
     with pytest.raises(RuntimeError):
         q.load(os.path.join(ROOT, "does_not_exist.so"))
+
+
+def test_linear_pass_argument_checks(lib):
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+
+    def layers(*specs):
+        arr = (q.PassLayer * len(specs))()
+        for i, (x, N, K, after, res) in enumerate(specs):
+            arr[i] = q.PassLayer(x, FAKE, FAKE, FAKE, N, K, after, res)
+        return arr
+
+    f = lib.qspec_linear_pass
+    ok = layers((FAKE, 512, 256, 0, 0), (FAKE, 64, 4096, 1, 0))
+    W = lib.qspec_linear_pass_workspace_size()
+    assert W >= 8
+    assert f(4, 1, None, 2, FAKE, W, None) == 1                 # no descriptors
+    assert f(4, 1, ok, 0, FAKE, W, None) == 1                   # no layers
+    assert f(4, 0, ok, 2, FAKE, W, None) == 1                   # no tokens
+    assert f(5, 1, ok, 2, FAKE, W, None) == 1                   # no such mode
+    assert f(16, 5, ok, 2, FAKE, W, None) == 2                  # M above QSPEC_PASS_MAX_M
+    assert f(16, 1, layers(*[(FAKE, 512, 256, 0, 0)] * 17), 17, FAKE, W, None) == 2   # too many layers
+    assert f(16, 4, layers((FAKE, 512, 25600 + 128, 0, 0)), 1, FAKE, W, None) == 2    # staging does not fit
+    assert f(16, 1, layers((FAKE, 510, 256, 0, 0)), 1, FAKE, W, None) == 2           # N % 8
+    assert f(16, 1, layers((FAKE, 512, 200, 0, 0)), 1, FAKE, W, None) == 2           # K % 128
+    assert f(16, 1, layers((None, 512, 256, 0, 0)), 1, FAKE, W, None) == 1           # null pointer
+    assert f(16, 1, layers((FAKE, 512, 256, 0, 7)), 1, FAKE, W, None) == 1           # reserved not 0
+    assert f(16, 1, layers((FAKE + 8, 512, 256, 0, 0)), 1, FAKE, W, None) == 3       # misaligned x
+    assert f(16, 1, ok, 2, None, W, None) == 4                  # no workspace
+    assert f(16, 1, ok, 2, FAKE + 8, W, None) == 3              # misaligned workspace
+    assert f(16, 1, ok, 2, FAKE, W - 1, None) == 4              # workspace too small

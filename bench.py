@@ -296,7 +296,9 @@ def gpu_arm(args, rank, world):
         torch.cuda.synchronize()
         pack_times.append(e0.elapsed_time(e1) * 1e-3)
         pack_bytes += N * K * 2 + N * K // 2 + N * (K // 128) * 2
-        packed[name] = (Wp, S, q.new_linear_workspace(GAMMA + 1, N, K, device=dev))
+        # a workspace per (layer, token count): the two modes' calls are planned per shape
+        packed[name] = (Wp, S, {1: q.new_linear_workspace(1, N, K, device=dev),
+                                GAMMA + 1: q.new_linear_workspace(GAMMA + 1, N, K, device=dev)})
         del W
     torch.cuda.empty_cache()
 
@@ -359,12 +361,12 @@ def gpu_arm(args, rank, world):
             for d in range(GAMMA):
                 for name, N, K in LAYERS:
                     Wp, S, lws = packed[name]
-                    timed(("w4a4", name), lambda: q.qspec_linear_w4a4(x1[name][d], Wp, S, y1[name], lws))
+                    timed(("w4a4", name), lambda: q.qspec_linear_w4a4(x1[name][d], Wp, S, y1[name], lws[1]))
 
         def verify_pass():
             for name, N, K in LAYERS:
                 Wp, S, lws = packed[name]
-                timed(("w4a16", name), lambda: q.qspec_linear_w4a16(x4[name], Wp, S, y4[name], lws))
+                timed(("w4a16", name), lambda: q.qspec_linear_w4a16(x4[name], Wp, S, y4[name], lws[GAMMA + 1]))
 
         family("w4a4", draft)
         family("w4a16", verify_pass)

@@ -22,7 +22,7 @@ bool gemv_supported(int M, int N, int K) {
 size_t gemv_workspace_bytes(int M, int N, int K) {
   if (!gemv_supported(M, N, K)) return 0;
   const int MT = token_slots(M), G = K / kGroup;
-  return chunk_ws_bytes(MT, N, G, pick_kc(MT, G));
+  return chunk_ws_bytes(MT, N, G, plan_kc(MT, N, G));
 }
 
 qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
@@ -30,7 +30,7 @@ qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_
                   cudaStream_t stream) {
   const __half* Sh = reinterpret_cast<const __half*>(S);
   const int MT = token_slots(M), G = K / kGroup;
-  const int KC = pick_kc(MT, G);
+  const int KC = plan_kc(MT, N, G);
   if (KC == 0) return QSPEC_ERR_UNSUPPORTED_SHAPE;
   Outs o{xq_out, xs_out, acc_out, nullptr, nullptr, nullptr, guard};
   if (KC > 1) {  // chunk partials and tickets live after the tensor-core path's regions

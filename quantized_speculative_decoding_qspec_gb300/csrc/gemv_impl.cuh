@@ -616,6 +616,59 @@ inline int pick_kc(int MT, int G) {
   return 0;
 }
 
+// K split among a CTA's warps: the fewest rounds of (groups per slice + fixed cost), ties to the
+// wider grid, among the splits whose slices hold a multiple of D groups; false if there is none.
+inline bool pick_ks(long long tiles, int Gc, int KC, int D, int* best_ks, int* best_grid, long long* cost_out = nullptr) {
+  const int chunk_grids = std::max(1, num_sms() / KC);  // CTAs per K chunk
+  long long best_cost = -1;
+  for (int ks = 1; ks <= kWarps; ks *= 2) {
+    if (Gc % ks != 0 || (Gc / ks) % D != 0) continue;
+    const long long slots = kWarps / ks;
+    const int grid = static_cast<int>(std::min<long long>(chunk_grids, (tiles + slots - 1) / slots));
+    const long long rounds = (tiles + grid * slots - 1) / (grid * slots);
+    const long long cost = rounds * (Gc / ks + 2);
+    if (best_cost < 0 || cost < best_cost || (cost == best_cost && grid > *best_grid)) {
+      best_cost = cost;
+      *best_ks = ks;
+      *best_grid = grid;
+    }
+  }
+  if (cost_out) *cost_out = best_cost;
+  return best_cost >= 0;
+}
+
+// Groups in flight per warp for MT token slots (the weights wait in 8 registers per group and lane).
+constexpr int depth_of(int MT) { return MT <= 16 ? 4 : 1; }
+
+// K chunks for up to eight token slots: besides making the staged activations fit, chunks let a
+// layer with few row tiles but long K keep more warps streaming (each warp's serial share is what
+// a latency-bound stream pays for).  Among the chunk counts that fit, the one with the fewest
+// groups per warp plus the fixup of split tiles (about 4 groups' time + a quarter per chunk, ties
+// to fewer chunks); e.g. the Llama-3-8B down layer (256 row tiles, 112 groups) at one token takes
+// seven chunks of 16 groups instead of one chunk in which only 1024 of the 2432 warps stream (28
+// groups each).  Sixteen and 32 slots keep the fewest chunks that fit.  Deterministic in (MT, N, G, SM count), so
+// the workspace size and the launch agree.
+inline int plan_kc(int MT, int N, int G) {
+  const int kc_min = pick_kc(MT, G);
+  if (kc_min == 0 || MT > 8) return kc_min;
+  const long long tiles = (static_cast<long long>(N) + 15) / 16;
+  const int D = depth_of(MT);
+  int best_kc = kc_min;
+  double best = -1.0;
+  for (int kc = kc_min; kc <= G; ++kc) {
+    if (G % kc != 0 || smem_bytes(MT, G / kc) > kSmemCap) continue;
+    int ks = 1, grid = 1;
+    long long c = 0;
+    if (!pick_ks(tiles, G / kc, kc, D, &ks, &grid, &c)) continue;
+    const double cost = static_cast<double>(c) + (kc > 1 ? 4.0 + 0.25 * kc : 0.0);
+    if (best < 0.0 || cost < best) {
+      best = cost;
+      best_kc = kc;
+    }
+  }
+  return best_kc;
+}
+
 inline size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace bytes of the chunk partials and tile tickets (0 when K is not chunked).
@@ -658,26 +711,6 @@ qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int
              : QSPEC_ERR_CUDA;
 }
 
-// K split among a CTA's warps: the fewest rounds of (groups per slice + fixed cost), ties to the
-// wider grid, among the splits whose slices hold a multiple of D groups; false if there is none.
-inline bool pick_ks(long long tiles, int Gc, int KC, int D, int* best_ks, int* best_grid) {
-  const int chunk_grids = std::max(1, num_sms() / KC);  // CTAs per K chunk
-  long long best_cost = -1;
-  for (int ks = 1; ks <= kWarps; ks *= 2) {
-    if (Gc % ks != 0 || (Gc / ks) % D != 0) continue;
-    const long long slots = kWarps / ks;
-    const int grid = static_cast<int>(std::min<long long>(chunk_grids, (tiles + slots - 1) / slots));
-    const long long rounds = (tiles + grid * slots - 1) / (grid * slots);
-    const long long cost = rounds * (Gc / ks + 2);
-    if (best_cost < 0 || cost < best_cost || (cost == best_cost && grid > *best_grid)) {
-      best_cost = cost;
-      *best_ks = ks;
-      *best_grid = grid;
-    }
-  }
-  return best_cost >= 0;
-}
-
 template <int QB, bool ACC, int MT, int D>
 qspec_status launch_depth(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
                           Outs o, int KC, cudaStream_t stream) {
@@ -699,7 +732,7 @@ qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M
   if constexpr (QB != 0) {
     if (o.acc) return launch_depth<QB, true, MT, (MT < 32 ? 2 : 1)>(x, Wp, S, M, N, K, y, o, KC, stream);
   }
-  return launch_depth<QB, false, MT, (MT < 16 ? 4 : (MT < 32 ? 2 : 1))>(x, Wp, S, M, N, K, y, o, KC, stream);
+  return launch_depth<QB, false, MT, depth_of(MT)>(x, Wp, S, M, N, K, y, o, KC, stream);
 }
 
 // The modes that quantise inside the kernel (QB = 4, 8) serve at most three tokens (from four on

@@ -175,6 +175,49 @@ def time_oracle(budget_s, frac=None):
     return nbytes, dt, frac
 
 
+def _oracle_worker(frac, q_ready, ev_go, q_out):
+    """One process of the all-cores oracle timing (started with spawn, BLAS pinned to one thread by
+    the inherited environment): build the sample, wait for the start signal, time one pass."""
+    data = oracle_inputs(frac)
+    q_ready.put(1)
+    ev_go.wait()
+    t0 = time.time()
+    nbytes = oracle_sample_step(data, frac)
+    q_out.put((t0, time.time(), nbytes))
+
+
+def time_oracle_all_cores(frac, procs):
+    """The oracle on every host core: `procs` single-threaded processes run the same row sample at
+    once; bytes of all of them / wall time from the first start to the last finish."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q_ready, q_out, ev_go = ctx.Queue(), ctx.Queue(), ctx.Event()
+    ps = [ctx.Process(target=_oracle_worker, args=(frac, q_ready, ev_go, q_out)) for _ in range(procs)]
+    import queue
+
+    def get(qq, deadline):  # a result, or an error as soon as a worker has died
+        while True:
+            try:
+                return qq.get(timeout=1.0)
+            except queue.Empty:
+                if time.time() > deadline or any(p_.exitcode not in (None, 0) for p_ in ps):
+                    for p_ in ps:
+                        if p_.is_alive():
+                            p_.terminate()
+                    raise RuntimeError("all-cores oracle timing: a worker failed")
+
+    for p_ in ps:
+        p_.start()
+    deadline = time.time() + 900
+    for _ in ps:
+        get(q_ready, deadline)
+    ev_go.set()
+    res = [get(q_out, deadline) for _ in ps]
+    for p_ in ps:
+        p_.join()
+    return sum(r[2] for r in res), max(r[1] for r in res) - min(r[0] for r in res)
+
+
 def threads_used():
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var) == "1":
@@ -473,6 +516,33 @@ def gpu_arm(args, rank, world):
                                        "TOPS": round(2 * M * N * K / t / 1e12, 3)}
     ver_t = {f: fam_time[f] for f in ("greedy", "sample")}
 
+    # ---- one decoder layer: q, k, v, o, gate, up, down back to back in one CUDA graph per mode,
+    # rotating through weight copies of at least 3x L2 (113 MB of packed weights per layer)
+    dec_layers = [l for l in LAYERS if l[0] != "lm_head"]
+    dec_bytes = {4: sum(linear_bytes(1, N, K) for _, N, K in dec_layers),
+                 16: sum(linear_bytes(GAMMA + 1, N, K) for _, N, K in dec_layers)}
+    R_dec = copies_for(dec_bytes[4])
+    dec_sets = [{n: packed[n][:2] for n, _, _ in dec_layers}]
+    dec_sets += [{n: (packed[n][0].clone(), packed[n][1].clone()) for n, _, _ in dec_layers} for _ in range(R_dec - 1)]
+    decoder_layer = {}
+    for abits, M in ((4, 1), (16, GAMMA + 1)):
+        f = q.qspec_linear_w4a4 if abits == 4 else q.qspec_linear_w4a16
+        xin = {n: (x1[n][0] if abits == 4 else x4[n]) for n, _, _ in dec_layers}
+        yout = {n: (y1[n] if abits == 4 else y4[n]) for n, _, _ in dec_layers}
+        wsd = [{n: q.new_linear_workspace(M, N, K, device=dev) for n, N, K in dec_layers} for _ in range(R_dec)]
+
+        def layer_call(i, f=f, xin=xin, yout=yout, wsd=wsd):
+            for n, _, _ in dec_layers:
+                f(xin[n], dec_sets[i][n][0], dec_sets[i][n][1], yout[n], wsd[i][n])
+
+        t_dec = _rotating_time([(lambda i=i: layer_call(i)) for i in range(R_dec)])
+        decoder_layer[f"w4a{abits}_M{M}"] = {"us": round(t_dec * 1e6, 2),
+                                              "GB_s": round(dec_bytes[abits] / t_dec / 1e9, 1),
+                                              "hbm_frac": round(dec_bytes[abits] / t_dec / 1e9 / peaks()[0], 4)}
+        del wsd
+    q.qspec_check_status()
+    del dec_sets
+
     # ---- end to end through the public API with host buffers: H2D of the step's inputs from pinned
     # memory, the calls, D2H of the verify results.  The activations go over in one copy ahead of
     # the linears; the verify inputs are copied on a second stream while the linears run and joined
@@ -574,6 +644,9 @@ def gpu_arm(args, rank, world):
             "layers_timing": f"CUDA events around every kernel in {n_kern} instrumented steps after the timed "
                              "region (separating the launches adds gaps: per-layer times are upper bounds)",
             "pack_GB_s": round(pack_bytes / sum(pack_times) / 1e9, 1),
+            "decoder_layer": decoder_layer,
+            "decoder_layer_timing": ("q, k, v, o, gate, up, down back to back in one CUDA graph, rotating through "
+                                     f"{R_dec} weight copies (at least 3x L2); W4A4 at M=1, W4A16 at M={GAMMA + 1}"),
         },
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": round(e2e_t * 1e3, 4),
@@ -657,6 +730,44 @@ def profile_case(spec, reps):
                       "note": "eager back-to-back launches; inputs resident"}))
 
 
+def l2_bytes():
+    import torch
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 129 * 2 ** 20
+
+
+def copies_for(nbytes, cap=512):
+    """Input copies whose total is at least 3x L2, so that a rotation through them reads HBM (at
+    most `cap` copies: the tiniest cells, latency-bound anyway, then rotate through less; each sweep
+    line reports the bytes its rotation covers)."""
+    return max(1, min(cap, -(-3 * l2_bytes() // max(1, nbytes))))
+
+
+def _rotating_time(calls, iters=5):
+    """Seconds per call, from CUDA-graph replays of the given calls (one per input copy, rotated so
+    that every call reads inputs no earlier call of the replay touched)."""
+    import torch
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for c in calls:
+            c()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3 / (len(calls) * iters)
+
+
 LLAMA70B = [("qo", 8192, 8192), ("kv", 1024, 8192), ("gate_up", 28672, 8192), ("down", 8192, 28672),
             ("lm_head", 32000, 8192)]
 
@@ -700,27 +811,32 @@ def sweep_linear():
         S = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
         q.qspec_pack_weights(W, Wp, S)
         del W
+        # rotate through weight copies of at least 3x L2 (the smaller layers would stay in L2)
+        R = copies_for(linear_bytes(1, N, K))
+        sets = [(Wp, S)] + [(Wp.clone(), S.clone()) for _ in range(R - 1)]
         for M in (1, 2, 4, 8, 16, 32, 64, 128, 256):
             x = torch.from_numpy(syn.activations(M, K, 3, step=M).view(np.int16)).to(dev).view(torch.bfloat16)
             y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-            ws = q.new_linear_workspace(M, N, K, device=dev)
+            wss = [q.new_linear_workspace(M, N, K, device=dev) for _ in range(R)]
             for mode in ("a16", "a4", "a8") if M in (1, 4, 16, 64) else ("a16", "a4"):
-                fn = {"a16": lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws),
-                      "a4": lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws),
-                      "a8": lambda: q.qspec_linear_w4a8(x, Wp, S, y, ws)}[mode]
-                t = _graph_time(fn)
+                f = {"a16": q.qspec_linear_w4a16, "a4": q.qspec_linear_w4a4, "a8": q.qspec_linear_w4a8}[mode]
+                t = _rotating_time([(lambda i=i: f(x, sets[i][0], sets[i][1], y, wss[i])) for i in range(R)])
                 b = linear_bytes(M, N, K)
                 print(json.dumps({"sweep": "llama70b_linear", "layer": name, "N": N, "K": K, "M": M, "mode": mode,
                                   "us": round(t * 1e6, 2), "GB_s": round(b / t / 1e9, 1),
-                                  "hbm_frac": round(b / t / 1e9 / hbm, 3),
+                                  "hbm_frac": round(b / t / 1e9 / hbm, 3), "weight_copies": R,
+                                  "rotation_bytes": R * b, "l2_bytes": l2_bytes(),
                                   "TOPS": round(2 * M * N * K / t / 1e12, 2)}), flush=True)
+            del wss
         q.qspec_check_status()
+        del sets
 
 
 def sweep_batched():
     """Batched verify (16 sequences x gamma = 3): W4A16 at M = 64 and W4A4 at M = 16 on the
     Llama-3-8B shapes, and greedy verify over [64, 128256] bf16 logits with per-sequence accept
-    lengths.  One JSON line per item."""
+    lengths.  Every cell rotates through input copies of at least 3x L2 (HBM, not L2, figures).
+    One JSON line per item."""
     import numpy as np
     import torch
 
@@ -736,33 +852,40 @@ def sweep_batched():
         S = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
         q.qspec_pack_weights(W, Wp, S)
         del W
+        R = copies_for(linear_bytes(64, N, K))
+        sets = [(Wp, S)] + [(Wp.clone(), S.clone()) for _ in range(R - 1)]
         for M, mode in ((64, "a16"), (16, "a4")):
             x = torch.from_numpy(syn.activations(M, K, 2, step=M).view(np.int16)).to(dev).view(torch.bfloat16)
-            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-            ws = q.new_linear_workspace(M, N, K, device=dev)
-            fn = ((lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws)) if mode == "a16"
-                  else (lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws)))
-            t = _graph_time(fn)
+            ys = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+            ws = [q.new_linear_workspace(M, N, K, device=dev) for _ in range(R)]
+            f = q.qspec_linear_w4a16 if mode == "a16" else q.qspec_linear_w4a4
+            t = _rotating_time([(lambda i=i: f(x, sets[i][0], sets[i][1], ys[i], ws[i])) for i in range(R)])
             b = linear_bytes(M, N, K)
             print(json.dumps({"sweep": "batched_linear", "layer": name, "N": N, "K": K, "M": M, "mode": mode,
                               "us": round(t * 1e6, 2), "GB_s": round(b / t / 1e9, 1),
-                              "hbm_frac": round(b / t / 1e9 / hbm, 3), "l2_resident": b < 100e6,
+                              "hbm_frac": round(b / t / 1e9 / hbm, 3), "weight_copies": R,
+                              "rotation_bytes": R * b, "l2_bytes": l2_bytes(),
                               "TOPS": round(2 * M * N * K / t / 1e12, 2)}), flush=True)
+            del ys, ws
         q.qspec_check_status()
-        del Wp, S
+        del Wp, S, sets
     B, gamma = 16, GAMMA
     inp = syn.verify_inputs(B, gamma, VOCAB, 0.5, workload_id=2, sampling=False)
     gt = torch.from_numpy(np.ascontiguousarray(inp["tgt"]).view(np.int16)).to(dev).view(torch.bfloat16)
     gd = torch.from_numpy(inp["d"]).to(dev)
-    gws = q.new_verify_workspace(B, gamma, VOCAB, device=dev)
+    b = verify_bytes(B, gamma, VOCAB, False)
+    R = copies_for(b)
+    gts = [gt] + [gt.clone() for _ in range(R - 1)]
+    gws = [q.new_verify_workspace(B, gamma, VOCAB, device=dev) for _ in range(R)]
     gn = torch.empty(B, dtype=torch.int32, device=dev)
     go = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
-    t = _graph_time(lambda: q.qspec_verify_greedy(gt, gd, gn, go, gws), reps=10, iters=3)
-    q.qspec_check_status(gws)
-    b = verify_bytes(B, gamma, VOCAB, False)
+    t = _rotating_time([(lambda i=i: q.qspec_verify_greedy(gts[i], gd, gn, go, gws[i])) for i in range(R)])
+    for w in gws:
+        q.qspec_check_status(w)
     print(json.dumps({"sweep": "batched_greedy_verify", "B": B, "gamma": gamma, "V": VOCAB,
                       "us": round(t * 1e6, 2), "GB_s": round(b / t / 1e9, 1), "hbm_frac": round(b / t / 1e9 / hbm, 3),
-                      "l2_resident": b < 100e6, "accept_len": gn.cpu().tolist()}), flush=True)
+                      "logits_copies": R, "rotation_bytes": R * b, "l2_bytes": l2_bytes(),
+                      "accept_len": gn.cpu().tolist()}), flush=True)
 
 
 def sweep_sampling(quick=False):
@@ -789,40 +912,50 @@ def sweep_sampling(quick=False):
             for V in vocabs:
                 # greedy verify on the same shapes (it does not depend on the draft noise)
                 ginp = syn.verify_inputs(B, gamma, V, 0.5, workload_id=4, sampling=False)
+                # every cell rotates through logits copies of at least 3x L2 (HBM, not L2, figures)
+                bg = verify_bytes(B, gamma, V, False)
+                R = copies_for(bg)
                 gt = bf(ginp["tgt"])
+                gts = [gt] + [gt.clone() for _ in range(R - 1)]
                 gd = torch.from_numpy(ginp["d"]).to(dev)
-                gws = q.new_verify_workspace(B, gamma, V, device=dev)
+                gws = [q.new_verify_workspace(B, gamma, V, device=dev) for _ in range(R)]
                 gn = torch.empty(B, dtype=torch.int32, device=dev)
                 go = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
-                tg = _graph_time(lambda: q.qspec_verify_greedy(gt, gd, gn, go, gws), reps=10, iters=3)
-                q.qspec_check_status(gws)
-                bg = verify_bytes(B, gamma, V, False)
+                tg = _rotating_time([(lambda i=i: q.qspec_verify_greedy(gts[i], gd, gn, go, gws[i]))
+                                     for i in range(R)], iters=3)
+                for w in gws:
+                    q.qspec_check_status(w)
                 print(json.dumps({"sweep": "greedy_verify", "gamma": gamma, "B": B, "V": V,
                                   "us": round(tg * 1e6, 2), "GB_s": round(bg / tg / 1e9, 1),
-                                  "hbm_frac": round(bg / tg / 1e9 / hbm, 3),
-                                  "l2_resident": bg < 100e6,
+                                  "hbm_frac": round(bg / tg / 1e9 / hbm, 3), "logits_copies": R,
+                                  "rotation_bytes": R * bg,
                                   "positions_per_s": round(B * (gamma + 1) / tg, 1),
                                   "tokens_per_call": round(float(gn.float().mean().item()) + 1, 3)}), flush=True)
-                del gt, gd, gws
+                del gt, gts, gd, gws
                 for sigma in sigmas:
                     inp = syn.verify_inputs(B, gamma, V, sigma, workload_id=4, sampling=True)
+                    b = verify_bytes(B, gamma, V, True)
+                    R = copies_for(B * (2 * gamma + 1) * V * 2)
                     tgt, drf = bf(inp["tgt"]), bf(inp["drf"])
+                    sets = [(tgt, drf)] + [(tgt.clone(), drf.clone()) for _ in range(R - 1)]
                     d = torch.from_numpy(inp["d"]).to(dev)
                     ua, ur = torch.from_numpy(inp["u_acc"]).to(dev), torch.from_numpy(inp["u_res"]).to(dev)
-                    ws = q.new_verify_workspace(B, gamma, V, device=dev)
+                    wss = [q.new_verify_workspace(B, gamma, V, device=dev) for _ in range(R)]
                     n = torch.empty(B, dtype=torch.int32, device=dev)
                     o = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
                     a = torch.empty(B, gamma, dtype=torch.float32, device=dev)
-                    fn = lambda: q.qspec_verify_sample(tgt, drf, d, ua, ur, n, o, ws, accept_prob=a)
-                    t = _graph_time(fn, reps=10, iters=3)
-                    fn()
-                    q.qspec_check_status(ws)
+                    t = _rotating_time([(lambda i=i: q.qspec_verify_sample(sets[i][0], sets[i][1], d, ua, ur, n, o,
+                                                                           wss[i], accept_prob=a))
+                                        for i in range(R)], iters=3)
+                    for w in wss:
+                        q.qspec_check_status(w)
                     alpha = float(a.mean().item())
                     et = (gamma + 1.0) if alpha >= 1.0 else (1 - alpha ** (gamma + 1)) / (1 - alpha)
-                    b = verify_bytes(B, gamma, V, True)
+                    del sets, wss
                     print(json.dumps({"sweep": "sampling_verify", "gamma": gamma, "B": B, "V": V, "sigma": sigma,
                                       "us": round(t * 1e6, 2), "GB_s": round(b / t / 1e9, 1),
-                                      "hbm_frac": round(b / t / 1e9 / hbm, 3), "l2_resident": b < 100e6,
+                                      "hbm_frac": round(b / t / 1e9 / hbm, 3), "logits_copies": R,
+                                      "rotation_bytes": R * b,
                                       "positions_per_s": round(B * (gamma + 1) / t, 1),
                                       "tokens_per_call": round(float(n.float().mean().item()) + 1, 3),
                                       "mean_accept_prob": round(alpha, 4), "E_T_at_mean_alpha": round(et, 3)}),
@@ -887,6 +1020,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-all-cores", action="store_true", help="skip the all-cores oracle timing")
     ap.add_argument("--eager", action="store_true",
                     help="issue the step's launches directly instead of replaying CUDA graphs (for ncu)")
     args = ap.parse_args()
@@ -947,6 +1081,13 @@ def main():
             "value": round(nbytes / dt / 1e9, 6), "unit": "GB/s", "cores": threads_used(), "kind": "oracle",
             "sample": f"one oracle pass over {frac:.5f} of every layer's output rows (3 W4A4 + 1 W4A16 passes) "
                       f"plus full greedy and sampling verify; {dt:.1f} s; GB/s of the same algorithmic bytes"}
+        if not args.no_all_cores:
+            procs = os.cpu_count() or 1
+            nb_all, dt_all = time_oracle_all_cores(frac, procs)
+            result["cpu_baseline"]["all_cores"] = {
+                "value": round(nb_all / dt_all / 1e9, 6), "unit": "GB/s", "cores": procs,
+                "sample": f"{procs} single-threaded oracle processes, each the same sample as above at once; "
+                          f"{dt_all:.1f} s wall"}
     if world > 1:
         import torch.distributed as tdist
         tdist.destroy_process_group()

@@ -38,8 +38,13 @@ struct Plan {
   int chunk_len;   // elements per chunk (multiple of 8)
 };
 
-Plan plan_rows(int64_t rows, int V) {
-  int64_t c = (kPlanCTAs + rows - 1) / rows;
+// Chunks per row.  The argmax passes (greedy, top-1, tree) take about kPlanCTAs CTAs in all (more,
+// smaller CTAs measured faster for them: greedy over [64 x 8, 152064] 31.7 us with 1536 CTAs, 37.7
+// us with 1024).  Sampling pass 1 (one_wave) takes no more chunks than keep every CTA resident at
+// once (about 8 per SM), so no partial second wave idles most of the GPU: its largest cell ([64 x 15,
+// 152064], 960 rows) 76.2 -> 72.0 us for both passes with one chunk per row instead of two.
+Plan plan_rows(int64_t rows, int V, bool one_wave = false) {
+  int64_t c = one_wave ? kPlanCTAs / rows : (kPlanCTAs + rows - 1) / rows;
   const int64_t max_c = (V + kMinChunk - 1) / kMinChunk;
   if (c > max_c) c = max_c;
   if (c < 1) c = 1;
@@ -62,7 +67,7 @@ struct Layout {
 Layout layout(int B, int gamma, int V) {
   Layout L;
   L.pg = plan_rows(int64_t(B) * (gamma + 1), V);
-  L.p1 = plan_rows(int64_t(B) * (2 * gamma + 1), V);
+  L.p1 = plan_rows(int64_t(B) * (2 * gamma + 1), V, true);
   L.pt = plan_rows(int64_t(B) * (2 * gamma), V);
   L.chunks2 = (V + kChunk2 - 1) / kChunk2;
   size_t off = 0;

@@ -22,6 +22,13 @@ struct WsGuard {
   unsigned int* err;        // device address of the linear error word (current context)
 };
 enum : unsigned int { kErrTimeout = 1u, kErrWorkspace = 2u };
+// The tickets of the tensor-core kernels (split tiles) follow the header.  They must read zero when a
+// kernel starts (each kernel resets the ones it used), so both kernels keep them in one region of
+// this many words -- enough for 128-row tiles of 16 tokens, the finest split either kernel uses --
+// and place their other regions after it.
+inline long long tc_ticket_count(int M, int N) {
+  return (static_cast<long long>(N) + 127) / 128 * ((static_cast<long long>(M) + 15) / 16);
+}
 unsigned long long ws_tag(int M, int N, int K);
 // Device address of the linear error word in the current CUDA context (looked up once per context).
 unsigned int* linear_error_word();
@@ -34,7 +41,18 @@ __device__ __forceinline__ bool ws_claim(const WsGuard& g) {
   return false;
 }
 
-// Tensor-core (tcgen05) kernels: the shapes for which linear_tc_supported() is true.
+// Tensor-core W4A16 kernel that dequantises the weights on chip (linear_dq.cu), for kDqMinTokens
+// tokens or more (fewer run on the exact-code kernel, which measured faster there): the shapes for
+// which linear_dq_supported() is true.
+constexpr int kDqMinTokens = 65;
+bool linear_dq_supported(int M, int N, int K);
+size_t linear_dq_workspace_size(int M, int N, int K);
+qspec_status linear_dq(const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K, uint16_t* y,
+                       void* ws, size_t ws_bytes, const WsGuard& guard, cudaStream_t stream);
+
+// Tensor-core (tcgen05) kernels: the shapes for which linear_tc_supported() is true (W4A16 from
+// kDqMinTokens tokens on runs on linear_dq, everything else on the exact-code kernel of
+// linear_tc.cu).
 bool linear_tc_supported(int abits, int M, int N, int K);
 size_t linear_tc_workspace_size(int abits, int M, int N, int K);
 qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M,

@@ -144,15 +144,14 @@ struct TcArgs {
   WsGuard guard;          // the workspace's layout claim
 };
 
-constexpr uint32_t kSuspendNs = 2000;  // hardware suspend per try_wait while a phase is incomplete
 
 // Bounded wait: false if it gave up (then the whole CTA runs in abort mode).
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (*abort_flag) return false;
-    if (mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (clock64() - t0 > kWaitLimit) {
       *abort_flag = 1;
       atomicOr(&g_linear_error, 1u);
@@ -164,7 +163,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 // Wait that ignores the abort flag (used to let in-flight copies land before exit); bounded.
 __device__ __forceinline__ void wait_bar_final(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
-  while (!mbar_try_wait_hint(bar, parity, kSuspendNs)) {
+  while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > kWaitLimit) {
       atomicOr(&g_linear_error, 1u);
       return;
@@ -822,11 +821,10 @@ int pick_ctas(int NM, long long U, int G, int sms) {
 }
 
 WsLayout ws_layout(int abits, int M, int N, int K, int P) {
-  const int NM = pick_nm(abits, M);
-  const long long T = (static_cast<long long>(N) + 127) / 128 * ((M + NM - 1) / NM);
+  const int NM = pick_nm(abits, M);  // tiles of NM >= 16 tokens: at most tc_ticket_count tickets
   WsLayout L;
   size_t off = kWsHeader;  // the layout header comes first
-  L.ticket = off;  off = al256(off + sizeof(unsigned int) * T);
+  L.ticket = off;  off = al256(off + sizeof(unsigned int) * tc_ticket_count(M, N));
   L.partial = off; off = al256(off + sizeof(float) * size_t(P) * 2 * 128 * NM);
   // quantised codes and scales: used by the codes mode here, and by the GEMV when it quantises
   // the tokens in a separate kernel
@@ -860,6 +858,7 @@ qspec_status launch_tc(const CUtensorMap& tmW, const CUtensorMap& tmX, const TcA
 }  // namespace
 
 bool linear_tc_supported(int abits, int M, int N, int K) {
+  if (abits == 16 && linear_dq_supported(M, N, K)) return true;
   if (M < 1 || M > QSPEC_MAX_M || N < 8 || K < kGroup) return false;
   const int NM = pick_nm(abits, M);
   const long long U = (static_cast<long long>(N) + 127) / 128 * ((M + NM - 1) / NM) * (K / kGroup);
@@ -867,12 +866,14 @@ bool linear_tc_supported(int abits, int M, int N, int K) {
 }
 
 size_t linear_tc_workspace_size(int abits, int M, int N, int K) {
+  if (abits == 16 && linear_dq_supported(M, N, K)) return linear_dq_workspace_size(M, N, K);
   return ws_layout(abits, M, N, K, num_sms()).total;
 }
 
 qspec_status linear_tc(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
                        uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, size_t ws_bytes,
                        const WsGuard& guard, cudaStream_t stream) {
+  if (abits == 16 && linear_dq_supported(M, N, K)) return linear_dq(x, Wp, S, M, N, K, y, ws, ws_bytes, guard, stream);
   const int NM = pick_nm(abits, M);
   const int T_m = (M + NM - 1) / NM;
   const long long T = (static_cast<long long>(N) + 127) / 128 * T_m;

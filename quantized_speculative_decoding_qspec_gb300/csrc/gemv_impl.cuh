@@ -711,15 +711,35 @@ qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int
              : QSPEC_ERR_CUDA;
 }
 
+// The cheapest warp split over the depths D, D / 2, .., 1 (cost as in pick_ks); -1 if none fits.
+inline long long cost_upto(long long tiles, int Gc, int KC, int D) {
+  long long best = -1;
+  for (int d = D; d >= 1; d /= 2) {
+    int ks = 1, grid = 1;
+    long long c = -1;
+    if (pick_ks(tiles, Gc, KC, d, &ks, &grid, &c) && (best < 0 || c < best)) best = c;
+  }
+  return best;
+}
+
+// Launches with D groups in flight unless a shallower pipeline fits no split at D or allows a split
+// at least a quarter cheaper: a slice of Gc groups must hold a multiple of D, so e.g. the Llama-3-8B
+// down layer at sixteen tokens (4 chunks of 28 groups) only runs unsplit at D = 4 -- 16 warps to a
+// CTA, 64 CTAs -- but two ways split at D = 2, on twice the CTAs.
 template <int QB, bool ACC, int MT, int D>
 qspec_status launch_depth(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
                           Outs o, int KC, cudaStream_t stream) {
   int ks = 1, grid = 1;
+  long long c = -1;
   const long long tiles = (static_cast<long long>(N) + 15) / 16;
-  if (!pick_ks(tiles, K / kGroup / KC, KC, D, &ks, &grid)) {
-    if constexpr (D > 1) return launch_depth<QB, ACC, MT, D / 2>(x, Wp, S, M, N, K, y, o, KC, stream);
-    return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  const int Gc = K / kGroup / KC;
+  const bool fits = pick_ks(tiles, Gc, KC, D, &ks, &grid, &c);
+  if constexpr (D > 1) {
+    const long long below = cost_upto(tiles, Gc, KC, D / 2);
+    if (!fits || (below >= 0 && 4 * below <= 3 * c))
+      return launch_depth<QB, ACC, MT, D / 2>(x, Wp, S, M, N, K, y, o, KC, stream);
   }
+  if (!fits) return QSPEC_ERR_UNSUPPORTED_SHAPE;
   return launch_d<QB, ACC, MT, D>(x, Wp, S, M, N, K, y, o, ks, KC, grid * KC, stream);
 }
 

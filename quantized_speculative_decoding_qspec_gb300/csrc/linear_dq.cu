@@ -83,7 +83,9 @@ struct Plan {
 // largest of: its weight bytes at the per-SM share of HBM bandwidth, its dequantisation (about 170
 // cycles a tile plus a hand-over) and its MMAs (about 0.6 NM cycles each on the tensor core).  With
 // one accumulator set in TMEM every item's drain stalls the MMAs; an item cut between CTAs costs its
-// last contributor a read of every contributor's partial tile.
+// last contributor a read of every contributor's partial tile.  (The constants were set by timing
+// the Llama-2-70B layers at 128 and 256 tokens; raising the partial-tile cost moved those to J = 1
+// and made them up to 35% slower.)
 double plan_cost(int NM, int J, int KB, int P, uint32_t dp, uint32_t sk_units) {
   const double hbm = J * (dq::kWTile / dq::kQuad) / 21.0;
   const double conv = J * 170.0 + 150.0;

@@ -61,7 +61,16 @@ struct Layout {
   Plan pg;
   Plan pt;            // top-1 statistics: B * 2 gamma rows
   int chunks2;
-  size_t err, cnt1, cnt2, seq_n, rowstat, part1, part2, part3, total;
+  size_t err, cnt1, cnt2, seq_n, rowstat, part1, part2, part3, rec2, total;
+};
+
+// What sampling pass 1 hands to pass 2 for one sequence, in one 32-byte record: the first rejected
+// position n (gamma: all accepted) and the softmax statistics of target row n and draft row n.
+struct Rec2 {
+  int n;
+  float mt, inv_st;  // target row n: max and 1 / sum exp(l - max)
+  float md, inv_sd;  // draft row n (0, 0 for the bonus row)
+  float pad[3];
 };
 
 Layout layout(int B, int gamma, int V) {
@@ -81,6 +90,7 @@ Layout layout(int B, int gamma, int V) {
   L.part1 = off;    off = align256(off + (part_g > part_s ? part_g : part_s));
   L.part2 = off;    off = align256(off + sizeof(float) * size_t(B) * L.chunks2);
   L.part3 = off;    off = align256(off + sizeof(float4) * size_t(B) * (2 * gamma) * L.pt.chunks);
+  L.rec2 = off;     off = align256(off + sizeof(Rec2) * size_t(B));
   L.total = off;
   return L;
 }
@@ -94,6 +104,7 @@ struct WS {
   float2* part1;
   float* part2;
   float4* part3;
+  Rec2* rec2;
 };
 
 WS bind(void* base, const Layout& L) {
@@ -101,7 +112,8 @@ WS bind(void* base, const Layout& L) {
   return {reinterpret_cast<unsigned int*>(p + L.err), reinterpret_cast<unsigned int*>(p + L.cnt1),
           reinterpret_cast<unsigned int*>(p + L.cnt2), reinterpret_cast<int*>(p + L.seq_n),
           reinterpret_cast<float2*>(p + L.rowstat), reinterpret_cast<float2*>(p + L.part1),
-          reinterpret_cast<float*>(p + L.part2), reinterpret_cast<float4*>(p + L.part3)};
+          reinterpret_cast<float*>(p + L.part2), reinterpret_cast<float4*>(p + L.part3),
+          reinterpret_cast<Rec2*>(p + L.rec2)};
 }
 
 // ------------------------------------------------------------------ argmax (greedy)
@@ -244,9 +256,10 @@ __device__ __forceinline__ MS ms_merge(MS a, MS b) {
   return {m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
 }
 
-// 2^x from the SFU (ex2.approx: relative error below 2^-22).  Used for the streamed row sums only:
-// the terms that matter have x near 0, and the fp32 summation of ~10^5 terms already carries a
-// larger relative error; the probabilities reported per token use the accurate expf.
+// 2^x from the SFU (ex2.approx: relative error below 2^-22).  Used for the streamed row sums and the
+// residual terms of pass 2 (exp_diff): the terms that matter have x near 0, and the fp32 summation
+// of ~10^5 terms already carries a larger relative error; the probabilities reported per token use
+// the accurate expf.
 __device__ __forceinline__ float exp2_sfu(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -416,6 +429,13 @@ __global__ void __launch_bounds__(kThreads, 8) sample_pass1_kernel(
     for (int i = 0; i < G1; ++i)
       if (i != n) out_tok[int64_t(b) * G1 + i] = i < n ? d[int64_t(b) * gamma + i] : -1;
     ws.seq_n[b] = n;
+    // the record as two 16-byte stores: n, max and 1 / sum of target row n, max and 1 / sum of draft
+    // row n (zeros for the bonus row)
+    const float md = n < gamma ? s_stat[G1 + n].x : 0.0f;
+    const float inv_sd = n < gamma ? 1.0f / s_stat[G1 + n].y : 0.0f;
+    int4* rec = reinterpret_cast<int4*>(ws.rec2 + b);
+    rec[0] = make_int4(n, __float_as_int(s_stat[n].x), __float_as_int(1.0f / s_stat[n].y), __float_as_int(md));
+    rec[1] = make_int4(__float_as_int(inv_sd), 0, 0, 0);
     ws.cnt1[b] = 0;
   }
 }
@@ -429,10 +449,16 @@ struct RowPair {
   bool bonus;         // r = p (bonus token, or the p fallback when the residual sums to 0)
 };
 
+// exp(d) for d = l - m of two bf16-valued floats (exact in fp32): 2^(d log2 e) from the SFU.  The
+// error is relative 2^-22 from ex2.approx plus |d| log2(e) 2^-24 ln 2 from rounding the product --
+// largest for the smallest terms and never shared by a whole row, so a residual max(0, p - q) keeps
+// its relative accuracy where p and q nearly cancel.
+__device__ __forceinline__ float exp_diff(float d) { return exp2_sfu(d * kLog2e); }
+
 __device__ __forceinline__ float resid(const RowPair& rp, float lt, float ld) {
-  const float p = expf(lt - rp.mt) * rp.inv_st;
+  const float p = exp_diff(lt - rp.mt) * rp.inv_st;
   if (rp.bonus) return p;
-  return fmaxf(0.0f, p - expf(ld - rp.md) * rp.inv_sd);
+  return fmaxf(0.0f, p - exp_diff(ld - rp.md) * rp.inv_sd);
 }
 
 // r values of this thread's kSeg2 contiguous elements of chunk c (zeros beyond V).
@@ -538,34 +564,31 @@ __device__ int chunk_select(const RowPair& rp, int V, int c, float target) {
 // chunk; the last CTA of a sequence walks the chunk sums in index order and selects the token with
 // the inverse CDF.
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) sample_pass2_kernel(
+__global__ void __launch_bounds__(kThreads, 8) sample_pass2_kernel(
     const uint16_t* __restrict__ Lt, const uint16_t* __restrict__ Ld,
-    const float* __restrict__ u_res, int B, int gamma, int V, int chunks2, WS ws,
+    const float* __restrict__ u_res, int B, int gamma, int V, int chunks2, int ctas_per_seq, WS ws,
     int32_t* __restrict__ out_tok) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int groups = (chunks2 + kPass2Chunks - 1) / kPass2Chunks;
-  const int b = blockIdx.x / groups;
-  const int c0 = (blockIdx.x % groups) * kPass2Chunks;
+  const int b = blockIdx.x / ctas_per_seq;
+  const int g0 = blockIdx.x % ctas_per_seq;  // this CTA takes chunk groups g0, g0 + ctas_per_seq, ..
   const int G1 = gamma + 1;
-  const int n = __ldcg(ws.seq_n + b);
+  // pass 1's record for this sequence (one 32-byte read)
+  const int4 r0 = __ldcg(reinterpret_cast<const int4*>(ws.rec2 + b));
+  const int4 r1 = __ldcg(reinterpret_cast<const int4*>(ws.rec2 + b) + 1);
+  const int n = r0.x;
   RowPair rp;
   rp.bonus = n == gamma;
-  const int64_t rt = int64_t(b) * G1 + n;
-  const int64_t rq = int64_t(B) * G1 + int64_t(b) * gamma + n;
-  const float2 st = __ldcg(ws.rowstat + rt);
-  rp.t = Lt + rt * V;
-  rp.mt = st.x;
-  rp.inv_st = 1.0f / st.y;
+  rp.t = Lt + (int64_t(b) * G1 + n) * V;
+  rp.mt = __int_as_float(r0.y);
+  rp.inv_st = __int_as_float(r0.z);
   rp.q = rp.bonus ? nullptr : Ld + (int64_t(b) * gamma + n) * V;
-  if (!rp.bonus) {
-    const float2 sq = __ldcg(ws.rowstat + rq);
-    rp.md = sq.x;
-    rp.inv_sd = 1.0f / sq.y;
-  } else {
-    rp.md = 0.0f;
-    rp.inv_sd = 0.0f;
-  }
-  {
+  rp.md = __int_as_float(r0.w);
+  rp.inv_sd = __int_as_float(r1.x);
+  __shared__ float s_ps[kPass2Chunks][kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int g = g0; g < groups; g += ctas_per_seq) {
+    const int c0 = g * kPass2Chunks;
     float r[kPass2Chunks][kSeg2];
 #pragma unroll
     for (int k = 0; k < kPass2Chunks; ++k) {
@@ -576,8 +599,6 @@ __global__ void __launch_bounds__(kThreads) sample_pass2_kernel(
         for (int e = 0; e < kSeg2; ++e) r[k][e] = 0.0f;
       }
     }
-    __shared__ float s_ps[kPass2Chunks][kThreads / 32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int k = 0; k < kPass2Chunks; ++k) {
       float v = 0.0f;
@@ -595,13 +616,14 @@ __global__ void __launch_bounds__(kThreads) sample_pass2_kernel(
       ws.part2[int64_t(b) * chunks2 + c0 + threadIdx.x] = t;
       __threadfence();  // each writer publishes its chunk sum before the ticket below
     }
+    __syncthreads();  // s_ps is reused by the next group
   }
 
   __shared__ bool s_last;
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned int prev = atomicAdd(ws.cnt2 + b, 1u);
-    s_last = prev == static_cast<unsigned int>(groups - 1);
+    s_last = prev == static_cast<unsigned int>(ctas_per_seq - 1);
   }
   __syncthreads();
   if (!s_last) return;
@@ -968,6 +990,28 @@ extern "C" qspec_status qspec_verify_greedy(const uint16_t* tgt_logits, const in
                     int(gamma), int(V), L.pg, w, accept_len, out_tok, tgt_argmax);
 }
 
+namespace qspec {
+namespace {
+// CTAs of sampling pass 2 that are resident at once on this device (occupancy x SMs; looked up once
+// per device ordinal, the kernels being the same in every context).
+int pass2_resident_ctas() {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_pass2_kernel<true>, kThreads, 0) != cudaSuccess ||
+      per_sm <= 0)
+    return 0;
+  const int r = per_sm * num_sms();
+  if (dev < 64) cached[dev] = r;
+  return r;
+}
+}  // namespace
+}  // namespace qspec
+
 extern "C" qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const uint16_t* draft_logits,
                                             const int32_t* draft_tok, const float* u_accept,
                                             const float* u_resample, int32_t B, int32_t gamma,
@@ -996,8 +1040,14 @@ extern "C" qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const ui
 
   // Pass 2 with programmatic dependent launch: its CTAs are scheduled while pass 1 drains and
   // wait (griddepcontrol.wait) for pass 1 to complete before reading the workspace.
+  // One resident wave: as many CTAs per sequence as fit the GPU at once (each loops over its share of
+  // the chunk groups), so no second wave waits behind the first one's latency chain.
+  const int groups2 = (L.chunks2 + kPass2Chunks - 1) / kPass2Chunks;
+  const int resident = pass2_resident_ctas();
+  if (resident <= 0) return QSPEC_ERR_CUDA;
+  const int per_seq = std::max(1, std::min(groups2, resident / int(B)));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(int64_t(B) * ((L.chunks2 + kPass2Chunks - 1) / kPass2Chunks)));
+  cfg.gridDim = dim3(unsigned(int64_t(B) * per_seq));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -1009,10 +1059,10 @@ extern "C" qspec_status qspec_verify_sample(const uint16_t* tgt_logits, const ui
   cudaError_t e;
   if (vec)
     e = cudaLaunchKernelEx(&cfg, sample_pass2_kernel<true>, tgt_logits, draft_logits, u_resample, int(B),
-                           int(gamma), int(V), L.chunks2, w, out_tok);
+                           int(gamma), int(V), L.chunks2, per_seq, w, out_tok);
   else
     e = cudaLaunchKernelEx(&cfg, sample_pass2_kernel<false>, tgt_logits, draft_logits, u_resample, int(B),
-                           int(gamma), int(V), L.chunks2, w, out_tok);
+                           int(gamma), int(V), L.chunks2, per_seq, w, out_tok);
   return e == cudaSuccess ? QSPEC_OK : QSPEC_ERR_CUDA;
 }
 

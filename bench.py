@@ -37,9 +37,16 @@ LAYERS = [  # name, N (out), K (in)
     ("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096),
     ("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336), ("lm_head", VOCAB, 4096),
 ]
+# The linears of a decoder layer that read the same activations go out as one grouped launch
+# (qspec_linear_group): q, k and v read the normed hidden state, gate and up the post-attention one.
+GROUPS = [("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",)),
+          ("lm_head", ("lm_head",))]
+LEADER = {m: members[0] for _, members in GROUPS for m in members}
+SHAPE = {name: (N, K) for name, N, K in LAYERS}
 WORKLOAD = ("Llama-3-8B-shaped decode linears q,k,v,o,gate,up,down,lm_head ([N,K] packed INT4, group 128, "
-            "fp16 scales); one QSpec iteration for 1 sequence, gamma=3: 3 W4A4 draft passes at M=1 + 1 W4A16 "
-            "verify pass at M=4, then greedy and sampling verify over bf16 logits [1,4,128256]")
+            "fp16 scales; q,k,v and gate,up read one input each and go out as grouped launches); one QSpec "
+            "iteration for 1 sequence, gamma=3: 3 W4A4 draft passes at M=1 + 1 W4A16 verify pass at M=4, then "
+            "greedy and sampling verify over bf16 logits [1,4,128256]")
 
 
 def linear_bytes(M, N, K):
@@ -54,9 +61,15 @@ def verify_bytes(B, gamma, V, sampling):
     return B * (2 * gamma + 1) * V * 2 + B * 2 * V * 2
 
 
+def group_bytes(M, members):
+    """Algorithmic bytes of one grouped launch: every part's weights, scales and y; x once."""
+    K = SHAPE[members[0]][1]
+    return sum(linear_bytes(M, SHAPE[m][0], K) for m in members) - (len(members) - 1) * M * K * 2
+
+
 def step_bytes():
-    lin16 = sum(linear_bytes(GAMMA + 1, N, K) for _, N, K in LAYERS)
-    lin4 = sum(linear_bytes(1, N, K) for _, N, K in LAYERS)
+    lin16 = sum(group_bytes(GAMMA + 1, members) for _, members in GROUPS)
+    lin4 = sum(group_bytes(1, members) for _, members in GROUPS)
     ver = verify_bytes(1, GAMMA, VOCAB, False) + verify_bytes(1, GAMMA, VOCAB, True)
     return {"w4a4": GAMMA * lin4, "w4a16": lin16, "verify": ver, "total": GAMMA * lin4 + lin16 + ver}
 
@@ -122,11 +135,13 @@ def oracle_sample_step(data, frac):
         rows = max(1, int(round(frac * N)))
         Wp, S = data["packed"][name]
         Wp, S = Wp[:rows], S[:rows]
+        lead = LEADER[name]
+        shared_x = lead != name  # a group's input is counted once, with its first member
         for d in range(GAMMA):
-            oracle.linear_w4a4(data["x1"][name][d], Wp, S)
-            nbytes += linear_bytes(1, rows, K)
-        oracle.linear_w4a16(data["x4"][name], Wp, S)
-        nbytes += linear_bytes(GAMMA + 1, rows, K)
+            oracle.linear_w4a4(data["x1"][lead][d], Wp, S)
+            nbytes += linear_bytes(1, rows, K) - (K * 2 if shared_x else 0)
+        oracle.linear_w4a16(data["x4"][lead], Wp, S)
+        nbytes += linear_bytes(GAMMA + 1, rows, K) - ((GAMMA + 1) * K * 2 if shared_x else 0)
     v = data["verify"]
     oracle.verify_greedy(v["tgt"], v["d_greedy"])
     oracle.verify_sample(v["tgt"], v["drf"], v["d_sample"], v["u_acc"], v["u_res"])
@@ -145,8 +160,9 @@ def oracle_inputs(frac):
         g = syn.rng(1, syn.STREAM_WEIGHTS, li)
         w = g.standard_normal((rows, K), dtype=np.float32) * np.float32(0.02)  # same rows as the GPU's
         data["packed"][name] = oracle.pack_weights(syn.f32_to_bf16_bits(w))
-        data["x1"][name] = [syn.activations(1, K, 1, step=10 * li + d) for d in range(GAMMA)]
-        data["x4"][name] = syn.activations(GAMMA + 1, K, 1, step=10 * li + 9)
+        if LEADER[name] == name:
+            data["x1"][name] = [syn.activations(1, K, 1, step=10 * li + d) for d in range(GAMMA)]
+            data["x4"][name] = syn.activations(GAMMA + 1, K, 1, step=10 * li + 9)
     data["verify"] = verify_data()
     return data
 
@@ -339,18 +355,19 @@ def gpu_arm(args, rank, world):
         torch.cuda.synchronize()
         pack_times.append(e0.elapsed_time(e1) * 1e-3)
         pack_bytes += N * K * 2 + N * K // 2 + N * (K // 128) * 2
-        # a workspace per (layer, token count): the two modes' calls are planned per shape
-        packed[name] = (Wp, S, {1: q.new_linear_workspace(1, N, K, device=dev),
-                                GAMMA + 1: q.new_linear_workspace(GAMMA + 1, N, K, device=dev)})
+        packed[name] = (Wp, S)
         del W
     torch.cuda.empty_cache()
 
     # ---- per-step inputs (resident in HBM) and outputs
     # the step's activations are views of one device buffer, so that the end-to-end run moves them
     # with one host-to-device copy per step
-    xbuf = torch.empty(sum((2 * GAMMA + 1) * K for _, _, K in LAYERS), dtype=torch.bfloat16, device=dev)
+    xbuf = torch.empty(sum((2 * GAMMA + 1) * K for n, _, K in LAYERS if LEADER[n] == n), dtype=torch.bfloat16,
+                       device=dev)
     x1, x4, off = {}, {}, 0
     for li, (n, N, K) in enumerate(LAYERS):
+        if LEADER[n] != n:  # the group's later members read the first member's input
+            continue
         x1[n] = []
         for d in range(GAMMA):
             x1[n].append(xbuf[off:off + K].view(1, K))
@@ -359,8 +376,17 @@ def gpu_arm(args, rank, world):
         x4[n] = xbuf[off:off + (GAMMA + 1) * K].view(GAMMA + 1, K)
         x4[n].copy_(bf(syn.activations(GAMMA + 1, K, 1, step=10 * li + 9)))
         off += (GAMMA + 1) * K
+    for n, _, _ in LAYERS:
+        x1[n], x4[n] = x1[LEADER[n]], x4[LEADER[n]]
     y1 = {n: torch.empty(1, N, dtype=torch.bfloat16, device=dev) for n, N, K in LAYERS}
     y4 = {n: torch.empty(GAMMA + 1, N, dtype=torch.bfloat16, device=dev) for n, N, K in LAYERS}
+    # one grouped call per (group, draft position) and per group for the verify pass, built once
+    gws = {gn: {M: q.new_linear_group_workspace(M, [SHAPE[m][0] for m in members], SHAPE[members[0]][1], device=dev)
+                for M in (1, GAMMA + 1)} for gn, members in GROUPS}
+    calls4 = [{gn: q.LinearGroup(4, x1[members[0]][d], [(packed[m][0], packed[m][1], y1[m]) for m in members],
+                                 gws[gn][1]) for gn, members in GROUPS} for d in range(GAMMA)]
+    calls16 = {gn: q.LinearGroup(16, x4[members[0]], [(packed[m][0], packed[m][1], y4[m]) for m in members],
+                                 gws[gn][GAMMA + 1]) for gn, members in GROUPS}
     vd = verify_data()
     tgt, drf = bf(vd["tgt"]), bf(vd["drf"])
     dg = torch.from_numpy(vd["d_greedy"]).to(dev)
@@ -402,14 +428,12 @@ def gpu_arm(args, rank, world):
 
         def draft():
             for d in range(GAMMA):
-                for name, N, K in LAYERS:
-                    Wp, S, lws = packed[name]
-                    timed(("w4a4", name), lambda: q.qspec_linear_w4a4(x1[name][d], Wp, S, y1[name], lws[1]))
+                for gn, _ in GROUPS:
+                    timed(("w4a4", gn), calls4[d][gn].run)
 
         def verify_pass():
-            for name, N, K in LAYERS:
-                Wp, S, lws = packed[name]
-                timed(("w4a16", name), lambda: q.qspec_linear_w4a16(x4[name], Wp, S, y4[name], lws[GAMMA + 1]))
+            for gn, _ in GROUPS:
+                timed(("w4a16", gn), calls16[gn].run)
 
         family("w4a4", draft)
         family("w4a16", verify_pass)
@@ -419,7 +443,7 @@ def gpu_arm(args, rank, world):
         family("sample", lambda: timed(("sample", ""),
                                        lambda: q.qspec_verify_sample(tgt, drf, ds, ua, ur, n_s, o_s, ws_s)))
 
-    launches_per_step = GAMMA * len(LAYERS) + len(LAYERS) + 1 + 2
+    launches_per_step = GAMMA * len(GROUPS) + len(GROUPS) + 1 + 2
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -499,7 +523,7 @@ def gpu_arm(args, rank, world):
     fam_bytes = {"w4a4": sb["w4a4"], "w4a16": sb["w4a16"],
                  "greedy": verify_bytes(1, GAMMA, VOCAB, False), "sample": verify_bytes(1, GAMMA, VOCAB, True)}
     fam_time = {f: family_time(f) for f in fam_bytes}
-    fam_launches = {"w4a4": GAMMA * len(LAYERS), "w4a16": len(LAYERS), "greedy": 1, "sample": 2}
+    fam_launches = {"w4a4": GAMMA * len(GROUPS), "w4a16": len(GROUPS), "greedy": 1, "sample": 2}
     dominant = max(fam_time, key=fam_time.get)
     hbm_peak, peak_kind = peaks()
     achieved = fam_bytes[dominant] / fam_time[dominant] / 1e9
@@ -508,38 +532,46 @@ def gpu_arm(args, rank, world):
     layers = {}
     for (fam, name), v in sorted(per_kind.items()):
         if fam in ("w4a4", "w4a16") and name != "*":
-            N, K = [(n_, k_) for nm, n_, k_ in LAYERS if nm == name][0]
+            members = dict(GROUPS)[name]
             M = 1 if fam == "w4a4" else GAMMA + 1
             t = sum(v) / len(v)
+            flops = sum(2 * M * SHAPE[m][0] * SHAPE[m][1] for m in members)
             layers[f"{fam}:{name}"] = {"us": round(t * 1e6, 2),
-                                       "GB_s": round(linear_bytes(M, N, K) / t / 1e9, 1),
-                                       "TOPS": round(2 * M * N * K / t / 1e12, 3)}
+                                       "GB_s": round(group_bytes(M, members) / t / 1e9, 1),
+                                       "TOPS": round(flops / t / 1e12, 3)}
     ver_t = {f: fam_time[f] for f in ("greedy", "sample")}
 
-    # ---- one decoder layer: q, k, v, o, gate, up, down back to back in one CUDA graph per mode,
-    # rotating through weight copies of at least 3x L2 (113 MB of packed weights per layer)
-    dec_layers = [l for l in LAYERS if l[0] != "lm_head"]
-    dec_bytes = {4: sum(linear_bytes(1, N, K) for _, N, K in dec_layers),
-                 16: sum(linear_bytes(GAMMA + 1, N, K) for _, N, K in dec_layers)}
+    # ---- one decoder layer: its grouped launches (q+k+v, o, gate+up, down) back to back in one CUDA
+    # graph per mode, rotating through weight copies of at least 3x L2 (113 MB of packed weights per layer)
+    dec_groups = [(gn, members) for gn, members in GROUPS if gn != "lm_head"]
+    dec_names = [m for _, members in dec_groups for m in members]
+    dec_bytes = {4: sum(group_bytes(1, members) for _, members in dec_groups),
+                 16: sum(group_bytes(GAMMA + 1, members) for _, members in dec_groups)}
     R_dec = copies_for(dec_bytes[4])
-    dec_sets = [{n: packed[n][:2] for n, _, _ in dec_layers}]
-    dec_sets += [{n: (packed[n][0].clone(), packed[n][1].clone()) for n, _, _ in dec_layers} for _ in range(R_dec - 1)]
+    dec_sets = [{n: packed[n] for n in dec_names}]
+    dec_sets += [{n: (packed[n][0].clone(), packed[n][1].clone()) for n in dec_names} for _ in range(R_dec - 1)]
     decoder_layer = {}
     for abits, M in ((4, 1), (16, GAMMA + 1)):
-        f = q.qspec_linear_w4a4 if abits == 4 else q.qspec_linear_w4a16
-        xin = {n: (x1[n][0] if abits == 4 else x4[n]) for n, _, _ in dec_layers}
-        yout = {n: (y1[n] if abits == 4 else y4[n]) for n, _, _ in dec_layers}
-        wsd = [{n: q.new_linear_workspace(M, N, K, device=dev) for n, N, K in dec_layers} for _ in range(R_dec)]
+        xin = {n: (x1[n][0] if abits == 4 else x4[n]) for n in dec_names}
+        yout = {n: (y1[n] if abits == 4 else y4[n]) for n in dec_names}
+        calls = []
+        for i in range(R_dec):
+            gl = []
+            for gn, members in dec_groups:
+                K = SHAPE[members[0]][1]
+                ws = q.new_linear_group_workspace(M, [SHAPE[m][0] for m in members], K, device=dev)
+                gl.append(q.LinearGroup(abits, xin[members[0]], [(*dec_sets[i][m], yout[m]) for m in members], ws))
+            calls.append(gl)
 
-        def layer_call(i, f=f, xin=xin, yout=yout, wsd=wsd):
-            for n, _, _ in dec_layers:
-                f(xin[n], dec_sets[i][n][0], dec_sets[i][n][1], yout[n], wsd[i][n])
+        def layer_call(i, calls=calls):
+            for c in calls[i]:
+                c.run()
 
         t_dec = _rotating_time([(lambda i=i: layer_call(i)) for i in range(R_dec)])
         decoder_layer[f"w4a{abits}_M{M}"] = {"us": round(t_dec * 1e6, 2),
                                               "GB_s": round(dec_bytes[abits] / t_dec / 1e9, 1),
                                               "hbm_frac": round(dec_bytes[abits] / t_dec / 1e9 / peaks()[0], 4)}
-        del wsd
+        del calls
     q.qspec_check_status()
     del dec_sets
 
@@ -645,7 +677,8 @@ def gpu_arm(args, rank, world):
                              "region (separating the launches adds gaps: per-layer times are upper bounds)",
             "pack_GB_s": round(pack_bytes / sum(pack_times) / 1e9, 1),
             "decoder_layer": decoder_layer,
-            "decoder_layer_timing": ("q, k, v, o, gate, up, down back to back in one CUDA graph, rotating through "
+            "decoder_layer_timing": ("the grouped launches q+k+v, o, gate+up, down back to back in one CUDA graph, "
+                                     "rotating through "
                                      f"{R_dec} weight copies (at least 3x L2); W4A4 at M=1, W4A16 at M={GAMMA + 1}"),
         },
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -665,8 +698,9 @@ def gpu_arm(args, rank, world):
 
 
 def profile_case(spec, reps):
-    """Run one kernel of the step repeatedly (for profilers): LAYER:MODE:M, e.g. lm_head:a4:1,
-    or verify:greedy / verify:sample on the step's logits."""
+    """Run one kernel of the step repeatedly (for profilers): LAYER:MODE:M, e.g. lm_head:a4:1, a group
+    of the step as one grouped launch (qkv:a4:1, gate_up:a16:4), or verify:greedy / verify:sample on
+    the step's logits."""
     import numpy as np
     import torch
 
@@ -700,21 +734,35 @@ def profile_case(spec, reps):
               else (lambda: q.qspec_verify_sample(tgt, drf, d, ua, ur, n, o, ws)))
         nbytes = verify_bytes(Bc, gc, Vc, parts[1] != "greedy")
     else:
+        # a layer (one linear) or a group of the step (one grouped launch, e.g. qkv:a4:1)
         name, mode, M = parts[0], parts[1], int(parts[2])
-        li = [l[0] for l in LAYERS].index(name)
-        _, N, K = LAYERS[li]
-        W = bf(syn.weights(N, K, 1, layer=li))
-        Wp = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
-        S = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
-        q.qspec_pack_weights(W, Wp, S)
-        del W
-        x = bf(syn.activations(M, K, 1, step=10 * li))
-        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-        ws = q.new_linear_workspace(M, N, K, device=dev)
-        fn = {"a4": lambda: q.qspec_linear_w4a4(x, Wp, S, y, ws),
-              "a8": lambda: q.qspec_linear_w4a8(x, Wp, S, y, ws),
-              "a16": lambda: q.qspec_linear_w4a16(x, Wp, S, y, ws)}[mode]
-        nbytes = linear_bytes(M, N, K)
+        groups = dict(GROUPS)
+        grouped = name in groups and M <= 4  # the grouped launch serves up to 4 tokens
+        members = groups[name] if grouped else (name,)
+        K = SHAPE[members[0]][1]
+        lead = [l[0] for l in LAYERS].index(members[0])
+        x = bf(syn.activations(M, K, 1, step=10 * lead))
+        mats = []
+        for m in members:
+            li = [l[0] for l in LAYERS].index(m)
+            N = SHAPE[m][0]
+            W = bf(syn.weights(N, K, 1, layer=li))
+            Wp = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+            S = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+            q.qspec_pack_weights(W, Wp, S)
+            del W
+            mats.append((Wp, S, torch.empty(M, N, dtype=torch.bfloat16, device=dev)))
+        abits = {"a4": 4, "a8": 8, "a16": 16}[mode]
+        if grouped:
+            ws = q.new_linear_group_workspace(M, [SHAPE[m][0] for m in members], K, device=dev)
+            fn = q.LinearGroup(abits, x, mats, ws).run
+            nbytes = group_bytes(M, members)
+        else:
+            Wp, S, y = mats[0]
+            ws = q.new_linear_workspace(M, SHAPE[name][0], K, device=dev)
+            f = {4: q.qspec_linear_w4a4, 8: q.qspec_linear_w4a8, 16: q.qspec_linear_w4a16}[abits]
+            fn = lambda: f(x, Wp, S, y, ws)
+            nbytes = linear_bytes(M, SHAPE[name][0], K)
     for _ in range(reps):
         fn()
     torch.cuda.synchronize()

@@ -140,6 +140,42 @@ qspec_status qspec_linear_w4a8(const uint16_t* x, const uint8_t* Wp, const uint1
                                int32_t* acc_out, void* ws, size_t ws_bytes, qspec_stream_t stream);
 
 /*
+ * qspec_linear_group -- several linears that read the same activations, in one launch and one mode
+ * (steps a2, a3 + a4, or the W4A8 configuration of f3): e.g. the q, k and v projections of a
+ * decoder layer, or its gate and up projections.
+ *
+ * QSpec article, section "QSpec の W4A4 モードと W4A16 モード": both modes read the same packed weights.
+ * Part i computes exactly what qspec_linear_w4a16 / _w4a4 / _w4a8 compute for (x, Wp_i, S_i):
+ *     y_i = x . dequant(Wp_i, S_i)^T          (abits = 16)
+ *     y_i = s_a . sum_g s . acc               (abits = 4 or 8, x quantised once per token)
+ * with the same definitions and tolerances (the fp32 summation order may differ in the last bits).
+ * The parts' rows stream as one run of 16-row tiles, so the launch, the activation staging and the
+ * per-token quantisation are paid once for the group.
+ *
+ *   abits     16 (W4A16), 4 (W4A4) or 8 (W4A8)
+ *   x         [M, K] bf16, 1 <= M <= QSPEC_GROUP_MAX_M, K % 128 == 0
+ *   parts     HOST array of n_parts descriptors, 1 <= n_parts <= QSPEC_GROUP_MAX_PARTS; each:
+ *               Wp [N, K/2] uint8, S [N, K/128] fp16 (from qspec_pack_weights), y [M, N] bf16
+ *               (output), N % 8 == 0; read during the call
+ *   ws, ws_bytes  device workspace, >= qspec_linear_group_workspace_size(M, parts, n_parts, K),
+ *             zero-filled before its first use; its header records the layout as (M, R, K), R = 16
+ *             x the parts' 16-row tiles (QSPEC_ERR_WORKSPACE for a workspace laid out otherwise)
+ * Shapes the decode-size kernel does not serve return QSPEC_ERR_UNSUPPORTED_SHAPE (call the parts
+ * one by one then).
+ */
+#define QSPEC_GROUP_MAX_PARTS 4
+#define QSPEC_GROUP_MAX_M 4
+typedef struct {
+  const uint8_t* Wp;
+  const uint16_t* S;
+  uint16_t* y;
+  int64_t N;
+} qspec_linear_part;
+size_t qspec_linear_group_workspace_size(int64_t M, const qspec_linear_part* parts, int32_t n_parts, int64_t K);
+qspec_status qspec_linear_group(int32_t abits, const uint16_t* x, int64_t M, int64_t K, const qspec_linear_part* parts,
+                                int32_t n_parts, void* ws, size_t ws_bytes, qspec_stream_t stream);
+
+/*
  * qspec_linear_pass -- one launch for a pass of decode-size linears in one mode (steps a2, a3 + a4,
  * or the W4A8 configuration of f3), e.g. every linear of a decoder layer and the lm_head.
  *

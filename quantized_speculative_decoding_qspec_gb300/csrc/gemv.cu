@@ -25,10 +25,11 @@ size_t gemv_workspace_bytes(int M, int N, int K) {
   return chunk_ws_bytes(MT, N, G, plan_kc(MT, N, G));
 }
 
-qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
-                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, const WsGuard& guard,
-                  cudaStream_t stream) {
-  const __half* Sh = reinterpret_cast<const __half*>(S);
+namespace {
+// The GEMV over the parts of P (N = 16 x their tiles, the row count that the planners and the
+// workspace see; the workspace belongs to that (M, N, K)).
+qspec_status gemv_parts(int abits, const uint16_t* x, const Parts& P, int M, int N, int K, int8_t* xq_out,
+                        float* xs_out, int32_t* acc_out, void* ws, const WsGuard& guard, cudaStream_t stream) {
   const int MT = token_slots(M), G = K / kGroup;
   const int KC = plan_kc(MT, N, G);
   if (KC == 0) return QSPEC_ERR_UNSUPPORTED_SHAPE;
@@ -58,11 +59,50 @@ qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_
     qb = 1;
   }
   switch (qb) {
-    case 4: return launch_mode<4>(MT, x, Wp, Sh, M, N, K, y, o, KC, stream);
-    case 8: return launch_mode<8>(MT, x, Wp, Sh, M, N, K, y, o, KC, stream);
-    case 1: return launch_mode<1>(MT, x, Wp, Sh, M, N, K, y, o, KC, stream);
-    default: return launch_mode<0>(MT, x, Wp, Sh, M, N, K, y, o, KC, stream);
+    case 4: return launch_mode<4>(MT, x, P, M, N, K, o, KC, stream);
+    case 8: return launch_mode<8>(MT, x, P, M, N, K, o, KC, stream);
+    case 1: return launch_mode<1>(MT, x, P, M, N, K, o, KC, stream);
+    default: return launch_mode<0>(MT, x, P, M, N, K, o, KC, stream);
   }
+}
+}  // namespace
+
+qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_t* S, int M, int N, int K,
+                  uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, const WsGuard& guard,
+                  cudaStream_t stream) {
+  Parts P{};
+  P.n = 1;
+  P.tile_end[0] = (N + 15) / 16;
+  P.N[0] = N;
+  P.Wp[0] = Wp;
+  P.S[0] = reinterpret_cast<const __half*>(S);
+  P.y[0] = y;
+  return gemv_parts(abits, x, P, M, N, K, xq_out, xs_out, acc_out, ws, guard, stream);
+}
+
+static_assert(kMaxParts == QSPEC_GROUP_MAX_PARTS && kPartsMaxMT == QSPEC_GROUP_MAX_M, "group limits");
+
+int gemv_group_rows(const int64_t* N, int n) {
+  long long tiles = 0;
+  for (int i = 0; i < n; ++i) tiles += (N[i] + 15) / 16;
+  return static_cast<int>(tiles * 16);
+}
+
+qspec_status gemv_group(int abits, const uint16_t* x, int M, int K, const GroupPart* parts, int n, void* ws,
+                        const WsGuard& guard, cudaStream_t stream) {
+  if (n < 1 || n > kMaxParts || token_slots(M) > kPartsMaxMT) return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  Parts P{};
+  P.n = n;
+  int tiles = 0;
+  for (int i = 0; i < n; ++i) {
+    tiles += static_cast<int>((parts[i].N + 15) / 16);
+    P.tile_end[i] = tiles;
+    P.N[i] = static_cast<int>(parts[i].N);
+    P.Wp[i] = parts[i].Wp;
+    P.S[i] = reinterpret_cast<const __half*>(parts[i].S);
+    P.y[i] = parts[i].y;
+  }
+  return gemv_parts(abits, x, P, M, tiles * 16, K, nullptr, nullptr, nullptr, ws, guard, stream);
 }
 
 }  // namespace qspec

@@ -212,10 +212,40 @@ __device__ __forceinline__ void item_mma(float (&d)[NB][4], const uint4& wl, con
 // ahead across tile boundaries, so the stream never drains; the first fetches are issued before
 // the kernel waits for its predecessor (no library kernel that may run ahead of this one writes
 // packed weights or scales).
+// Up to kMaxParts weight matrices that read the same activations (one linear, or e.g. the q, k and v
+// projections of a decoder layer), streamed as one run of 16-row tiles: part i owns the tiles
+// [tile_end[i - 1], tile_end[i]) and its rows, scales and outputs are its own.
+constexpr int kMaxParts = 4;
+struct Parts {
+  int n;
+  int tile_end[kMaxParts];
+  int N[kMaxParts];
+  const uint8_t* Wp[kMaxParts];
+  const __half* S[kMaxParts];
+  uint16_t* y[kMaxParts];
+};
+
+// Token slots for which the kernel serves several parts (above, one part: the lookup's registers
+// would push the 16- and 32-slot kernels past their 128).
+constexpr int kPartsMaxMT = 4;
+
+// The part that tile belongs to (the last part for tiles past the end).
+template <int MT>
+__device__ __forceinline__ int part_of(const Parts& p, int tile) {
+  if constexpr (MT > kPartsMaxMT) {
+    return 0;
+  } else {
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxParts - 1; ++i) s += (i + 1 < p.n && tile >= p.tile_end[i]) ? 1 : 0;
+    return s;
+  }
+}
+
 template <int QB, bool ACC, int MT, int D, bool CHUNK>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ Wp, const __half* __restrict__ S,
-                int M, int N, int K, int KS, int KC_arg, uint16_t* __restrict__ y, int8_t* __restrict__ xq_out,
+    gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ Parts parts, int M, int K, int KS,
+                int KC_arg, int8_t* __restrict__ xq_out,
                 float* __restrict__ xs_out, int32_t* __restrict__ acc_out, const float* __restrict__ s_a_in,
                 float* __restrict__ part, unsigned int* __restrict__ tick, const WsGuard guard) {
   constexpr bool A4 = QB != 0;                       // activations quantised (W4A4 or W4A8)
@@ -240,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
-  const int tiles = (N + 15) / 16;
+  const int tiles = parts.tile_end[parts.n - 1];
   const int per_cta = kWarps / KS;  // row tiles a CTA works on at once
   const int wtile = warp / KS, ks = warp - wtile * KS;
   const int gs = Gc / KS, g_beg = ks * gs;  // this warp's groups within the chunk
@@ -250,16 +280,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t row_bytes = static_cast<size_t>(K) / 2;
 
   // fetch cursor: the tile, its row pointers (at the slice's first group) and the group index
-  const uint8_t* f_wlo = Wp;
-  const uint8_t* f_whi = Wp;
-  const __half* f_slo = S;
-  const __half* f_shi = S;
+  const uint8_t* f_wlo = parts.Wp[0];
+  const uint8_t* f_whi = parts.Wp[0];
+  const __half* f_slo = parts.S[0];
+  const __half* f_shi = parts.S[0];
   bool f_vlo = false, f_vhi = false;
   int f_tile = tile0, f_i = 0;
   auto point = [&]() {
-    const int n_lo = f_tile * 16 + g, n_hi = n_lo + 8;
-    f_vlo = f_tile < tiles && n_lo < N;
-    f_vhi = f_tile < tiles && n_hi < N;
+    const int ps = part_of<MT>(parts, f_tile);
+    const int n_lo = (f_tile - (ps ? parts.tile_end[ps - 1] : 0)) * 16 + g, n_hi = n_lo + 8;
+    const int Np = parts.N[ps];
+    const uint8_t* Wp = parts.Wp[ps];
+    const __half* S = parts.S[ps];
+    f_vlo = f_tile < tiles && n_lo < Np;
+    f_vhi = f_tile < tiles && n_hi < Np;
     f_wlo = Wp + static_cast<size_t>(f_vlo ? n_lo : 0) * row_bytes + (gb + g_beg) * 64 + t * 16;
     f_whi = Wp + static_cast<size_t>(f_vhi ? n_hi : 0) * row_bytes + (gb + g_beg) * 64 + t * 16;
     f_slo = S + static_cast<size_t>(f_vlo ? n_lo : 0) * G + gb + g_beg;
@@ -507,7 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[nb][3] = fmaf(sh[k], d[nb][3], acc[nb][3]);
         }
         if constexpr (A4 && ACC) {
-          if (tile < tiles) {  // exact integer group sums
+          if (tile < tiles) {  // exact integer group sums (one part only)
+            const int N = parts.N[0];
             const int n_lo = tile * 16 + g, n_hi = n_lo + 8, gi = gb + g_beg + i0 + k;
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
@@ -580,7 +615,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (store) {
-      const int n_lo = tile * 16 + g, n_hi = n_lo + 8;
+      const int ps = part_of<MT>(parts, tile);
+      const int N = parts.N[ps];
+      uint16_t* y = parts.y[ps];
+      const int n_lo = (tile - (ps ? parts.tile_end[ps - 1] : 0)) * 16 + g, n_hi = n_lo + 8;
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
         const int m0 = nb * 8 + 2 * t, m1 = m0 + 1;
@@ -689,7 +727,7 @@ struct Outs {
 };
 
 template <int QB, bool ACC, int MT, int D>
-qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+qspec_status launch_d(const uint16_t* x, const Parts& P, int M, int N, int K,
                       Outs o, int best_ks, int KC, int best_grid, cudaStream_t stream) {
   const size_t smem = smem_bytes(MT, K / kGroup / KC);
   auto kern = KC > 1 ? gemv_kernel<QB, ACC, MT, D, true> : gemv_kernel<QB, ACC, MT, D, false>;
@@ -705,7 +743,7 @@ qspec_status launch_d(const uint16_t* x, const uint8_t* Wp, const __half* S, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, x, Wp, S, M, N, K, best_ks, KC, y, o.xq, o.xs, o.acc, o.s_in, o.part,
+  return cudaLaunchKernelEx(&cfg, kern, x, P, M, K, best_ks, KC, o.xq, o.xs, o.acc, o.s_in, o.part,
                             o.tick, o.guard) == cudaSuccess
              ? QSPEC_OK
              : QSPEC_ERR_CUDA;
@@ -727,7 +765,7 @@ inline long long cost_upto(long long tiles, int Gc, int KC, int D) {
 // down layer at sixteen tokens (4 chunks of 28 groups) only runs unsplit at D = 4 -- 16 warps to a
 // CTA, 64 CTAs -- but two ways split at D = 2, on twice the CTAs.
 template <int QB, bool ACC, int MT, int D>
-qspec_status launch_depth(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+qspec_status launch_depth(const uint16_t* x, const Parts& P, int M, int N, int K,
                           Outs o, int KC, cudaStream_t stream) {
   int ks = 1, grid = 1;
   long long c = -1;
@@ -737,67 +775,63 @@ qspec_status launch_depth(const uint16_t* x, const uint8_t* Wp, const __half* S,
   if constexpr (D > 1) {
     const long long below = cost_upto(tiles, Gc, KC, D / 2);
     if (!fits || (below >= 0 && 4 * below <= 3 * c))
-      return launch_depth<QB, ACC, MT, D / 2>(x, Wp, S, M, N, K, y, o, KC, stream);
+      return launch_depth<QB, ACC, MT, D / 2>(x, P, M, N, K, o, KC, stream);
   }
   if (!fits) return QSPEC_ERR_UNSUPPORTED_SHAPE;
-  return launch_d<QB, ACC, MT, D>(x, Wp, S, M, N, K, y, o, ks, KC, grid * KC, stream);
+  return launch_d<QB, ACC, MT, D>(x, P, M, N, K, o, ks, KC, grid * KC, stream);
 }
 
 // Groups in flight per warp (the weights wait in 8 registers per group and lane): 4 up to eight
 // tokens, 2 for sixteen (two column blocks of accumulators), 1 for 32; the checking path (int32
 // group sums out) at most 2.
 template <int QB, int MT>
-qspec_status launch(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+qspec_status launch(const uint16_t* x, const Parts& P, int M, int N, int K,
                     Outs o, int KC, cudaStream_t stream) {
   if constexpr (QB != 0) {
-    if (o.acc) return launch_depth<QB, true, MT, (MT < 32 ? 2 : 1)>(x, Wp, S, M, N, K, y, o, KC, stream);
+    if (o.acc) return launch_depth<QB, true, MT, (MT < 32 ? 2 : 1)>(x, P, M, N, K, o, KC, stream);
   }
-  return launch_depth<QB, false, MT, depth_of(MT)>(x, Wp, S, M, N, K, y, o, KC, stream);
+  return launch_depth<QB, false, MT, depth_of(MT)>(x, P, M, N, K, o, KC, stream);
 }
 
 // The modes that quantise inside the kernel (QB = 4, 8) serve at most three tokens (from four on
 // the separate quantiser runs and QB = 1 stages its codes), so they are instantiated for up to 4
 // token slots only; 32 slots serve W4A16 and codes.
 template <int QB, int MT>
-qspec_status launch_slots(const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K, uint16_t* y,
+qspec_status launch_slots(const uint16_t* x, const Parts& P, int M, int N, int K,
                           Outs o, int KC, cudaStream_t stream) {
   if constexpr ((QB == 4 || QB == 8) && MT > 4) {
     return QSPEC_ERR_UNSUPPORTED_SHAPE;
   } else {
-    return launch<QB, MT>(x, Wp, S, M, N, K, y, o, KC, stream);
+    return launch<QB, MT>(x, P, M, N, K, o, KC, stream);
   }
 }
 
 // The launcher of one activation mode (0: W4A16, 4: W4A4, 8: W4A8, 1: staged codes) for MT token
 // slots; each mode is instantiated in a translation unit of its own (they compile in parallel).
 template <int QB>
-qspec_status launch_mode(int MT, const uint16_t* x, const uint8_t* Wp, const __half* S, int M, int N, int K,
-                         uint16_t* y, Outs o, int KC, cudaStream_t stream);
+qspec_status launch_mode(int MT, const uint16_t* x, const Parts& P, int M, int N, int K, Outs o, int KC,
+                         cudaStream_t stream);
 
 template <>
-qspec_status launch_mode<0>(int, const uint16_t*, const uint8_t*, const __half*, int, int, int, uint16_t*, Outs, int,
-                            cudaStream_t);
+qspec_status launch_mode<0>(int, const uint16_t*, const Parts&, int, int, int, Outs, int, cudaStream_t);
 template <>
-qspec_status launch_mode<1>(int, const uint16_t*, const uint8_t*, const __half*, int, int, int, uint16_t*, Outs, int,
-                            cudaStream_t);
+qspec_status launch_mode<1>(int, const uint16_t*, const Parts&, int, int, int, Outs, int, cudaStream_t);
 template <>
-qspec_status launch_mode<4>(int, const uint16_t*, const uint8_t*, const __half*, int, int, int, uint16_t*, Outs, int,
-                            cudaStream_t);
+qspec_status launch_mode<4>(int, const uint16_t*, const Parts&, int, int, int, Outs, int, cudaStream_t);
 template <>
-qspec_status launch_mode<8>(int, const uint16_t*, const uint8_t*, const __half*, int, int, int, uint16_t*, Outs, int,
-                            cudaStream_t);
+qspec_status launch_mode<8>(int, const uint16_t*, const Parts&, int, int, int, Outs, int, cudaStream_t);
 
 #define QSPEC_GEMV_MODE_UNIT(QB_)                                                                      \
   template <>                                                                                          \
-  qspec_status launch_mode<QB_>(int MT, const uint16_t* x, const uint8_t* Wp, const __half* S, int M,  \
-                                int N, int K, uint16_t* y, Outs o, int KC, cudaStream_t stream) {      \
+  qspec_status launch_mode<QB_>(int MT, const uint16_t* x, const Parts& P, int M, int N, int K, Outs o, \
+                                int KC, cudaStream_t stream) {                                         \
     switch (MT) {                                                                                      \
-      case 1: return launch_slots<QB_, 1>(x, Wp, S, M, N, K, y, o, KC, stream);                        \
-      case 2: return launch_slots<QB_, 2>(x, Wp, S, M, N, K, y, o, KC, stream);                        \
-      case 4: return launch_slots<QB_, 4>(x, Wp, S, M, N, K, y, o, KC, stream);                        \
-      case 8: return launch_slots<QB_, 8>(x, Wp, S, M, N, K, y, o, KC, stream);                        \
-      case 16: return launch_slots<QB_, 16>(x, Wp, S, M, N, K, y, o, KC, stream);                      \
-      default: return launch_slots<QB_, 32>(x, Wp, S, M, N, K, y, o, KC, stream);                      \
+      case 1: return launch_slots<QB_, 1>(x, P, M, N, K, o, KC, stream);                        \
+      case 2: return launch_slots<QB_, 2>(x, P, M, N, K, o, KC, stream);                        \
+      case 4: return launch_slots<QB_, 4>(x, P, M, N, K, o, KC, stream);                        \
+      case 8: return launch_slots<QB_, 8>(x, P, M, N, K, o, KC, stream);                        \
+      case 16: return launch_slots<QB_, 16>(x, P, M, N, K, o, KC, stream);                      \
+      default: return launch_slots<QB_, 32>(x, P, M, N, K, o, KC, stream);                      \
     }                                                                                                  \
   }
 

@@ -111,3 +111,59 @@ extern "C" qspec_status qspec_linear_w4a8(const uint16_t* x, const uint8_t* Wp, 
                                           size_t ws_bytes, qspec_stream_t stream) {
   return linear_quantised(8, x, Wp, S, M, N, K, y, xq_out, xs_out, acc_out, ws, ws_bytes, stream);
 }
+
+namespace {
+// 16 x the parts' 16-row tiles, or -1 if a part is invalid; *st gets the status of the first
+// invalid part.
+int64_t group_rows(const qspec_linear_part* parts, int32_t n, int64_t K, qspec_status* st) {
+  using namespace qspec;
+  *st = QSPEC_OK;
+  int64_t tiles = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const qspec_linear_part& p = parts[i];
+    if (!p.Wp || !p.S || !p.y || p.N <= 0) { *st = QSPEC_ERR_INVALID_ARG; return -1; }
+    if (p.N % 8 != 0 || p.N > (int64_t(1) << 30) || p.N * K >= (int64_t(1) << 40)) {
+      *st = QSPEC_ERR_UNSUPPORTED_SHAPE;
+      return -1;
+    }
+    if (!aligned16(p.Wp) || !aligned16(p.S) || !aligned16(p.y)) { *st = QSPEC_ERR_MISALIGNED; return -1; }
+    tiles += (p.N + 15) / 16;
+  }
+  if (tiles * 16 > (int64_t(1) << 30)) { *st = QSPEC_ERR_UNSUPPORTED_SHAPE; return -1; }
+  return tiles * 16;
+}
+}  // namespace
+
+extern "C" size_t qspec_linear_group_workspace_size(int64_t M, const qspec_linear_part* parts, int32_t n_parts,
+                                                    int64_t K) {
+  if (!parts || n_parts < 1 || n_parts > QSPEC_GROUP_MAX_PARTS || M < 1 || M > QSPEC_GROUP_MAX_M || K <= 0 ||
+      K % qspec::kGroup != 0)
+    return 0;
+  qspec_status st;
+  const int64_t R = group_rows(parts, n_parts, K, &st);
+  if (R < 0) return 0;
+  return qspec_linear_workspace_size(M, R, K);
+}
+
+extern "C" qspec_status qspec_linear_group(int32_t abits, const uint16_t* x, int64_t M, int64_t K,
+                                           const qspec_linear_part* parts, int32_t n_parts, void* ws,
+                                           size_t ws_bytes, qspec_stream_t stream) {
+  using namespace qspec;
+  if (!x || !parts || n_parts < 1 || M <= 0 || K <= 0) return QSPEC_ERR_INVALID_ARG;
+  if (abits != 4 && abits != 8 && abits != 16) return QSPEC_ERR_INVALID_ARG;
+  if (n_parts > QSPEC_GROUP_MAX_PARTS || M > QSPEC_GROUP_MAX_M || K % kGroup != 0 || K > (int64_t(1) << 30))
+    return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  qspec_status st;
+  const int64_t R = group_rows(parts, n_parts, K, &st);
+  if (R < 0) return st;
+  if (!aligned16(x)) return QSPEC_ERR_MISALIGNED;
+  if (!gemv_supported(int(M), int(R), int(K))) return QSPEC_ERR_UNSUPPORTED_SHAPE;
+  if (!ws) return QSPEC_ERR_WORKSPACE;
+  if (!aligned16(ws)) return QSPEC_ERR_MISALIGNED;
+  if (ws_bytes < qspec_linear_workspace_size(M, R, K)) return QSPEC_ERR_WORKSPACE;
+  WsGuard guard;
+  if (!make_guard(int(M), int(R), int(K), ws, &guard)) return QSPEC_ERR_CUDA;
+  GroupPart gp[QSPEC_GROUP_MAX_PARTS];
+  for (int32_t i = 0; i < n_parts; ++i) gp[i] = GroupPart{parts[i].Wp, parts[i].S, parts[i].y, parts[i].N};
+  return gemv_group(abits, x, int(M), int(K), gp, n_parts, ws, guard, reinterpret_cast<cudaStream_t>(stream));
+}

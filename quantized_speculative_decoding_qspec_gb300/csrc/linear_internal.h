@@ -79,6 +79,19 @@ qspec_status gemv(int abits, const uint16_t* x, const uint8_t* Wp, const uint16_
                   uint16_t* y, int8_t* xq_out, float* xs_out, int32_t* acc_out, void* ws, const WsGuard& guard,
                   cudaStream_t stream);
 
+// One weight matrix of a group that reads the same activations (qspec_linear_group).
+struct GroupPart {
+  const uint8_t* Wp;
+  const uint16_t* S;
+  uint16_t* y;
+  int64_t N;
+};
+// The GEMV over a group of parts as one run of 16-row tiles; the planners and the workspace see
+// gemv_group_rows(N, n) rows (16 x the parts' tiles).
+int gemv_group_rows(const int64_t* N, int n);
+qspec_status gemv_group(int abits, const uint16_t* x, int M, int K, const GroupPart* parts, int n, void* ws,
+                        const WsGuard& guard, cudaStream_t stream);
+
 // A 2-D tensor map for TMA loads (dims {inner, outer} elements of type dt, row pitch row_bytes, box
 // {box_inner, box_outer}, 128-byte swizzle or none); out-of-range boxes read as zeros.  False if the
 // driver offers no encoder or rejects the arguments.

@@ -48,6 +48,8 @@ SIGNATURES = {
     "qspec_verify_tree_greedy": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "qspec_gather_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _P, _P]),
     "qspec_select_tokens": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
+    "qspec_linear_group_workspace_size": (ctypes.c_size_t, [_I64, _P, _I32, _I64]),
+    "qspec_linear_group": (ctypes.c_int, [_I32, _P, _I64, _I64, _P, _I32, _P, ctypes.c_size_t, _P]),
     "qspec_linear_pass_workspace_size": (ctypes.c_size_t, []),
     "qspec_linear_pass": (ctypes.c_int, [_I32, _I64, _P, _I32, _P, ctypes.c_size_t, _P]),
     "qspec_check_status": (ctypes.c_int, [_P, _P]),
@@ -182,6 +184,60 @@ def qspec_linear_w4a8(x, Wp, S, y, ws, xq_out=None, xs_out=None, acc_out=None, s
     _check("qspec_linear_w4a8",
            load().qspec_linear_w4a8(_ptr(x), _ptr(Wp), _ptr(S), M, N, K, _ptr(y), _ptr(xq_out), _ptr(xs_out),
                                     _ptr(acc_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+class LinearPart(ctypes.Structure):
+    """One part of qspec_linear_group (the C struct qspec_linear_part)."""
+    _fields_ = [("Wp", ctypes.c_void_p), ("S", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int64)]
+
+
+class LinearGroup:
+    """Several linears that read the same activations, in one launch (qspec_linear_group).
+
+    x: bf16 [M, K]; parts: list of (Wp, S, y) -- Wp uint8 [N, K/2], S fp16 [N, K/128], y bf16 [M, N].
+    abits: 16 (W4A16), 4 (W4A4) or 8 (W4A8).  The tensors must stay alive while the group is used.
+    """
+
+    def __init__(self, abits, x, parts, ws):
+        _dt(x, torch.bfloat16, "x"); _dt(ws, torch.uint8, "ws")
+        if not parts:
+            raise ValueError("a group needs at least one part")
+        self.M, self.K = x.shape
+        self.abits, self.x, self.ws = int(abits), x, ws
+        self.arr = (LinearPart * len(parts))()
+        self._keep = [x]
+        for i, (Wp, S, y) in enumerate(parts):
+            _dt(Wp, torch.uint8, "Wp"); _dt(S, torch.float16, "S"); _dt(y, torch.bfloat16, "y")
+            N = Wp.shape[0]
+            _need_linear(self.M, N, self.K, Wp, S, y)
+            self.arr[i] = LinearPart(_ptr(Wp), _ptr(S), _ptr(y), N)
+            self._keep += [Wp, S, y]
+
+    def run(self, stream=None):
+        _check("qspec_linear_group", load().qspec_linear_group(self.abits, _ptr(self.x), self.M, self.K, self.arr,
+                                                               len(self.arr), _ptr(self.ws), self.ws.numel(),
+                                                               _stream(stream)))
+
+
+def qspec_linear_group_workspace_size(M, Ns, K):
+    """Bytes of the workspace for a group of parts with N in Ns (0 if the arguments are invalid)."""
+    arr = (LinearPart * len(Ns))()
+    for i, N in enumerate(Ns):
+        arr[i] = LinearPart(16, 16, 16, int(N))  # (only N is read; non-null, aligned placeholders)
+    return int(load().qspec_linear_group_workspace_size(M, arr, len(Ns), K))
+
+
+def new_linear_group_workspace(M, Ns, K, device="cuda"):
+    """A zero-filled workspace for qspec_linear_group over parts with N in Ns."""
+    n = qspec_linear_group_workspace_size(M, Ns, K)
+    if n == 0:
+        raise ValueError("invalid group shape")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def qspec_linear_group(abits, x, parts, ws, stream=None):
+    """One launch over (Wp, S, y) parts that read the same x (see LinearGroup)."""
+    LinearGroup(abits, x, parts, ws).run(stream)
 
 
 class PassLayer(ctypes.Structure):

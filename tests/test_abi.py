@@ -200,3 +200,35 @@ def test_linear_pass_argument_checks(lib):
     assert f(16, 1, ok, 2, None, W, None) == 4                  # no workspace
     assert f(16, 1, ok, 2, FAKE + 8, W, None) == 3              # misaligned workspace
     assert f(16, 1, ok, 2, FAKE, W - 1, None) == 4              # workspace too small
+
+
+def test_linear_group_argument_checks(lib):
+    from quantized_speculative_decoding_qspec_gb300 import qspec as q
+
+    def parts(*specs):
+        arr = (q.LinearPart * len(specs))()
+        for i, (wp, N) in enumerate(specs):
+            arr[i] = q.LinearPart(wp, FAKE, FAKE, N)
+        return arr
+
+    f, wsz = lib.qspec_linear_group, lib.qspec_linear_group_workspace_size
+    qkv = parts((FAKE, 4096), (FAKE, 1024), (FAKE, 1024))
+    W = wsz(1, qkv, 3, 4096)
+    assert W > 0 and W == wsz(1, parts((FAKE, 6144)), 1, 4096)  # the parts' rows as one run of tiles
+    assert wsz(5, qkv, 3, 4096) == 0                             # M above QSPEC_GROUP_MAX_M
+    assert wsz(1, qkv, 5, 4096) == 0 and wsz(1, qkv, 0, 4096) == 0
+    assert wsz(1, parts((FAKE, 100)), 1, 4096) == 0              # N % 8
+    assert f(4, None, 1, 4096, qkv, 3, FAKE, W, None) == 1       # no activations
+    assert f(4, FAKE, 1, 4096, None, 3, FAKE, W, None) == 1      # no parts
+    assert f(4, FAKE, 1, 4096, qkv, 0, FAKE, W, None) == 1       # zero parts
+    assert f(5, FAKE, 1, 4096, qkv, 3, FAKE, W, None) == 1       # no such mode
+    assert f(16, FAKE, 5, 4096, qkv, 3, FAKE, W, None) == 2      # M above QSPEC_GROUP_MAX_M
+    assert f(16, FAKE, 1, 4096, parts(*[(FAKE, 64)] * 5), 5, FAKE, W, None) == 2   # too many parts
+    assert f(16, FAKE, 1, 200, qkv, 3, FAKE, W, None) == 2       # K % 128
+    assert f(16, FAKE, 1, 4096, parts((FAKE, 64), (FAKE, 60)), 2, FAKE, W, None) == 2  # N % 8
+    assert f(16, FAKE, 1, 4096, parts((None, 64)), 1, FAKE, W, None) == 1          # null weights
+    assert f(16, FAKE, 1, 4096, parts((FAKE + 8, 64)), 1, FAKE, W, None) == 3      # misaligned weights
+    assert f(16, FAKE + 8, 1, 4096, qkv, 3, FAKE, W, None) == 3  # misaligned x
+    assert f(16, FAKE, 1, 4096, qkv, 3, None, W, None) == 4      # no workspace
+    assert f(16, FAKE, 1, 4096, qkv, 3, FAKE + 8, W, None) == 3  # misaligned workspace
+    assert f(16, FAKE, 1, 4096, qkv, 3, FAKE, W - 1, None) == 4  # workspace too small

@@ -23,8 +23,13 @@ def test_verify_bytes_by_hand():
 def test_step_workload():
     sb = bench.step_bytes()
     assert [n for n, _, _ in bench.LAYERS] == ["q", "k", "v", "o", "gate", "up", "down", "lm_head"]
-    assert sb["w4a4"] == bench.GAMMA * sum(bench.linear_bytes(1, N, K) for _, N, K in bench.LAYERS)
-    assert sb["w4a16"] == sum(bench.linear_bytes(bench.GAMMA + 1, N, K) for _, N, K in bench.LAYERS)
+    # every member of a group appears once, and the members of a group share K
+    assert sorted(m for _, ms in bench.GROUPS for m in ms) == sorted(n for n, _, _ in bench.LAYERS)
+    assert all(len({bench.SHAPE[m][1] for m in ms}) == 1 for _, ms in bench.GROUPS)
+    # a grouped launch reads its input once: q, k, v and gate, up save 2 and 1 activation reads
+    shared = lambda M: (2 + 1) * M * 4096 * 2
+    assert sb["w4a4"] == bench.GAMMA * (sum(bench.linear_bytes(1, N, K) for _, N, K in bench.LAYERS) - shared(1))
+    assert sb["w4a16"] == sum(bench.linear_bytes(bench.GAMMA + 1, N, K) for _, N, K in bench.LAYERS) - shared(4)
     assert sb["total"] == sb["w4a4"] + sb["w4a16"] + sb["verify"]
     assert 1.5e9 < sb["total"] < 1.6e9          # larger than L2 (129 MB): no flush needed between steps
 

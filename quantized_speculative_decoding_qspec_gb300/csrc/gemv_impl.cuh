@@ -472,6 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 #pragma unroll
     for (int e = 0; e < kU; ++e) {
+      // a warp whose chunks of this batch all lie past the tokens is done (the same for all its
+      // lanes, so the offset sums' shuffles stay warp-uniform): one token of 4096 channels fills
+      // only the first of a thread's kU chunk slots
+      if (static_cast<int>(threadIdx.x & ~31u) + e * kThreads >= total) break;
       const int c = threadIdx.x + e * kThreads;
       uint4 st = make_uint4(0, 0, 0, 0);
       if (c < total) {

@@ -88,7 +88,7 @@ Layout layout(int B, int gamma, int V) {
   const size_t part_g = sizeof(float2) * size_t(B) * (gamma + 1) * L.pg.chunks;
   const size_t part_s = sizeof(float2) * size_t(B) * (2 * gamma + 1) * L.p1.chunks;
   L.part1 = off;    off = align256(off + (part_g > part_s ? part_g : part_s));
-  L.part2 = off;    off = align256(off + sizeof(float) * size_t(B) * L.chunks2);
+  L.part2 = off;    off = align256(off + sizeof(float) * size_t(B) * L.chunks2 * (kThreads / 32));
   L.part3 = off;    off = align256(off + sizeof(float4) * size_t(B) * (2 * gamma) * L.pt.chunks);
   L.rec2 = off;     off = align256(off + sizeof(Rec2) * size_t(B));
   L.total = off;
@@ -212,7 +212,14 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(const uint16_t* __rest
   __threadfence();
 
   __shared__ int s_t[QSPEC_MAX_GAMMA + 1];
+  __shared__ int s_x[QSPEC_MAX_GAMMA];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the draft tokens, read by gamma threads at once (not one dependent read after another)
+  if (threadIdx.x < gamma) {
+    const int x = d[int64_t(b) * gamma + threadIdx.x];
+    s_x[threadIdx.x] = x;
+    if (x < 0 || x >= V) atomicOr(ws.err, kErrBadToken);
+  }
   for (int i = warp; i < G1; i += kThreads / 32) {
     const int64_t r = int64_t(b) * G1 + i;
     float v = -INFINITY;
@@ -227,16 +234,10 @@ __global__ void __launch_bounds__(kThreads) greedy_kernel(const uint16_t* __rest
   __syncthreads();
   if (threadIdx.x == 0) {
     int n = 0;
-    bool bad = false;
-    for (int i = 0; i < gamma; ++i) {
-      const int x = d[int64_t(b) * gamma + i];
-      if (x < 0 || x >= V) bad = true;
-    }
-    while (n < gamma && d[int64_t(b) * gamma + n] == s_t[n]) ++n;
-    if (bad) atomicOr(ws.err, kErrBadToken);
+    while (n < gamma && s_x[n] == s_t[n]) ++n;
     accept_len[b] = n;
     for (int i = 0; i < G1; ++i) {
-      out_tok[int64_t(b) * G1 + i] = i < n ? d[int64_t(b) * gamma + i] : (i == n ? s_t[n] : -1);
+      out_tok[int64_t(b) * G1 + i] = i < n ? s_x[i] : (i == n ? s_t[n] : -1);
       if (tgt_argmax) tgt_argmax[int64_t(b) * G1 + i] = s_t[i];
     }
     ws.cnt1[b] = 0;
@@ -404,30 +405,36 @@ __global__ void __launch_bounds__(kThreads, 8) sample_pass1_kernel(
     }
   }
   __syncthreads();
+  // every draft position's test in a thread of its own (their reads of p and q at the draft token
+  // are independent); thread 0 then takes the first rejection
+  __shared__ int s_x[QSPEC_MAX_GAMMA], s_rej[QSPEC_MAX_GAMMA];
+  if (threadIdx.x < gamma) {
+    const int i = threadIdx.x;
+    const int x = d[int64_t(b) * gamma + i];
+    float p = 0.0f, q = 0.0f, acc = 0.0f;
+    if (x >= 0 && x < V) {
+      const float lt = bf16_lo(Lt[(int64_t(b) * G1 + i) * V + x]);
+      const float ld = bf16_lo(Ld[(int64_t(b) * gamma + i) * V + x]);
+      p = __fdiv_rn(expf(lt - s_stat[i].x), s_stat[i].y);
+      q = __fdiv_rn(expf(ld - s_stat[G1 + i].x), s_stat[G1 + i].y);
+      acc = q == 0.0f ? 1.0f : fminf(1.0f, __fdiv_rn(p, q));
+    } else {
+      atomicOr(ws.err, kErrBadToken);  // an invalid draft token is rejected
+    }
+    if (accept_prob) accept_prob[int64_t(b) * gamma + i] = acc;
+    if (p_tok) p_tok[int64_t(b) * gamma + i] = p;
+    if (q_tok) q_tok[int64_t(b) * gamma + i] = q;
+    s_x[i] = x;
+    s_rej[i] = !(u_acc[int64_t(b) * gamma + i] < acc);
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     int n = gamma;
-    bool bad = false;
-    for (int i = 0; i < gamma; ++i) {
-      const int x = d[int64_t(b) * gamma + i];
-      float p = 0.0f, q = 0.0f, acc = 0.0f;
-      if (x >= 0 && x < V) {
-        const float lt = bf16_lo(Lt[(int64_t(b) * G1 + i) * V + x]);
-        const float ld = bf16_lo(Ld[(int64_t(b) * gamma + i) * V + x]);
-        p = __fdiv_rn(expf(lt - s_stat[i].x), s_stat[i].y);
-        q = __fdiv_rn(expf(ld - s_stat[G1 + i].x), s_stat[G1 + i].y);
-        acc = q == 0.0f ? 1.0f : fminf(1.0f, __fdiv_rn(p, q));
-      } else {
-        bad = true;  // an invalid draft token is rejected
-      }
-      if (accept_prob) accept_prob[int64_t(b) * gamma + i] = acc;
-      if (p_tok) p_tok[int64_t(b) * gamma + i] = p;
-      if (q_tok) q_tok[int64_t(b) * gamma + i] = q;
-      if (n == gamma && !(u_acc[int64_t(b) * gamma + i] < acc)) n = i;
-    }
-    if (bad) atomicOr(ws.err, kErrBadToken);
+    for (int i = gamma - 1; i >= 0; --i)
+      if (s_rej[i]) n = i;
     accept_len[b] = n;
     for (int i = 0; i < G1; ++i)
-      if (i != n) out_tok[int64_t(b) * G1 + i] = i < n ? d[int64_t(b) * gamma + i] : -1;
+      if (i != n) out_tok[int64_t(b) * G1 + i] = i < n ? s_x[i] : -1;
     ws.seq_n[b] = n;
     // the record as two 16-byte stores: n, max and 1 / sum of target row n, max and 1 / sum of draft
     // row n (zeros for the bonus row)
@@ -461,10 +468,9 @@ __device__ __forceinline__ float resid(const RowPair& rp, float lt, float ld) {
   return fmaxf(0.0f, p - exp_diff(ld - rp.md) * rp.inv_sd);
 }
 
-// r values of this thread's kSeg2 contiguous elements of chunk c (zeros beyond V).
+// r values of the kSeg2 contiguous elements from i0 (zeros beyond V).
 template <bool kVec>
-__device__ __forceinline__ void seg_values(const RowPair& rp, int V, int c, float (&r)[kSeg2]) {
-  const int i0 = c * kChunk2 + threadIdx.x * kSeg2;
+__device__ __forceinline__ void seg_values_at(const RowPair& rp, int V, int i0, float (&r)[kSeg2]) {
   if (kVec && i0 + kSeg2 <= V) {
     const uint4 ut = ld_stream_v4(rp.t + i0);
     const uint4 uq = rp.bonus ? make_uint4(0, 0, 0, 0) : ld_stream_v4(rp.q + i0);
@@ -484,85 +490,57 @@ __device__ __forceinline__ void seg_values(const RowPair& rp, int V, int c, floa
   }
 }
 
-__device__ __forceinline__ float block_sum(float v) {
-  __shared__ float sw[kThreads / 32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Pass 2 keeps one residual sum per warp segment: the 32 x kSeg2 = 256 contiguous elements that the
+// lanes of one warp cover in a chunk (element c kChunk2 + (32 w + lane) kSeg2 + e).
+constexpr int kSegsPerChunk = kThreads / 32;
+
+// The sum of one warp segment's r values (lane sums, then a fixed xor-shuffle tree).
+__device__ __forceinline__ float warp_segment_sum(const float (&r)[kSeg2]) {
+  float v = 0.0f;
+#pragma unroll
+  for (int e = 0; e < kSeg2; ++e) v += r[e];
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-  if (lane == 0) sw[warp] = v;
-  __syncthreads();
-  float t = 0.0f;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) t += sw[w];
-  __syncthreads();
-  return t;
+  return v;
 }
 
-template <bool kVec>
-__device__ __forceinline__ float chunk_sum(const RowPair& rp, int V, int c) {
-  float r[kSeg2];
-  seg_values<kVec>(rp, V, c, r);
-  float s = 0.0f;
+// Inclusive prefix sums over the block of four consecutive values per thread (in thread order), in a
+// fixed order; excl gets the sum before the thread's first value; returns the block's total, which
+// equals the last thread's last prefix.
+__device__ __forceinline__ float block_incl_scan4(float (&v)[4], float& excl_out) {
+  __shared__ float s_w[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  v[1] += v[0];
+  v[2] += v[1];
+  v[3] += v[2];
+  const float t = v[3];
+  float incl = t;
 #pragma unroll
-  for (int e = 0; e < kSeg2; ++e) s += r[e];
-  return block_sum(s);
-}
-
-// Index of the first element of chunk c whose running sum exceeds `target` (sums start at 0 at the
-// chunk's first element); if rounding leaves no such element, the last element with r > 0.
-// Returns -1 when the chunk has no positive element.
-template <bool kVec>
-__device__ int chunk_select(const RowPair& rp, int V, int c, float target) {
-  __shared__ float s_pref[kThreads];
-  __shared__ int s_hit, s_last_pos;
-  float r[kSeg2];
-  seg_values<kVec>(rp, V, c, r);
-  float seg = 0.0f;
-  int last_pos = -1;
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  float wbase = 0.0f, total = 0.0f;
 #pragma unroll
-  for (int e = 0; e < kSeg2; ++e) {
-    seg += r[e];
-    if (r[e] > 0.0f) last_pos = e;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const float x = s_w[w];
+    if (w < warp) wbase += x;
+    total += x;
   }
-  if (threadIdx.x == 0) { s_hit = INT_MAX; s_last_pos = -1; }
-  // inclusive scan of the segment sums in thread order
-  s_pref[threadIdx.x] = seg;
-  __syncthreads();
-  for (int off = 1; off < kThreads; off <<= 1) {
-    const float add = threadIdx.x >= off ? s_pref[threadIdx.x - off] : 0.0f;
-    __syncthreads();
-    s_pref[threadIdx.x] += add;
-    __syncthreads();
-  }
-  const float incl = s_pref[threadIdx.x];
-  const float excl = threadIdx.x ? s_pref[threadIdx.x - 1] : 0.0f;
-  const int base = c * kChunk2 + threadIdx.x * kSeg2;
-  if (incl > target) {
-    float run = excl;
-    int j = -1;
+  const float excl = wbase + (incl - t);
 #pragma unroll
-    for (int e = 0; e < kSeg2; ++e) {
-      run += r[e];
-      if (j < 0 && run > target) j = e;
-    }
-    if (j < 0) j = last_pos;  // rounding: the segment sum crossed but no element did
-    if (j >= 0) atomicMin(&s_hit, (threadIdx.x << 8) | j);
-  }
-  if (last_pos >= 0) atomicMax(&s_last_pos, base + last_pos);
-  __syncthreads();
-  int res;
-  if (s_hit != INT_MAX) {
-    res = c * kChunk2 + (s_hit >> 8) * kSeg2 + (s_hit & 0xFF);
-  } else {
-    res = s_last_pos;
-  }
-  __syncthreads();
-  return res;
+  for (int e = 0; e < 4; ++e) v[e] += excl;
+  excl_out = excl;
+  __syncthreads();  // s_w is reused by the next call
+  return total;
 }
 
 // Pass 2: per (sequence, group of kPass2Chunks chunks of 2048) residual mass of row n, one sum per
-// chunk; the last CTA of a sequence walks the chunk sums in index order and selects the token with
-// the inverse CDF.
+// warp segment of 256 elements; the last CTA of a sequence scans the segment sums in index order
+// (a block scan), finds the segment where the running sum passes u R, and one warp rescans those 256
+// elements for the token (the inverse CDF).
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads, 8) sample_pass2_kernel(
     const uint16_t* __restrict__ Lt, const uint16_t* __restrict__ Ld,
@@ -585,15 +563,16 @@ __global__ void __launch_bounds__(kThreads, 8) sample_pass2_kernel(
   rp.q = rp.bonus ? nullptr : Ld + (int64_t(b) * gamma + n) * V;
   rp.md = __int_as_float(r0.w);
   rp.inv_sd = __int_as_float(r1.x);
-  __shared__ float s_ps[kPass2Chunks][kThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nseg = chunks2 * kSegsPerChunk;
+  float* segs = ws.part2 + int64_t(b) * nseg;
   for (int g = g0; g < groups; g += ctas_per_seq) {
     const int c0 = g * kPass2Chunks;
     float r[kPass2Chunks][kSeg2];
 #pragma unroll
     for (int k = 0; k < kPass2Chunks; ++k) {
       if (c0 + k < chunks2) {
-        seg_values<kVec>(rp, V, c0 + k, r[k]);
+        seg_values_at<kVec>(rp, V, (c0 + k) * kChunk2 + threadIdx.x * kSeg2, r[k]);
       } else {
 #pragma unroll
         for (int e = 0; e < kSeg2; ++e) r[k][e] = 0.0f;
@@ -601,23 +580,11 @@ __global__ void __launch_bounds__(kThreads, 8) sample_pass2_kernel(
     }
 #pragma unroll
     for (int k = 0; k < kPass2Chunks; ++k) {
-      float v = 0.0f;
-#pragma unroll
-      for (int e = 0; e < kSeg2; ++e) v += r[k][e];
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-      if (lane == 0) s_ps[k][warp] = v;
+      const float v = warp_segment_sum(r[k]);
+      if (lane == 0 && c0 + k < chunks2) segs[(c0 + k) * kSegsPerChunk + warp] = v;
     }
-    __syncthreads();
-    if (threadIdx.x < kPass2Chunks && c0 + static_cast<int>(threadIdx.x) < chunks2) {
-      float t = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kThreads / 32; ++w) t += s_ps[threadIdx.x][w];
-      ws.part2[int64_t(b) * chunks2 + c0 + threadIdx.x] = t;
-      __threadfence();  // each writer publishes its chunk sum before the ticket below
-    }
-    __syncthreads();  // s_ps is reused by the next group
   }
+  __threadfence();  // every segment sum is published before the ticket below
 
   __shared__ bool s_last;
   __syncthreads();
@@ -629,71 +596,129 @@ __global__ void __launch_bounds__(kThreads, 8) sample_pass2_kernel(
   if (!s_last) return;
   __threadfence();
 
-  constexpr int kParts = 1024;
-  __shared__ float s_parts[kParts];
-  __shared__ float s_R;
-  __shared__ int s_c, s_fallback;
-  __shared__ float s_before;
+  __shared__ float s_R, s_before;
+  __shared__ int s_found, s_last_pos;
   const float u = u_res[int64_t(b) * G1 + n];
   for (int attempt = 0; attempt < 2; ++attempt) {
     if (attempt == 1) {
       // The residual has no mass (p == q in fp32): draw from p instead.
       rp.bonus = true;
       for (int cc = 0; cc < chunks2; ++cc) {
-        const float s = chunk_sum<kVec>(rp, V, cc);
-        if (threadIdx.x == 0) ws.part2[int64_t(b) * chunks2 + cc] = s;
+        float r[kSeg2];
+        seg_values_at<kVec>(rp, V, cc * kChunk2 + threadIdx.x * kSeg2, r);
+        const float v = warp_segment_sum(r);
+        if (lane == 0) segs[cc * kSegsPerChunk + warp] = v;
       }
+      __threadfence();
       __syncthreads();
     }
-    // Chunk sums are staged in shared memory by all threads (one tile of kParts at a time) and
-    // walked in chunk order by thread 0: R first, then the chunk where the running sum passes u*R.
-    float R = 0.0f, cum = 0.0f, before = 0.0f;
-    int found = -1, last_pos = -1;
+    // Segment sums in tiles of 4 per thread: R first (pass 0), then the first segment whose running
+    // sum passes u R (pass 1), with the running sum before it; the last segment with mass as the
+    // fallback when rounding leaves no crossing.
+    if (threadIdx.x == 0) {
+      s_found = INT_MAX;
+      s_last_pos = -1;
+    }
+    float R = 0.0f;
     for (int pass = 0; pass < 2; ++pass) {
       const float target = u * R;
-      for (int t0 = 0; t0 < chunks2; t0 += kParts) {
-        const int cnt = min(kParts, chunks2 - t0);
-        for (int i = threadIdx.x; i < cnt; i += kThreads) s_parts[i] = __ldcg(ws.part2 + int64_t(b) * chunks2 + t0 + i);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          for (int i = 0; i < cnt; ++i) {
-            const float rc2 = s_parts[i];
-            if (pass == 0) {
-              R += rc2;
-            } else {
-              if (rc2 > 0.0f) last_pos = t0 + i;
-              if (found < 0 && cum + rc2 > target) {
-                found = t0 + i;
-                before = cum;
-              }
-              cum += rc2;
-            }
-          }
+      float carry = 0.0f;
+      for (int t0 = 0; t0 < nseg; t0 += 4 * kThreads) {
+        float v[4], raw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = t0 + threadIdx.x * 4 + e;
+          raw[e] = i < nseg ? __ldcg(segs + i) : 0.0f;
+          v[e] = raw[e];
         }
-        __syncthreads();
+        float excl = 0.0f;
+        const float tot = block_incl_scan4(v, excl);
+        if (pass == 1) {
+          // the prefixes rise with i (r >= 0), so the crossing is a thread's first e past the target
+          // whose previous prefix is not; one atomic per warp for the lowest such lane, and likewise
+          // for the last segment with mass
+          int first = -1, lastp = -1;
+          float prev = carry + excl, before = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = t0 + threadIdx.x * 4 + e;
+            if (i < nseg && first < 0 && carry + v[e] > target) {
+              first = i;
+              before = prev;
+            }
+            if (i < nseg && raw[e] > 0.0f) lastp = i;
+            prev = carry + v[e];
+          }
+          const unsigned int fm = __ballot_sync(0xFFFFFFFFu, first >= 0);
+          if (fm != 0u && lane == __ffs(fm) - 1) atomicMin(&s_found, first);
+          const unsigned int lm = __ballot_sync(0xFFFFFFFFu, lastp >= 0);
+          if (lm != 0u && lane == 31 - __clz(lm)) atomicMax(&s_last_pos, lastp);
+          __syncthreads();
+          if (first >= 0 && first == s_found) s_before = before;
+          __syncthreads();
+          if (s_found != INT_MAX) break;  // (uniform: read after the barrier)
+        }
+        carry += tot;
       }
-      if (threadIdx.x == 0 && pass == 0) s_R = R;
-      __syncthreads();
-      R = s_R;
+      if (pass == 0) R = carry;
     }
-    if (threadIdx.x == 0) {
-      s_fallback = found < 0;
-      s_c = found < 0 ? last_pos : found;
-      s_before = before;
-    }
+    if (threadIdx.x == 0) s_R = R;
     __syncthreads();
-    if (s_R > 0.0f || attempt == 1) break;
+    if (R > 0.0f || attempt == 1) break;
     __syncthreads();
   }
-  const int cs = s_c;
-  int j = -1;
-  if (cs >= 0) {
-    const float tgt = s_fallback ? INFINITY : u * s_R - s_before;
-    j = chunk_select<kVec>(rp, V, cs, tgt);
-  }
-  if (threadIdx.x == 0) {
-    out_tok[int64_t(b) * G1 + n] = j;
-    ws.cnt2[b] = 0;
+  // one warp rescans the chosen segment: the first element whose running sum (from the segment's
+  // start) passes u R - (mass before it); if rounding leaves none, the segment's last element with
+  // r > 0 (the row's last such element when no segment crossed: target infinity)
+  if (warp == 0) {
+    const bool crossed = s_found != INT_MAX;
+    const int seg = crossed ? s_found : s_last_pos;
+    int j = -1;
+    if (seg >= 0) {
+      const float tgt = crossed ? u * s_R - s_before : INFINITY;
+      const int c = seg / kSegsPerChunk, w = seg - c * kSegsPerChunk;
+      const int i0 = c * kChunk2 + (w * 32 + lane) * kSeg2;
+      float r[kSeg2];
+      seg_values_at<kVec>(rp, V, i0, r);
+      float sum = 0.0f;
+      int last_e = -1;
+#pragma unroll
+      for (int e = 0; e < kSeg2; ++e) {
+        sum += r[e];
+        if (r[e] > 0.0f) last_e = e;
+      }
+      float incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      int hit = -1;
+      if (incl > tgt) {
+        float run = incl - sum;
+#pragma unroll
+        for (int e = 0; e < kSeg2; ++e) {
+          run += r[e];
+          if (hit < 0 && run > tgt) hit = e;
+        }
+        if (hit < 0) hit = last_e;  // rounding: the lane's sum crossed but no element did
+      }
+      const unsigned int hits = __ballot_sync(0xFFFFFFFFu, hit >= 0);
+      if (hits != 0u) {
+        const int src = __ffs(hits) - 1;
+        j = __shfl_sync(0xFFFFFFFFu, i0 + hit, src);
+      } else {
+        const unsigned int pos = __ballot_sync(0xFFFFFFFFu, last_e >= 0);
+        if (pos != 0u) {
+          const int src = 31 - __clz(pos);
+          j = __shfl_sync(0xFFFFFFFFu, i0 + last_e, src);
+        }
+      }
+    }
+    if (lane == 0) {
+      out_tok[int64_t(b) * G1 + n] = j;
+      ws.cnt2[b] = 0;
+    }
   }
 }
 

@@ -193,6 +193,19 @@ def test_expected_tokens_on_gpu(q):
     assert np.abs(got["accept_prob"] - alpha_eff).max() < PROB_TOL
 
 
+def test_sample_long_vocab_two_scan_tiles(q):
+    # V = 300000: 147 chunks of 2048, 1176 warp segments, so the last CTA's scan of the segment sums
+    # runs over two tiles of 1024; u_res near 0, mid, near 1 put the crossing in either tile
+    B, gamma, V = 4, 2, 300000
+    inp = syn.verify_inputs(B, gamma, V, 0.5, workload_id=12, sampling=True)
+    for b, u in enumerate((0.3, 0.95, 0.999, 0.01)):
+        inp["u_res"][b, :] = np.float32(u)
+    got = run_sample(q, inp)
+    ref = oracle.verify_sample(inp["tgt"], inp["drf"], inp["d"], inp["u_acc"], inp["u_res"])
+    exact = compare_sample(got, ref, inp["u_acc"])
+    assert exact >= B - 1
+
+
 def test_sample_parity_largest_sweep_cell(q):
     # the largest cell of the sampling sweep: 64 sequences, gamma = 7, V = 152064 (1920 CTAs in pass 1,
     # two vocabulary chunks per row)

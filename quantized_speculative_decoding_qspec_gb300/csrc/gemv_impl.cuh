@@ -229,10 +229,12 @@ struct Parts {
 // would push the 16- and 32-slot kernels past their 128).
 constexpr int kPartsMaxMT = 4;
 
-// The part that tile belongs to (the last part for tiles past the end).
-template <int MT>
+// The part that tile belongs to (the last part for tiles past the end).  MP: the launch may have
+// several parts (single-part launches skip the lookup: measured, the W4A16 kernels of up to 4 token
+// slots run 5-9% faster without it; the quantised modes keep it, which measured no slower).
+template <int MT, bool MP>
 __device__ __forceinline__ int part_of(const Parts& p, int tile) {
-  if constexpr (MT > kPartsMaxMT) {
+  if constexpr (MT > kPartsMaxMT || !MP) {
     return 0;
   } else {
     int s = 0;
@@ -242,7 +244,7 @@ __device__ __forceinline__ int part_of(const Parts& p, int tile) {
   }
 }
 
-template <int QB, bool ACC, int MT, int D, bool CHUNK>
+template <int QB, bool ACC, int MT, int D, bool CHUNK, bool MP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const __grid_constant__ Parts parts, int M, int K, int KS,
                 int KC_arg, int8_t* __restrict__ xq_out,
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool f_vlo = false, f_vhi = false;
   int f_tile = tile0, f_i = 0;
   auto point = [&]() {
-    const int ps = part_of<MT>(parts, f_tile);
+    const int ps = part_of<MT, MP>(parts, f_tile);
     const int n_lo = (f_tile - (ps ? parts.tile_end[ps - 1] : 0)) * 16 + g, n_hi = n_lo + 8;
     const int Np = parts.N[ps];
     const uint8_t* Wp = parts.Wp[ps];
@@ -619,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (store) {
-      const int ps = part_of<MT>(parts, tile);
+      const int ps = part_of<MT, MP>(parts, tile);
       const int N = parts.N[ps];
       uint16_t* y = parts.y[ps];
       const int n_lo = (tile - (ps ? parts.tile_end[ps - 1] : 0)) * 16 + g, n_hi = n_lo + 8;
@@ -682,17 +684,22 @@ inline bool pick_ks(long long tiles, int Gc, int KC, int D, int* best_ks, int* b
 // Groups in flight per warp for MT token slots (the weights wait in 8 registers per group and lane).
 constexpr int depth_of(int MT) { return MT <= 16 ? 4 : 1; }
 
-// K chunks for up to eight token slots: besides making the staged activations fit, chunks let a
+// K chunks for up to sixteen token slots: besides making the staged activations fit, chunks let a
 // layer with few row tiles but long K keep more warps streaming (each warp's serial share is what
-// a latency-bound stream pays for).  Among the chunk counts that fit, the one with the fewest
-// groups per warp plus the fixup of split tiles (about 4 groups' time + a quarter per chunk, ties
-// to fewer chunks); e.g. the Llama-3-8B down layer (256 row tiles, 112 groups) at one token takes
-// seven chunks of 16 groups instead of one chunk in which only 1024 of the 2432 warps stream (28
-// groups each).  Sixteen and 32 slots keep the fewest chunks that fit.  Deterministic in (MT, N, G, SM count), so
-// the workspace size and the launch agree.
+// a latency-bound stream pays for), and they shrink what every CTA stages: all CTAs read the same
+// x, so staging 16 tokens' 128 KB per CTA takes ~5 us.  Among the chunk counts that fit, the one
+// with the fewest groups per warp plus the fixup of split tiles (about 4 groups' time + a quarter
+// per chunk) plus the staging (0.005 per staged (group, token slot): fitted to Llama-2-70B layers
+// at 4 to 16 tokens), ties to fewer chunks.  E.g. the Llama-3-8B down layer (256 row tiles, 112
+// groups) at one token takes seven chunks of 16 groups instead of one chunk in which only 1024 of
+// the 2432 warps stream (28 groups each); at 16 tokens Llama-2-70B gate_up takes four chunks
+// instead of two (46.3 -> 43.2 us), q/o four (22.7 -> 20.3 us), down eight instead of seven (51.1
+// -> 45.4 us), and down at 4 tokens four instead of two (39.6 -> 37.4 us).  32 slots keep the
+// fewest chunks that fit.  Deterministic in (MT, N, G, SM count), so the workspace size and the
+// launch agree.
 inline int plan_kc(int MT, int N, int G) {
   const int kc_min = pick_kc(MT, G);
-  if (kc_min == 0 || MT > 8) return kc_min;
+  if (kc_min == 0 || MT > 16) return kc_min;
   const long long tiles = (static_cast<long long>(N) + 15) / 16;
   const int D = depth_of(MT);
   int best_kc = kc_min;
@@ -702,7 +709,7 @@ inline int plan_kc(int MT, int N, int G) {
     int ks = 1, grid = 1;
     long long c = 0;
     if (!pick_ks(tiles, G / kc, kc, D, &ks, &grid, &c)) continue;
-    const double cost = static_cast<double>(c) + (kc > 1 ? 4.0 + 0.25 * kc : 0.0);
+    const double cost = static_cast<double>(c) + (kc > 1 ? 4.0 + 0.25 * kc : 0.0) + 0.005 * (G / kc) * MT;
     if (best < 0.0 || cost < best) {
       best = cost;
       best_kc = kc;
@@ -734,7 +741,12 @@ template <int QB, bool ACC, int MT, int D>
 qspec_status launch_d(const uint16_t* x, const Parts& P, int M, int N, int K,
                       Outs o, int best_ks, int KC, int best_grid, cudaStream_t stream) {
   const size_t smem = smem_bytes(MT, K / kGroup / KC);
-  auto kern = KC > 1 ? gemv_kernel<QB, ACC, MT, D, true> : gemv_kernel<QB, ACC, MT, D, false>;
+  // the part lookup is compiled in where several parts can reach it (see part_of)
+  constexpr bool kMP = MT <= kPartsMaxMT && QB != 0;
+  auto kern = KC > 1 ? gemv_kernel<QB, ACC, MT, D, true, kMP> : gemv_kernel<QB, ACC, MT, D, false, kMP>;
+  if constexpr (MT <= kPartsMaxMT && QB == 0) {
+    if (P.n > 1) kern = KC > 1 ? gemv_kernel<QB, ACC, MT, D, true, true> : gemv_kernel<QB, ACC, MT, D, false, true>;
+  }
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return QSPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};

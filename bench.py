@@ -742,35 +742,51 @@ def profile_case(spec, reps):
               else (lambda: q.qspec_verify_sample(tgt, drf, d, ua, ur, n, o, ws)))
         nbytes = verify_bytes(Bc, gc, Vc, parts[1] != "greedy")
     else:
-        # a layer (one linear) or a group of the step (one grouped launch, e.g. qkv:a4:1)
+        # a layer (one linear) or a group of the step (one grouped launch, e.g. qkv:a4:1), or a
+        # Llama-2-70B layer of the linear sweep (70b_gate_up:a16:16)
         name, mode, M = parts[0], parts[1], int(parts[2])
-        groups = dict(GROUPS)
-        grouped = name in groups and M <= 4  # the grouped launch serves up to 4 tokens
-        members = groups[name] if grouped else (name,)
-        K = SHAPE[members[0]][1]
-        lead = [l[0] for l in LAYERS].index(members[0])
-        x = bf(syn.activations(M, K, 1, step=10 * lead))
-        mats = []
-        for m in members:
-            li = [l[0] for l in LAYERS].index(m)
-            N = SHAPE[m][0]
-            W = bf(syn.weights(N, K, 1, layer=li))
+        if name.startswith("70b_"):
+            li = [l[0] for l in LLAMA70B].index(name[4:])
+            _, N, K = LLAMA70B[li]
+            W = bf(syn.weights(N, K, 3, layer=li))
             Wp = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
             S = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
             q.qspec_pack_weights(W, Wp, S)
             del W
-            mats.append((Wp, S, torch.empty(M, N, dtype=torch.bfloat16, device=dev)))
-        abits = {"a4": 4, "a8": 8, "a16": 16}[mode]
-        if grouped:
-            ws = q.new_linear_group_workspace(M, [SHAPE[m][0] for m in members], K, device=dev)
-            fn = q.LinearGroup(abits, x, mats, ws).run
-            nbytes = group_bytes(M, members)
-        else:
-            Wp, S, y = mats[0]
-            ws = q.new_linear_workspace(M, SHAPE[name][0], K, device=dev)
-            f = {4: q.qspec_linear_w4a4, 8: q.qspec_linear_w4a8, 16: q.qspec_linear_w4a16}[abits]
+            x = bf(syn.activations(M, K, 3, step=M))
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            ws = q.new_linear_workspace(M, N, K, device=dev)
+            f = {"a4": q.qspec_linear_w4a4, "a8": q.qspec_linear_w4a8, "a16": q.qspec_linear_w4a16}[mode]
             fn = lambda: f(x, Wp, S, y, ws)
-            nbytes = linear_bytes(M, SHAPE[name][0], K)
+            nbytes = linear_bytes(M, N, K)
+        else:
+            groups = dict(GROUPS)
+            grouped = name in groups and M <= 4  # the grouped launch serves up to 4 tokens
+            members = groups[name] if grouped else (name,)
+            K = SHAPE[members[0]][1]
+            lead = [l[0] for l in LAYERS].index(members[0])
+            x = bf(syn.activations(M, K, 1, step=10 * lead))
+            mats = []
+            for m in members:
+                li = [l[0] for l in LAYERS].index(m)
+                N = SHAPE[m][0]
+                W = bf(syn.weights(N, K, 1, layer=li))
+                Wp = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+                S = torch.empty(N, K // 128, dtype=torch.float16, device=dev)
+                q.qspec_pack_weights(W, Wp, S)
+                del W
+                mats.append((Wp, S, torch.empty(M, N, dtype=torch.bfloat16, device=dev)))
+            abits = {"a4": 4, "a8": 8, "a16": 16}[mode]
+            if grouped:
+                ws = q.new_linear_group_workspace(M, [SHAPE[m][0] for m in members], K, device=dev)
+                fn = q.LinearGroup(abits, x, mats, ws).run
+                nbytes = group_bytes(M, members)
+            else:
+                Wp, S, y = mats[0]
+                ws = q.new_linear_workspace(M, SHAPE[name][0], K, device=dev)
+                f = {4: q.qspec_linear_w4a4, 8: q.qspec_linear_w4a8, 16: q.qspec_linear_w4a16}[abits]
+                fn = lambda: f(x, Wp, S, y, ws)
+                nbytes = linear_bytes(M, SHAPE[name][0], K)
     for _ in range(reps):
         fn()
     torch.cuda.synchronize()

@@ -217,9 +217,10 @@ LLAMA70B_TC = {"gate_up": (28672, 8192, 2), "down": (8192, 28672, 3)}  # N, K, l
 
 @pytest.mark.parametrize("name", list(LLAMA70B_TC))
 def test_fullsize_70b_tensor_core_sampled_rows(q, name):
-    # the M = 64, 128, 256 cells of the Llama-2-70B sweep, both modes, on sampled output rows (the
-    # first and last rows always among them); every token tile and K contributor of a sampled row
-    # takes part in its value
+    # the M = 4, 8, 16 (GEMV with K chunks: four or eight at 16 tokens) and 64, 128, 256 (tensor-core
+    # kernels) cells of the Llama-2-70B sweep, both modes, on sampled output rows (the first and last
+    # rows always among them); every token tile and K contributor of a sampled row takes part in its
+    # value; W4A4 both through the checking path (exact group sums out) and the production one
     N, K, li = LLAMA70B_TC[name]
     W = syn.weights(N, K, 3, layer=li)
     Wp, S = packed_dev(q, W)
@@ -229,7 +230,7 @@ def test_fullsize_70b_tensor_core_sampled_rows(q, name):
     assert np.array_equal(Wp.cpu().numpy()[rows], Wp_ref)
     assert np.array_equal(S.cpu().numpy()[rows].view(np.uint16), S_ref.view(np.uint16))
     rows_dev = torch.from_numpy(rows).to(DEV)
-    for M in (64, 128, 256):
+    for M in (4, 8, 16, 64, 128, 256):
         X = syn.activations(M, K, 3, step=M)
         x = bf16_dev(X)
         ws = q.new_linear_workspace(M, N, K)
@@ -248,6 +249,9 @@ def test_fullsize_70b_tensor_core_sampled_rows(q, name):
         ulp = bf16_ulp_distance(bf16_host_bits(y4[:, rows_dev]), oracle.f64_to_bf16_bits(r["y"]))
         assert ulp.max() <= 1, f"W4A4 {name} M={M}: max ulp {ulp.max()}"
         del acc
+        q.qspec_linear_w4a4(x, Wp, S, y4, ws)
+        ulp = bf16_ulp_distance(bf16_host_bits(y4[:, rows_dev]), oracle.f64_to_bf16_bits(r["y"]))
+        assert ulp.max() <= 1, f"W4A4 {name} M={M} (no sums out): max ulp {ulp.max()}"
         q.qspec_check_status()
 
 

@@ -409,6 +409,23 @@ qspec_status qspec_select_tokens(const uint16_t* logits, int32_t R, int32_t V, c
                                  qspec_stream_t stream);
 
 /*
+ * qspec_copy -- move `bytes` from src to dst with one kernel on the SMs (no copy engine).
+ *
+ * For a decode step's small per-step transfers (a few tokens' activations in, the verify results
+ * out), where a copy-engine transfer is mostly fixed latency and the kernel after it cannot begin
+ * until it ends.  Either pointer may be device memory or pinned (page-locked, host-allocated or
+ * registered) host memory, which the kernel reads or writes through its device mapping over the
+ * host link; pageable host memory is refused.  Launched with programmatic dependent launch: the
+ * next kernel's prologue overlaps the copy; the copy writes dst only after the previous kernel in
+ * the stream has finished, and reads a device-memory src only then too (a host src earlier).
+ *
+ *   dst, src  16-byte aligned, not overlapping; bytes > 0, a multiple of 16.
+ * Returns QSPEC_ERR_INVALID_ARG for a null pointer, zero bytes or memory the GPU cannot address,
+ * QSPEC_ERR_MISALIGNED for an address or size that is not a multiple of 16.
+ */
+qspec_status qspec_copy(void* dst, const void* src, size_t bytes, qspec_stream_t stream);
+
+/*
  * qspec_check_status -- synchronises `stream`, then reports (and clears) the error words that the
  * kernels set on the device: the verify workspace's word when `ws` is not NULL, and the library's
  * own words for the linear and decode-loop kernels of the current device.  QSPEC_ERR_TIMEOUT if a

@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libqspec.so")
 
 UNITS = ["pack.cu", "linear.cu", "linear_tc.cu", "gemv.cu", "gemv_a16.cu", "gemv_a4.cu", "gemv_a8.cu",
          "gemv_codes.cu", "quant.cu", "verify.cu", "decode.cu", "api.cu", "pass.cu", "pass_a16.cu", "pass_a4.cu",
-         "pass_a8.cu", "linear_dq.cu", "dq_kernels.cu"]
+         "pass_a8.cu", "linear_dq.cu", "dq_kernels.cu", "copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -53,6 +53,7 @@ SIGNATURES = {
     "qspec_linear_pass_workspace_size": (ctypes.c_size_t, []),
     "qspec_linear_pass": (ctypes.c_int, [_I32, _I64, _P, _I32, _P, ctypes.c_size_t, _P]),
     "qspec_check_status": (ctypes.c_int, [_P, _P]),
+    "qspec_copy": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
     "qspec_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -416,6 +417,25 @@ def qspec_verify_tree_greedy(tgt_logits, tree_tok, tree_parent, accept_len, out_
            load().qspec_verify_tree_greedy(_ptr(tgt_logits), _ptr(tree_tok), _ptr(tree_parent), B, R - 1, V,
                                            _ptr(accept_len), _ptr(out_tok), _ptr(accept_nodes), _ptr(ws),
                                            ws.numel(), _stream(stream)))
+
+
+def _ptr_any(t, name):
+    """Pointer of a contiguous device tensor or pinned host tensor (qspec_copy's operands)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must live on the GPU or in pinned host memory")
+    return t.data_ptr()
+
+
+def qspec_copy(dst, src, stream=None):
+    """Copy src into dst (same number of bytes, device or pinned host tensors) with one kernel."""
+    nb = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nb:
+        raise ValueError(f"dst holds {dst.numel() * dst.element_size()} bytes, src {nb}")
+    _check("qspec_copy", load().qspec_copy(_ptr_any(dst, "dst"), _ptr_any(src, "src"), nb, _stream(stream)))
 
 
 def qspec_check_status(ws=None, stream=None):

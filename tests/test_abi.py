@@ -232,3 +232,14 @@ def test_linear_group_argument_checks(lib):
     assert f(16, FAKE, 1, 4096, qkv, 3, None, W, None) == 4      # no workspace
     assert f(16, FAKE, 1, 4096, qkv, 3, FAKE + 8, W, None) == 3  # misaligned workspace
     assert f(16, FAKE, 1, 4096, qkv, 3, FAKE, W - 1, None) == 4  # workspace too small
+
+
+def test_copy_argument_checks(lib):
+    # refused on the host before any CUDA call: null pointers, zero bytes, 16-byte alignment of both
+    # addresses and of the size
+    assert lib.qspec_copy(None, ctypes.c_void_p(64), 64, None) == 1
+    assert lib.qspec_copy(ctypes.c_void_p(64), None, 64, None) == 1
+    assert lib.qspec_copy(ctypes.c_void_p(64), ctypes.c_void_p(128), 0, None) == 1
+    assert lib.qspec_copy(ctypes.c_void_p(72), ctypes.c_void_p(128), 64, None) == 3
+    assert lib.qspec_copy(ctypes.c_void_p(64), ctypes.c_void_p(136), 64, None) == 3
+    assert lib.qspec_copy(ctypes.c_void_p(64), ctypes.c_void_p(128), 40, None) == 3

@@ -59,11 +59,12 @@ const void* device_view(const void* p, bool* on_host) {
     case cudaMemoryTypeManaged:
       return p;
     case cudaMemoryTypeHost:
-      if (!a.devicePointer) return nullptr;
+      if (!a.devicePointer || !a.hostPointer) return nullptr;
       *on_host = true;
-      // the mapping of a pointer inside the allocation: the same offset from its device view
+      // the device view of p: the same offset from the device pointer as p from the host pointer
+      // (the two are equal under unified addressing)
       return static_cast<const char*>(a.devicePointer) +
-             (static_cast<const char*>(p) - static_cast<const char*>(a.hostPointer ? a.hostPointer : p));
+             (static_cast<const char*>(p) - static_cast<const char*>(a.hostPointer));
     default:
       return nullptr;
   }

@@ -290,3 +290,43 @@ def test_workspace_of_another_shape_is_refused(q):
     q.qspec_check_status()
     r = oracle.linear_w4a4(X1, Wp_ref, S_ref)
     assert bf16_ulp_distance(bf16_host_bits(y1), oracle.f64_to_bf16_bits(r["y"])).max() <= 1
+
+
+# ---- seeded random shapes across the three kernels (the GEMV up to 32 tokens, the exact-code
+# tcgen05 kernel above it, the dequantising one for W4A16 from 65 tokens) and the K-chunk planner
+
+def _random_shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 11, 16, 23, 32, 40, 64, 65, 100, 128, 200, 256]))
+        N = int(rng.integers(1, 400)) * 8
+        K = int(rng.integers(1, 120)) * 128
+        out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", _random_shapes(24, 2024))
+def test_linear_random_shapes(q, M, N, K):
+    W = syn.weights(N, K, 5, layer=N % 97)
+    X = syn.activations(M, K, 5, step=M + K)
+    Wp, S = packed_dev(q, W)
+    rng = np.random.default_rng(M * 7 + N + K)
+    rows = np.unique(np.concatenate([[0, N - 1], rng.choice(N, size=min(N, 48), replace=False)]))
+    Wp_ref, S_ref = oracle.pack_weights(W[rows])
+    rows_dev = torch.from_numpy(rows).to(DEV)
+    x = bf16_dev(X)
+    ws = q.new_linear_workspace(M, N, K)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    q.qspec_linear_w4a16(x, Wp, S, y, ws)
+    err = rel_fro(bf16_host_f64(y[:, rows_dev]), oracle.linear_w4a16(X, Wp_ref, S_ref))
+    assert err <= W4A16_TOL, f"W4A16 M={M} N={N} K={K}: rel err {err}"
+    r = oracle.linear_w4a4(X, Wp_ref, S_ref)
+    for f in (q.qspec_linear_w4a4, q.qspec_linear_w4a8):
+        if f is q.qspec_linear_w4a8:
+            r = oracle.linear_w4a8(X, Wp_ref, S_ref)
+        yq = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+        f(x, Wp, S, yq, ws)
+        ulp = bf16_ulp_distance(bf16_host_bits(yq[:, rows_dev]), oracle.f64_to_bf16_bits(r["y"]))
+        assert ulp.max() <= 1, f"{f.__name__} M={M} N={N} K={K}: max ulp {ulp.max()}"
+    q.qspec_check_status()
